@@ -1,0 +1,115 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that a pin catches each.
+
+Each mutation replaces one oracle function with a subtly wrong variant; the
+test passes when at least one ``pin_*`` of ``tests/oracle_pins.py`` fails
+against the mutated oracle.
+"""
+import numpy as np
+import pytest
+
+from oracle import mla_ref
+from tests import oracle_pins
+
+_orig = {name: getattr(mla_ref, name) for name in dir(mla_ref) if not name.startswith("_")}
+
+
+def _rope_with(sign=1.0, freq_step=2, halves=False):
+    def rope(x, pos, base):
+        x = np.asarray(x, np.float64)
+        d = x.shape[-1]
+        inv = 1.0 / (float(base) ** (np.arange(0, d // 2) * freq_step / d))
+        theta = np.asarray(pos, np.float64)[..., None] * inv
+        c, s = np.cos(theta), sign * np.sin(theta)
+        if halves:
+            a, b = x[..., : d // 2], x[..., d // 2:]
+        else:
+            a, b = x[..., 0::2], x[..., 1::2]
+        shape = np.broadcast_shapes(x.shape, theta.shape[:-1] + (d,))
+        out = np.empty(shape)
+        if halves:
+            out[..., : d // 2] = a * c - b * s
+            out[..., d // 2:] = b * c + a * s
+        else:
+            out[..., 0::2] = a * c - b * s
+            out[..., 1::2] = b * c + a * s
+        return out
+    return rope
+
+
+def _absorbed_latent_no_rope(q_abs, c_kv, k_r_rot, scale):
+    d_c = c_kv.shape[1]
+    s = scale * (q_abs[:, :d_c] @ np.asarray(c_kv, np.float64).T)
+    p = _orig["softmax"](s, axis=1)
+    m = np.max(s, axis=1)
+    return p @ c_kv, m + np.log(np.sum(np.exp(s - m[:, None]), axis=1))
+
+
+def _absorb_query_shifted(q, w_uk, pos_q, base):
+    return _orig["absorb_query"](q, w_uk, pos_q + 1, base)
+
+
+def _naive_without_rope_key(q, c_kv, k_r_rot, w_uk, w_uv, pos_q, scale, base):
+    return _orig["naive_decode"](q, c_kv, np.zeros_like(np.asarray(k_r_rot, np.float64)),
+                                 w_uk, w_uv, pos_q, scale, base)
+
+
+def _softmax_unnormalised(s, axis=-1):
+    s = np.asarray(s, np.float64)
+    return np.exp(s - np.max(s, axis=axis, keepdims=True))
+
+
+def _causal_unmasked(x, w_dkv, w_q, w_uk, w_uv, scale, base):
+    n_h, d_nope, d_c = w_uk.shape
+    c_kv, k_r, q = _orig["project_inputs"](x, w_dkv, w_q, n_h, d_c)
+    L = c_kv.shape[0]
+    pos = np.arange(L)
+    k_r_rot = mla_ref.rope(k_r, pos, base)
+    q_pe = mla_ref.rope(q[:, :, d_nope:], pos[:, None], base)
+    out = np.empty((L, n_h, w_uv.shape[1]))
+    for h in range(n_h):
+        k = np.concatenate([c_kv @ w_uk[h].T, k_r_rot], axis=1)
+        v = c_kv @ w_uv[h].T
+        qh = np.concatenate([q[:, h, :d_nope], q_pe[:, h]], axis=1)
+        out[:, h] = _orig["softmax"](scale * (qh @ k.T), axis=1) @ v
+    return out
+
+
+def _split_linear_merge(q_abs, c_kv, k_r_rot, scale, bounds):
+    parts = [_orig["absorbed_latent"](q_abs, c_kv[a:b], k_r_rot[a:b], scale)
+             for a, b in zip(bounds[:-1], bounds[1:])]
+    w = np.stack([np.exp(p[1]) for p in parts])
+    w = w / w.sum(0)
+    lens = np.array([b - a for a, b in zip(bounds[:-1], bounds[1:])], float)
+    w = (w.T * lens / lens.mean()).T            # wrong: weights chunks by length too
+    return sum(w[j][:, None] * parts[j][0] for j in range(len(parts))), np.log(np.exp(np.stack([p[1] for p in parts])).sum(0))
+
+
+MUTATIONS = {
+    "rope_rotates_backwards": ("rope", _rope_with(sign=-1.0)),
+    "rope_frequency_step_1": ("rope", _rope_with(freq_step=1)),
+    "rope_pairs_by_halves": ("rope", _rope_with(halves=True)),
+    "scale_without_rope_width": ("default_scale", lambda d_nope, d_rope: 1.0 / np.sqrt(float(d_nope))),
+    "absorbed_drops_rope_score": ("absorbed_latent", _absorbed_latent_no_rope),
+    "query_position_off_by_one": ("absorb_query", _absorb_query_shifted),
+    "naive_drops_rope_key": ("naive_decode", _naive_without_rope_key),
+    "softmax_unnormalised": ("softmax", _softmax_unnormalised),
+    "causal_mask_missing": ("causal_forward_naive", _causal_unmasked),
+    "cache_bytes_without_rope": ("absorb_cache_bytes", lambda t, d_c, d_r, e: int(t) * int(d_c) * int(e)),
+    "naive_bytes_without_values": ("naive_cache_bytes", lambda t, n, dn, dr, dv, e: int(t) * int(n) * (int(dn) + int(dr)) * int(e)),
+    "read_bytes_times_heads": ("decode_kv_read_bytes", lambda B, s, d_c, d_r, e: _orig["decode_kv_read_bytes"](B, s, d_c, d_r, e) * 2),
+    "split_merge_weighted_by_length": ("split_latent", _split_linear_merge),
+    "up_projection_skipped": ("up_project", lambda o_lat, w_uv: o_lat[:, : w_uv.shape[1]]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_some_pin_catches(name, monkeypatch):
+    attr, fn = MUTATIONS[name]
+    monkeypatch.setattr(mla_ref, attr, fn)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(mla_ref)
+        except Exception as e:     # an assertion or a shape error both mean "caught"
+            caught.append(pin.__name__)
+    assert caught, f"mutation {name} passed every pin"
