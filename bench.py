@@ -1,0 +1,400 @@
+"""Benchmark of one absorbed-MLA decode step on a GB300 (prints ONE JSON line on rank 0).
+
+A step is the whole hot path over one batch: mla_kv_append of each sequence's
+new row, then mla_decode (planner, query absorption, split-KV flash decode over
+the paged latent cache, log-sum-exp combine + W_UV up-projection).
+
+Default workload: DeepSeek-V3 shapes, B = 64 sequences of 4096 tokens, bf16
+cache (n_h = 128, d_c = 512, d_rope = 64).  Metric: latent-KV GB/s, i.e. the
+decode-step cache read B * s_ctx * (d_c + d_rope) * e bytes ("G5 MLA KV
+访存建模设计规格" eq. gmkv-read) divided by the step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the CPU fp64 oracle (the reference arm of this method)
+on the host cores on a bounded sample of the same workload.
+Under torchrun each rank runs an independent replica (the path has no
+cross-sequence exchange), value = all ranks' bytes / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import os
+import sys
+
+# The CPU oracle legs use every host core through BLAS; fix the thread count
+# before numpy is imported so the reported core count is the one used.
+_CORES = os.cpu_count() or 1
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "absorbed-MLA decode µs/step, latent-KV GB/s and % of roofline at B×s_ctx"
+DECODE_SOURCES = ["mla_absorbed_latent_decode_gb300/csrc/decode_simt.cu",
+                  "mla_absorbed_latent_decode_gb300/csrc/decode_tc.cu"]
+DECODE_KERNEL_INDEX = 2          # position of the split-KV decode kernel in mla_profile_read
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="v3_b64_s4096_bf16")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU seconds of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def workload(name):
+    from mla_absorbed_latent_decode_gb300 import workloads as W
+    if name not in W.NAMED:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(W.NAMED)}")
+    return W.NAMED[name]()
+
+
+def algorithmic(wl):
+    """Bytes and FLOPs of one decode step (cache + W_UK + W_UV bytes; QK^T, P.c_kv, absorb, W_UV flops)."""
+    e = 1 if wl.cache_dtype == 2 else 2
+    tokens = wl.total_tokens
+    cache = tokens * (wl.d_c + wl.d_rope) * e
+    weights = 2 * wl.n_h * 128 * 512 * 2
+    flops = 2 * wl.n_h * tokens * (576 + 512) + 4 * wl.B * wl.n_h * 128 * 512
+    return cache, weights, flops
+
+
+def cache_bytes_per_token(wl):
+    return (wl.d_c + wl.d_rope) * (1 if wl.cache_dtype == 2 else 2)
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+
+def oracle_sample(wl, seconds):
+    """Time the oracle's absorbed decode on the first sequences of the workload until
+    about `seconds` of CPU work; return (GB/s of latent cache processed, description)."""
+    from oracle import mla_ref
+    from oracle import e4m3
+    starts = np.concatenate([[0], np.cumsum(wl.ctx_len.astype(np.int64))])
+    q = mla_ref.bf16_to_f64(wl.q)
+    w_uk = mla_ref.bf16_to_f64(wl.w_uk)
+    w_uv = mla_ref.bf16_to_f64(wl.w_uv)
+    scale = mla_ref.default_scale(wl.d_nope, wl.d_rope)
+    done_tokens, elapsed, nseq = 0, 0.0, 0
+    cached = wl.extra.setdefault("oracle_values", {})
+    for b in range(wl.B):
+        a, z = starts[b], starts[b + 1]
+        if b not in cached:                 # the oracle's own cache contents (prefill, untimed)
+            if wl.cache_dtype == 2:
+                st = mla_ref.stored_row_e4m3(wl.rows[a:z], wl.row_pos[a:z], wl.d_c, wl.rope_base,
+                                             np.float32(wl.fp8_scale))
+                cached[b] = e4m3.decode(st) * float(np.float32(wl.fp8_scale))
+            else:
+                cached[b] = mla_ref.bf16_to_f64(mla_ref.stored_row_bf16(wl.rows[a:z], wl.row_pos[a:z], wl.d_c,
+                                                                        wl.rope_base))
+        vals = cached[b]
+        t0 = time.perf_counter()
+        mla_ref.absorbed_decode(q[b], vals[:, :wl.d_c], vals[:, wl.d_c:], w_uk, w_uv, int(wl.ctx_len[b]) - 1,
+                                scale, wl.rope_base)
+        elapsed += time.perf_counter() - t0
+        done_tokens += int(z - a)
+        nseq += 1
+        if elapsed >= seconds:
+            break
+    gbps = done_tokens * cache_bytes_per_token(wl) / elapsed / 1e9
+    return gbps, elapsed, f"{nseq} of {wl.B} sequences ({done_tokens} tokens), fp64 absorbed path, {elapsed:.1f} s"
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return int(os.environ.get("OPENBLAS_NUM_THREADS", _CORES))
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = workload(args.workload)
+    per_step = max(0.5, min(3.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(wl, per_step)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        g, el, desc = oracle_sample(wl, per_step)
+        vals.append(g)
+        secs.append(el)
+    v = statistics.mean(vals)
+    us_equiv = wl.total_tokens * cache_bytes_per_token(wl) / (v * 1e9) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s (latent KV)",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us_equiv / 1000.0, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "s_ctx": wl.max_ctx, "n_h": wl.n_h,
+                   "cache": "fp8_e4m3" if wl.cache_dtype == 2 else "bf16",
+                   "note": "ms_per_step extrapolated from the sampled throughput to the whole batch"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s (latent KV)", "cores": blas_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(v, 4), "unit": "GB/s (latent KV)", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU leg
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc, self.gpu = None, gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sms, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def decode_source_hash():
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        p = os.path.join(ROOT, rel)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()
+
+
+def ncu_traffic(wl):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if it was
+    taken on the current decode source for this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    if d.get("source_sha256") != decode_source_hash() or d.get("workload") != wl.name:
+        return None
+    return d.get("bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from mla_absorbed_latent_decode_gb300 import binding as B
+    from mla_absorbed_latent_decode_gb300.runner import DecodeSession, bf16_tensor
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    wl = workload(args.workload)
+    sess = DecodeSession(wl, device=str(dev))
+    sess.prefill()
+    rows, seq, pos = sess.step_inputs()
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    sess.mla.set_option(B.MLA_OPT_PROFILE, 1)
+
+    def step():
+        sess.append_step(rows, seq, pos)
+        sess.decode()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if sess.status() != 0:
+        raise SystemExit("device check word set during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kernel_ms = []
+    for i in range(args.steps):
+        flush.zero_()                                      # L2 flush between steps, outside the events
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        kernel_ms.append(sess.mla.profile_read())          # syncs this step's events (between steps)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clock_info = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(step_ms)
+    if sess.status() != 0:
+        raise SystemExit("device check word set during the timed steps")
+
+    # end to end through the public API with host buffers: H2D of the step's inputs,
+    # append + decode, D2H of the result, every step
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    last = wl.last_row_index()
+    h_rows = pin(wl.rows[last].view(np.int16))
+    h_seq = pin(wl.row_seq[last].astype(np.int32))
+    h_pos = pin(wl.row_pos[last].astype(np.int32))
+    h_q = pin(wl.q.view(np.int16))
+    h_ctx = pin(wl.ctx_len.astype(np.int32))
+    h_out = torch.empty((wl.B, wl.n_h, wl.d_v), dtype=torch.int16).pin_memory()
+    d_rows = torch.empty_like(rows).view(torch.int16)
+    d_q = torch.empty_like(sess.q).view(torch.int16)
+    d_seq, d_pos, d_ctx = torch.empty_like(seq), torch.empty_like(pos), torch.empty_like(sess.ctx_len)
+    h2d = sum(t.numel() * t.element_size() for t in (h_rows, h_seq, h_pos, h_q, h_ctx))
+    d2h = h_out.numel() * h_out.element_size()
+    sess.mla.set_option(B.MLA_OPT_PROFILE, 0)
+
+    def e2e_step():
+        d_rows.copy_(h_rows, non_blocking=True)
+        d_seq.copy_(h_seq, non_blocking=True)
+        d_pos.copy_(h_pos, non_blocking=True)
+        d_q.copy_(h_q, non_blocking=True)
+        d_ctx.copy_(h_ctx, non_blocking=True)
+        sess.mla.kv_append(d_rows.view(torch.bfloat16), d_seq, d_pos, sess.block_table, sess.cache, wl.num_pages)
+        sess.mla.decode(d_q.view(torch.bfloat16), d_ctx, wl.max_ctx, sess.block_table, sess.cache, wl.num_pages,
+                        sess.workspace, sess.out)
+        h_out.copy_(sess.out.view(torch.int16), non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.zero_()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        e2e_step()
+        s1.record(stream)
+        s1.synchronize()
+        e2e_ms.append(s0.elapsed_time(s1))
+    e2e = statistics.mean(e2e_ms)
+
+    # max over ranks
+    t = torch.tensor([ms, e2e], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms, e2e = float(t[0]), float(t[1])
+
+    cache_b, weight_b, flops = algorithmic(wl)
+    hbm, tc_burst, tc_sust, peak_kind = peaks()
+    value = world * cache_b / (ms * 1e-3) / 1e9
+    e2e_value = world * cache_b / (e2e * 1e-3) / 1e9
+    roof_us = max((cache_b + weight_b) / (hbm * 1e9), flops / (tc_burst * 1e12)) * 1e6
+    dec_ms = statistics.mean(k.get("mla_decode_splitkv", float("nan")) for k in kernel_ms)
+    per_kernel = {k: round(statistics.mean(km[k] for km in kernel_ms) * 1000.0, 2) for k in kernel_ms[0]}
+    achieved = cache_b / (dec_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(wl)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s (latent KV)", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "us_per_step": round(ms * 1000.0, 2), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "roofline_us": round(roof_us, 2), "roofline_frac_step": round(roof_us / (ms * 1000.0), 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "s_ctx": wl.max_ctx, "n_h": wl.n_h, "d_c": wl.d_c,
+                       "d_rope": wl.d_rope, "cache": "fp8_e4m3" if wl.cache_dtype == 2 else "bf16",
+                       "total_tokens": wl.total_tokens,
+                       "l2": f"flushed between steps (write of {flush.numel() >> 20} MiB, outside the timed events)",
+                       "parallelism": f"replicas x{world}"},
+            "per_kernel_us": per_kernel,
+            "roofline": {"bound": "hbm", "kernel": "mla_decode_splitkv", "achieved": round(achieved, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                         "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                         "algorithmic_bytes_per_launch": cache_b},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s (latent KV)", "ms_per_step": round(e2e, 5),
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": args.steps * (1 + len(kernel_ms[0])),
+            "clocks": clock_info,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            g, el, desc = oracle_sample(wl, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": round(g, 4), "unit": "GB/s (latent KV)", "cores": blas_threads(),
+                                    "kind": "oracle", "sample": desc}
+        print(json.dumps(line), flush=True)
+    sess.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,223 @@
+/*
+ * mla.h -- C ABI of libmla.so: DeepSeek Multi-head Latent Attention (MLA)
+ * decode in absorb mode over a paged 576-wide latent cache, on one GB300
+ * (sm_103a).
+ *
+ * What is computed (citations name the source page by its title and section):
+ *
+ *   Each cached token is ONE row shared by all heads: the KV latent c (d_c =
+ *   512 values) followed by the decoupled RoPE key k_r (d_rope = 64), rotated
+ *   at the token's absolute position before it is stored
+ *   ("DeepSeek MLA 吸收式缓存：真实权重执行与 FlashMLA 架构边界" §2.4, 576 =
+ *   512 + 64 elements per token and layer).
+ *
+ *   A decode step of sequence b with context length L = ctx_len[b] computes,
+ *   for every head h, with the query at position L - 1:
+ *
+ *     q_lat[h] = W_UK[h]^T q_nope[h]                        (key absorption, §2.2)
+ *     s_t      = scale * ( q_lat[h] . c_t + RoPE(q_pe[h], L-1) . k_r,t )
+ *     o_lat[h] = sum_t softmax(s)_t c_t                     (latent sum, §2.3)
+ *     out[h]   = W_UV[h] o_lat[h]                           (value absorption, §2.3)
+ *
+ *   with scale = 1/sqrt(d_nope + d_rope) unless set.  In exact arithmetic this
+ *   equals standard MLA, which expands K = [W_UK c ; k_r] and V = W_UV c per
+ *   head ("80 行 PyTorch 从零写 DeepSeek 的 MLA" §4-§5).  RoPE rotates
+ *   interleaved pairs (2i, 2i+1) by pos * base^(-2i/d_rope) (same page,
+ *   附录 A).  The decode reads B * s_ctx * (d_c + d_rope) * e bytes of cache,
+ *   with no head count in it ("G5 MLA KV 访存建模设计规格" 算法与公式,
+ *   eq. gmkv-read).
+ *
+ * Conventions for every call:
+ *   - Tensor arguments are DEVICE pointers to caller-owned memory, row-major,
+ *     densely packed unless a stride is given.  bf16 means IEEE bfloat16 bits.
+ *   - Work is enqueued asynchronously on the given stream (NULL = legacy
+ *     default stream); the call returns after launching.  Host-side argument
+ *     checks happen before anything is launched: on error nothing is enqueued.
+ *   - mla_kv_append and mla_decode allocate nothing.
+ *   - Data-dependent problems found ON THE DEVICE (a context length or page id
+ *     out of range, an append index out of range) never trap: the affected
+ *     sequence's output is zeroed (or the row is not written) and a bit is
+ *     set in the handle's device check word, read by mla_get_status().
+ *   - The library is built for sm_103a only; there is no CPU or other-GPU
+ *     path.  mla_create fails with MLA_ERR_UNSUPPORTED on any other device.
+ *   - Error messages are kept per host thread; mla_last_error() returns the
+ *     message of the calling thread's last failed call.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                       /* identical to cudaStream_t's target */
+typedef struct CUstream_st* mla_stream_t;
+typedef struct mla_handle_s* mla_handle_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_MISSING_FIELD = 1,   /* a mandatory mla_config_t field is 0 / unset  */
+  MLA_ERR_INVALID_ARG = 2,     /* a pointer, size or stride argument is invalid */
+  MLA_ERR_UNSUPPORTED = 3,     /* valid but not built: shape, dtype, device     */
+  MLA_ERR_WORKSPACE = 4,       /* workspace NULL, too small or misaligned       */
+  MLA_ERR_CUDA = 5,            /* a CUDA runtime / driver call failed           */
+  MLA_ERR_DEVICE_CHECK = 6     /* mla_get_status: the device check word was set */
+} mla_status_t;
+
+typedef enum {
+  MLA_CACHE_BF16 = 1,          /* 576 bf16 per row: 1152 bytes                  */
+  MLA_CACHE_FP8_E4M3 = 2       /* 576 OCP e4m3 bytes per row, one fp32 scale    */
+} mla_cache_dtype_t;
+
+/* Bits of the device check word (mla_get_status's *device_flags). */
+#define MLA_CHECK_CTX_LEN      0x1u  /* ctx_len[b] < 1 or > max_ctx                  */
+#define MLA_CHECK_PAGE_ID      0x2u  /* a block-table entry outside [0, num_pages)   */
+#define MLA_CHECK_APPEND_INDEX 0x4u  /* append: seq or pos out of range              */
+#define MLA_CHECK_TIMEOUT      0x8u  /* a bounded in-kernel wait ran out             */
+
+/*
+ * Layer configuration.  Every field is mandatory: a zero (unset) integer or
+ * float field fails mla_create with MLA_ERR_MISSING_FIELD, and the message
+ * names the field and says it came from mla_config_t ("G5 MLA KV
+ * 访存建模设计规格" 约束: kv_lora_rank and qk_rope_head_dim must be given and
+ * a missing field raises with its name and source, never a silent default).
+ * The two exceptions are stated on their fields.
+ */
+typedef struct mla_config {
+  int32_t d_c;          /* KV latent width (kv_lora_rank).  Built: 512.                  */
+  int32_t d_rope;       /* decoupled RoPE key width (qk_rope_head_dim).  Built: 64.      */
+  int32_t n_h;          /* query heads.  Built: 1..128.                                   */
+  int32_t d_nope;       /* no-RoPE query/key width per head.  Built: 128.                 */
+  int32_t d_v;          /* value width per head.  Built: 128.                             */
+  int32_t page_size;    /* tokens per cache page.  Built: 64.                             */
+  int32_t cache_dtype;  /* mla_cache_dtype_t.                                             */
+  int32_t max_position; /* size of the RoPE table: positions 0..max_position-1.  <= 2^22. */
+  float rope_base;      /* RoPE base (10000 for the configurations here).                 */
+  float softmax_scale;  /* EXCEPTION: 0 means 1/sqrt(d_nope + d_rope).                    */
+  float fp8_scale;      /* EXCEPTION: mandatory (> 0) only for MLA_CACHE_FP8_E4M3, where a
+                           stored code x represents x * fp8_scale; ignored for bf16.      */
+} mla_config_t;
+
+/*
+ * mla_create -- validate the configuration, copy the weights, build tables.
+ *
+ *   cfg     host pointer to the configuration (copied).
+ *   w_uk    device, [n_h][d_nope][d_c] bf16: W_UK[h] maps a latent c to the
+ *           no-RoPE key of head h (k = W_UK[h] c; the first half of each head's
+ *           rows of kv_b_proj / wkv_b, "DeepSeek MLA 吸收式缓存" §3.3).
+ *   w_uv    device, [n_h][d_v][d_c] bf16: W_UV[h] maps a latent to head h's value.
+ *   stream  the copies run on it; mla_create synchronizes it before returning,
+ *           so the caller may free w_uk / w_uv afterwards.
+ *   out     receives the handle.
+ *
+ * The handle owns re-laid-out device copies of both weights, an fp32 RoPE
+ * cos/sin table (angles computed in float64 on the host) and a device check
+ * word.  Errors: MLA_ERR_MISSING_FIELD, MLA_ERR_INVALID_ARG (NULL pointer),
+ * MLA_ERR_UNSUPPORTED (shape other than the built ones, or not an sm_103
+ * device), MLA_ERR_CUDA.
+ */
+mla_status_t mla_create(const mla_config_t* cfg, const void* w_uk, const void* w_uv,
+                        mla_stream_t stream, mla_handle_t* out);
+
+/* mla_destroy -- synchronize the device and free everything the handle owns. NULL is a no-op. */
+mla_status_t mla_destroy(mla_handle_t h);
+
+/*
+ * mla_kv_append -- write n token rows into the paged cache.
+ *
+ * Row i (rows[i], d_c + d_rope bf16 values: latent first, then the UNROTATED
+ * RoPE key) is token pos[i] of sequence seq[i].  It is stored at page
+ * block_table[seq[i] * bt_stride + pos[i] / page_size], slot pos[i] % page_size:
+ * the latent copied unchanged, the RoPE key rotated at position pos[i]
+ * ("DeepSeek MLA 吸收式缓存" §2.4: the rope key depends on position and is
+ * cached; "80 行 PyTorch 从零写 DeepSeek 的 MLA" §2: keys rotated at their
+ * absolute positions).  For an FP8 cache all d_c + d_rope stored values are
+ * divided by fp8_scale in fp32 and encoded e4m3, nearest-even, saturating at
+ * +-448.  The rotation is computed in fp32 with fp32 cos/sin, each product
+ * and sum rounded separately.
+ *
+ *   rows         device [n][d_c + d_rope] bf16.
+ *   seq, pos     device [n] int32.
+ *   n            rows to write (0 is a no-op).
+ *   block_table  device [bt_rows][bt_stride] int32 page ids.
+ *   cache        device [num_pages][page_size][d_c + d_rope], bf16 or e4m3 bytes.
+ *
+ * Rows written by one call must target distinct slots.  Device checks: seq
+ * outside [0, bt_rows), pos outside [0, max_position) or past the block-table
+ * row, or a page id outside [0, num_pages): the row is skipped and
+ * MLA_CHECK_APPEND_INDEX / MLA_CHECK_PAGE_ID is set.
+ */
+mla_status_t mla_kv_append(mla_handle_t h, const void* rows, const int32_t* seq,
+                           const int32_t* pos, int32_t n, const int32_t* block_table,
+                           int32_t bt_rows, int32_t bt_stride, void* cache,
+                           int32_t num_pages, mla_stream_t stream);
+
+/*
+ * mla_decode_workspace_size -- bytes of device workspace mla_decode needs for
+ * a batch of `batch` sequences of at most `max_ctx` tokens.  The workspace
+ * holds the split plan, the absorbed queries and the split partials.
+ */
+mla_status_t mla_decode_workspace_size(mla_handle_t h, int32_t batch, int32_t max_ctx,
+                                       size_t* bytes);
+
+/*
+ * mla_decode -- one decode step for `batch` sequences (one query token each).
+ *
+ *   q            device [batch][n_h][d_nope + d_rope] bf16: per head the no-RoPE
+ *                part, then the unrotated RoPE part.  The query sits at position
+ *                ctx_len[b] - 1 (its own row must already be appended).
+ *   ctx_len      device [batch] int32, each in [1, max_ctx].
+ *   block_table  device [batch][bt_stride] int32: row b lists sequence b's pages.
+ *   cache        device, as written by mla_kv_append.
+ *   workspace    device, >= mla_decode_workspace_size(h, batch, max_ctx) bytes,
+ *                256-byte aligned; contents are scratch (not kept between calls).
+ *   out          device [batch][n_h][d_v] bf16: per head the attention output
+ *                before the output projection W_O.
+ *
+ * Long contexts are split across SM pairs and merged by log-sum-exp; the
+ * result does not depend on the split beyond fp32 rounding.  Device checks:
+ * a bad ctx_len or page id zeroes that sequence's output and sets
+ * MLA_CHECK_CTX_LEN / MLA_CHECK_PAGE_ID.
+ */
+mla_status_t mla_decode(mla_handle_t h, const void* q, const int32_t* ctx_len, int32_t batch,
+                        int32_t max_ctx, const int32_t* block_table, int32_t bt_stride,
+                        const void* cache, int32_t num_pages, void* workspace,
+                        size_t workspace_bytes, void* out, mla_stream_t stream);
+
+/*
+ * mla_get_status -- synchronize `stream`, read and clear the device check word.
+ * Returns MLA_OK when it was clear, else MLA_ERR_DEVICE_CHECK with the bits in
+ * *device_flags (may be NULL) and a message naming them.
+ */
+mla_status_t mla_get_status(mla_handle_t h, mla_stream_t stream, uint32_t* device_flags);
+
+/* Options for mla_set_option. */
+#define MLA_OPT_SPLITS  1   /* value 0: the planner chooses; k > 0: split every sequence into
+                               k chunks (capped at its page count).  Used to test that the
+                               result does not depend on the split. */
+#define MLA_OPT_PROFILE 2   /* value 1: record CUDA events around each kernel mla_decode
+                               launches; mla_profile_read returns the durations. 0: off. */
+
+mla_status_t mla_set_option(mla_handle_t h, int32_t option, int64_t value);
+
+/*
+ * mla_profile_read -- with MLA_OPT_PROFILE on, synchronize and return the
+ * device time in milliseconds of each kernel of the last mla_decode call, in
+ * launch order (plan, q-absorb, decode, combine + W_UV).  *count receives the
+ * number of kernels; at most `capacity` values are written.  Names of the
+ * kernels come from mla_profile_kernel_name.
+ */
+mla_status_t mla_profile_read(mla_handle_t h, float* kernel_ms, int32_t capacity, int32_t* count);
+const char* mla_profile_kernel_name(int32_t index);
+
+/* Thread-local message of this thread's last failed call ("" if none). */
+const char* mla_last_error(void);
+const char* mla_status_string(mla_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_H_ */

@@ -1,0 +1,125 @@
+// append.cu -- mla_kv_append: write token rows into the paged latent cache.
+//
+// A row is [c (512) | k_r (64)] bf16.  The latent is stored unchanged; the RoPE
+// key is rotated at the token's absolute position ("DeepSeek MLA 吸收式缓存：真实
+// 权重执行与 FlashMLA 架构边界" §2.4; rotation of interleaved pairs as in "80 行
+// PyTorch 从零写 DeepSeek 的 MLA" 附录 A).  An FP8 cache stores every value
+// divided by the tensor scale as OCP e4m3 (nearest even, saturating).
+//
+// One warp per row.  Lane l owns latent values [16 l, 16 l + 16) (32 bytes in,
+// 32 bytes (bf16) or 16 bytes (e4m3) out); lanes 0..3 also own RoPE values
+// [16 l, 16 l + 16) of the key.  HBM-bound: 1152 bytes read and 1152 (bf16) or
+// 576 (e4m3) bytes written per row.
+#include <cuda_fp8.h>
+
+#include "internal.cuh"
+
+namespace mla {
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
+
+// Rotate one interleaved pair by (cos, sin) with every product and sum rounded to fp32.
+__device__ __forceinline__ void rope_pair(float x0, float x1, float2 cs, float* o0, float* o1) {
+  *o0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+  *o1 = __fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y));
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(256) kv_append_kernel(
+    const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ seq,
+    const int32_t* __restrict__ pos, int n, const int32_t* __restrict__ block_table, int bt_rows,
+    int bt_stride, uint8_t* __restrict__ cache, int num_pages, const float2* __restrict__ rope_cs,
+    int max_position, float fp8_scale, unsigned* check) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= n) return;
+  const int s = seq[warp];
+  const int p = pos[warp];
+  if (s < 0 || s >= bt_rows || p < 0 || p >= max_position || p / kPage >= bt_stride) {
+    if (lane == 0) atomicOr(check, kCheckAppend);
+    return;
+  }
+  const int page = block_table[(size_t)s * bt_stride + p / kPage];
+  if (page < 0 || page >= num_pages) {
+    if (lane == 0) atomicOr(check, kCheckPageId);
+    return;
+  }
+  constexpr int kElem = kFp8 ? 1 : 2;
+  const uint4* src = reinterpret_cast<const uint4*>(rows + (size_t)warp * kRow);
+  uint8_t* dst = cache + ((size_t)page * kPage + (p % kPage)) * (size_t)(kRow * kElem);
+
+  // latent: values [16 lane, 16 lane + 16)
+  const uint4 a = src[2 * lane];
+  const uint4 b = src[2 * lane + 1];
+  if (!kFp8) {
+    reinterpret_cast<uint4*>(dst)[2 * lane] = a;
+    reinterpret_cast<uint4*>(dst)[2 * lane + 1] = b;
+  } else {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = pack_e4m3x4(__fdiv_rn(bf16_lo(w[2 * i]), fp8_scale), __fdiv_rn(bf16_hi(w[2 * i]), fp8_scale),
+                         __fdiv_rn(bf16_lo(w[2 * i + 1]), fp8_scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), fp8_scale));
+    reinterpret_cast<uint4*>(dst)[lane] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+
+  // RoPE key: lanes 0..3 own values [16 lane, 16 lane + 16) = pairs [8 lane, 8 lane + 8)
+  if (lane < 4) {
+    const uint4 ra = src[kDc / 8 + 2 * lane];
+    const uint4 rb = src[kDc / 8 + 2 * lane + 1];
+    const uint32_t w[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+    const float2* cs = rope_cs + (size_t)p * (kDr / 2) + 8 * lane;
+    float r[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rope_pair(bf16_lo(w[i]), bf16_hi(w[i]), cs[i], &r[2 * i], &r[2 * i + 1]);
+    if (!kFp8) {
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = pack_bf16(r[2 * i], r[2 * i + 1]);
+      uint4* d = reinterpret_cast<uint4*>(dst + kDc * kElem);
+      d[2 * lane] = make_uint4(o[0], o[1], o[2], o[3]);
+      d[2 * lane + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    } else {
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        o[i] = pack_e4m3x4(__fdiv_rn(r[4 * i], fp8_scale), __fdiv_rn(r[4 * i + 1], fp8_scale),
+                           __fdiv_rn(r[4 * i + 2], fp8_scale), __fdiv_rn(r[4 * i + 3], fp8_scale));
+      reinterpret_cast<uint4*>(dst + kDc * kElem)[lane] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const Handle& h, const __nv_bfloat16* rows, const int32_t* seq,
+                             const int32_t* pos, int n, const int32_t* block_table, int bt_rows,
+                             int bt_stride, void* cache, int num_pages, cudaStream_t st) {
+  const int threads = 256;
+  const int blocks = (int)(((long long)n * 32 + threads - 1) / threads);
+  if (h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3)
+    kv_append_kernel<true><<<blocks, threads, 0, st>>>(rows, seq, pos, n, block_table, bt_rows, bt_stride,
+                                                       static_cast<uint8_t*>(cache), num_pages, h.rope_cs,
+                                                       h.cfg.max_position, h.cfg.fp8_scale, h.check_word);
+  else
+    kv_append_kernel<false><<<blocks, threads, 0, st>>>(rows, seq, pos, n, block_table, bt_rows, bt_stride,
+                                                        static_cast<uint8_t*>(cache), num_pages, h.rope_cs,
+                                                        h.cfg.max_position, 0.0f, h.check_word);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,92 @@
+// internal.cuh -- types shared by the host API and the kernels of libmla.so.
+//
+// Shapes built: d_c = 512, d_rope = 64, d_nope = d_v = 128, page = 64 tokens,
+// 1 <= n_h <= 128.  A cache row is [c (512) | k_r (64)] = 576 values.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kDc = 512;          // KV latent width
+constexpr int kDr = 64;           // RoPE key width
+constexpr int kRow = kDc + kDr;   // 576 values per cached token
+constexpr int kDn = 128;          // no-RoPE query width per head
+constexpr int kDq = kDn + kDr;    // 192 query values per head
+constexpr int kDv = 128;          // value width per head
+constexpr int kPage = 64;         // tokens per page
+constexpr int kMaxHeads = 128;    // heads padded to one 128-row MMA tile
+constexpr int kMaxPosition = 1 << 20;
+
+// One unit of decode work: tokens [page_begin * 64, min(page_end * 64, ctx_len)) of sequence b.
+struct Unit {
+  int32_t b;
+  int32_t page_begin;
+  int32_t page_end;
+  int32_t part;        // index of this unit's partial slot, or -1 when the unit is the whole sequence
+};
+
+// Per-sequence plan entry.
+struct SeqPlan {
+  int32_t first_unit;  // first unit of the sequence (units of a sequence are consecutive)
+  int32_t nsplit;      // 0: invalid sequence (output zeroed), 1: unsplit, >1: split
+};
+
+// Device-side views of the workspace (all regions 256-byte aligned).
+struct Workspace {
+  int32_t* counters;        // [0] = number of units, [1] = number of partial slots
+  Unit* units;              // [max_units]
+  SeqPlan* seqs;            // [B]
+  __nv_bfloat16* q_abs;     // [B][n_h][576]: absorbed query (latent 512 | rotated rope 64)
+  __nv_bfloat16* o_lat;     // [B][n_h][512]: normalised latent sum of unsplit sequences
+  float* part_o;            // [max_parts][n_h][512]: normalised partial latent sums
+  float* part_lse;          // [max_parts][n_h]: natural-log normaliser of each partial
+  int max_units;
+  int max_parts;
+};
+
+struct Handle {
+  mla_config_t cfg;
+  float scale;              // softmax scale actually used
+  int device;
+  int num_sms;
+  int num_pairs;            // SM pairs available to the decode kernel
+  __nv_bfloat16* w_uk;      // [n_h][d_nope][d_c] (as given)
+  __nv_bfloat16* w_uv;      // [n_h][d_v][d_c]   (as given)
+  float2* rope_cs;          // [max_position][d_rope / 2] (cos, sin) fp32 from float64 angles
+  unsigned* check_word;     // device check word
+  int force_splits;         // MLA_OPT_SPLITS
+  int profile;              // MLA_OPT_PROFILE
+  cudaEvent_t ev[8];
+  int n_ev_recorded;
+};
+
+// Workspace sizing and carving (host).
+size_t workspace_bytes(const Handle& h, int batch, Workspace* carve, char* base);
+
+// Kernel launchers (each returns the launch error).
+cudaError_t launch_kv_append(const Handle& h, const __nv_bfloat16* rows, const int32_t* seq,
+                             const int32_t* pos, int n, const int32_t* block_table, int bt_rows,
+                             int bt_stride, void* cache, int num_pages, cudaStream_t st);
+cudaError_t launch_plan(const Handle& h, const int32_t* ctx_len, int batch, int max_ctx,
+                        const int32_t* block_table, int bt_stride, int num_pages,
+                        const Workspace& ws, cudaStream_t st);
+cudaError_t launch_q_absorb(const Handle& h, const __nv_bfloat16* q, const int32_t* ctx_len,
+                            int batch, const Workspace& ws, cudaStream_t st);
+cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch,
+                          const int32_t* block_table, int bt_stride, const void* cache,
+                          int num_pages, const Workspace& ws, cudaStream_t st);
+cudaError_t launch_combine_uv(const Handle& h, int batch, const Workspace& ws,
+                              __nv_bfloat16* out, cudaStream_t st);
+
+// Device check word bits (same values as the public MLA_CHECK_* macros).
+constexpr unsigned kCheckCtxLen = MLA_CHECK_CTX_LEN;
+constexpr unsigned kCheckPageId = MLA_CHECK_PAGE_ID;
+constexpr unsigned kCheckAppend = MLA_CHECK_APPEND_INDEX;
+constexpr unsigned kCheckTimeout = MLA_CHECK_TIMEOUT;
+
+}  // namespace mla

@@ -1,0 +1,149 @@
+// plan.cu -- the split-KV planner of a decode step (integer work, one CTA).
+//
+// Input: ctx_len[B] and the block table.  Output (in the workspace): a list of
+// units, each a contiguous page range of one sequence, and per sequence the
+// index of its first unit and its unit count.
+//
+//   valid(b)   = 1 <= ctx_len[b] <= max_ctx and every page id of the sequence
+//                lies in [0, num_pages); otherwise the sequence gets no unit,
+//                its output is zeroed and a check bit is set.
+//   pages(b)   = ceil(ctx_len[b] / 64) for a valid sequence, else 0.
+//   target     = max(1, ceil(sum_b pages(b) / num_pairs)): pages one SM pair
+//                should stream so that every pair gets about the same share.
+//   nsplit(b)  = ceil(pages(b) / target), or min(forced, pages(b)) when the
+//                split count is forced.
+//   unit j of b covers pages [j * pages(b) / nsplit(b), (j+1) * pages(b) / nsplit(b)).
+//
+// Units are numbered sequence by sequence.  A unit that is a whole sequence
+// writes the final latent sum; the others write partials (slot = unit index)
+// merged later by log-sum-exp.  Splitting is not on the pages; it is needed
+// because one sequence's context (up to 65536 tokens here) is far more work
+// than one SM pair should take when the batch is small.
+#include "internal.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+__device__ int block_sum(int v, int* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  int t = 0;
+  if (threadIdx.x < 32) {
+    t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (threadIdx.x == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+// Exclusive prefix sum over one value per thread; returns the block total in *total.
+__device__ int block_exclusive_scan(int v, int* red, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int w = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0;
+    int s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    red[threadIdx.x] = s - w;  // exclusive warp offsets
+    if (threadIdx.x == 31) red[32] = s;
+  }
+  __syncthreads();
+  const int r = red[warp] + x - v;
+  *total = red[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(
+    const int32_t* __restrict__ ctx_len, int B, int max_ctx, const int32_t* __restrict__ block_table,
+    int bt_stride, int num_pages, int num_pairs, int forced, Workspace ws, unsigned* check) {
+  __shared__ int red[64];
+  // 1. validate and count pages; pages(b) parked in seqs[b].nsplit
+  unsigned flags = 0;
+  int my_pages = 0;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int L = ctx_len[b];
+    int np = 0;
+    if (L < 1 || L > max_ctx) {
+      flags |= kCheckCtxLen;
+    } else {
+      np = (L + kPage - 1) / kPage;
+      const int32_t* row = block_table + (size_t)b * bt_stride;
+      for (int i = 0; i < np; ++i) {
+        const int pg = row[i];
+        if (pg < 0 || pg >= num_pages) { flags |= kCheckPageId; np = 0; break; }
+      }
+    }
+    ws.seqs[b].nsplit = np;
+    my_pages += np;
+  }
+  if (flags) atomicOr(check, flags);
+  const int total_pages = block_sum(my_pages, red);
+  const int target = max(1, (total_pages + num_pairs - 1) / max(1, num_pairs));
+
+  // 2. split counts, prefix-summed chunk by chunk into first_unit
+  int base = 0;
+  for (int b0 = 0; b0 < B; b0 += blockDim.x) {
+    const int b = b0 + threadIdx.x;
+    int ns = 0;
+    if (b < B) {
+      const int np = ws.seqs[b].nsplit;
+      ns = np == 0 ? 0 : (forced > 0 ? min(forced, np) : (np + target - 1) / target);
+    }
+    int chunk_total = 0;
+    const int off = block_exclusive_scan(ns, red, &chunk_total);
+    if (b < B) {
+      const int np = ws.seqs[b].nsplit;
+      const int first = base + off;
+      for (int j = 0; j < ns; ++j) {
+        Unit u;
+        u.b = b;
+        u.page_begin = (int)((long long)j * np / ns);
+        u.page_end = (int)((long long)(j + 1) * np / ns);
+        u.part = ns > 1 ? first + j : -1;
+        ws.units[first + j] = u;
+      }
+      SeqPlan sp;
+      sp.first_unit = first;
+      sp.nsplit = ns;
+      ws.seqs[b] = sp;
+    }
+    base += chunk_total;
+  }
+  if (threadIdx.x == 0) {
+    ws.counters[0] = base;
+    ws.counters[1] = base;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const Handle& h, const int32_t* ctx_len, int batch, int max_ctx,
+                        const int32_t* block_table, int bt_stride, int num_pages, const Workspace& ws,
+                        cudaStream_t st) {
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(ctx_len, batch, max_ctx, block_table, bt_stride, num_pages,
+                                          h.num_pairs, h.force_splits, ws, h.check_word);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

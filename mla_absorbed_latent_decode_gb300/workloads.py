@@ -105,7 +105,9 @@ def _paged_layout(rng, ctx_len, page_size, spare_pages, shuffle=True):
     """Block table over a pool whose pages are handed out in a seeded shuffled order."""
     n_pages = [(int(s) + page_size - 1) // page_size for s in ctx_len]
     total = int(sum(n_pages)) + int(spare_pages)
-    order = rng.permutation(total).astype(np.int32) if shuffle else np.arange(total, dtype=np.int32)
+    order = rng.permutation(total).astype(np.int32)     # drawn either way: the stream stays aligned
+    if not shuffle:
+        order = np.arange(total, dtype=np.int32)
     max_pages = max(1, max(n_pages) if n_pages else 1)
     bt = np.full((len(ctx_len), max_pages), -1, dtype=np.int32)
     off = 0

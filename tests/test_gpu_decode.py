@@ -1,0 +1,163 @@
+"""mla_decode on the GPU against the fp64 oracle on the same seeded inputs, at sizes
+that span several pages and a ragged tail, plus the bookkeeping and the
+invariances the method implies (split count, page order, repeatability)."""
+import numpy as np
+import pytest
+import torch
+
+from mla_absorbed_latent_decode_gb300 import binding as B
+from mla_absorbed_latent_decode_gb300 import workloads as W
+from mla_absorbed_latent_decode_gb300.runner import DecodeSession
+from tests.mla_cases import (BF16_TOL, FP8_TOL, bf16_out_to_f64, compare, oracle_decode,
+                             oracle_decode_paged, oracle_stored, oracle_values)
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = [1, 2, 63, 64, 65, 130, 257, 1000]
+
+
+def _run(wl, splits=0, max_position=None):
+    s = DecodeSession(wl, splits=splits, max_position=max_position)
+    s.append_rows()
+    out = s.decode()
+    flags = s.status()
+    return s, bf16_out_to_f64(out), flags
+
+
+@pytest.mark.parametrize("n_h", [16, 128, 40])
+@pytest.mark.parametrize("dtype", [W.CACHE_BF16, W.CACHE_FP8])
+def test_decode_matches_oracle_ragged(n_h, dtype):
+    wl = W.make_decode("ragged", 21 + n_h, n_h, RAGGED, cache_dtype=dtype)
+    s, out, flags = _run(wl)
+    assert flags == 0
+    ref = oracle_decode_paged(wl, oracle_values(wl, oracle_stored(wl)))
+    rel, err, scale = compare(out, ref, BF16_TOL if dtype == W.CACHE_BF16 else FP8_TOL)
+    assert rel <= (BF16_TOL if dtype == W.CACHE_BF16 else FP8_TOL), (rel, err, scale)
+    s.close()
+
+
+def test_naive_and_absorbed_oracles_agree_on_the_gpu_case():
+    wl = W.make_decode("naive", 31, 16, [5, 70])
+    vals = oracle_values(wl, oracle_stored(wl))
+    a = oracle_decode(wl, vals)
+    n = oracle_decode(wl, vals, path="naive")
+    assert np.max(np.abs(a - n)) < 1e-10
+    s, out, _ = _run(wl)
+    assert compare(out, n, BF16_TOL)[0] <= BF16_TOL
+    s.close()
+
+
+def _workspace_layout(batch, n_h, max_units):
+    al = lambda x: (x + 255) & ~255
+    off = {}
+    o = 0
+    for name, size in (("counters", 256), ("units", 16 * max_units), ("seqs", 8 * batch),
+                       ("q_abs", 2 * batch * n_h * 576), ("o_lat", 2 * batch * n_h * 512)):
+        off[name] = o
+        o = al(o + size)
+    return off
+
+
+def plan_reference(ctx_len, bt, num_pages, max_ctx, num_pairs, forced=0):
+    """The planner's rule restated: per-sequence page counts, a per-pair page target, balanced splits."""
+    pages = []
+    for b, L in enumerate(ctx_len):
+        np_b = 0
+        if 1 <= L <= max_ctx:
+            np_b = (L + 63) // 64
+            if any(not (0 <= bt[b][i] < num_pages) for i in range(np_b)):
+                np_b = 0
+        pages.append(np_b)
+    target = max(1, -(-sum(pages) // max(1, num_pairs)))
+    units, seqs = [], []
+    for b, np_b in enumerate(pages):
+        ns = 0 if np_b == 0 else (min(forced, np_b) if forced else -(-np_b // target))
+        seqs.append((len(units), ns))
+        first = len(units)
+        for j in range(ns):
+            units.append((b, j * np_b // ns, (j + 1) * np_b // ns, first + j if ns > 1 else -1))
+    return units, seqs
+
+
+@pytest.mark.parametrize("forced", [0, 3])
+def test_plan_is_bit_exact(forced):
+    ctx = [1, 4096, 65, 700, 3000, 64, 129, 2048] * 4
+    wl = W.make_decode("plan", 41, 16, ctx)
+    s, _, _ = _run(wl, splits=forced)
+    num_pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    max_units = wl.B * max(1, forced) + num_pairs
+    off = _workspace_layout(wl.B, wl.n_h, max_units)
+    ws = s.workspace.cpu().numpy()
+    n_units = int(ws[off["counters"]:off["counters"] + 4].view(np.int32)[0])
+    units = ws[off["units"]:off["units"] + 16 * n_units].view(np.int32).reshape(-1, 4)
+    seqs = ws[off["seqs"]:off["seqs"] + 8 * wl.B].view(np.int32).reshape(-1, 2)
+    ref_units, ref_seqs = plan_reference(wl.ctx_len.tolist(), wl.block_table, wl.num_pages, wl.max_ctx,
+                                         num_pairs, forced)
+    assert n_units == len(ref_units)
+    assert [tuple(u) for u in units.tolist()] == ref_units
+    assert [tuple(x) for x in seqs.tolist()] == ref_seqs
+    s.close()
+
+
+def test_split_count_does_not_change_the_result():
+    wl = W.make_decode("split", 51, 128, [3000, 1500, 64, 1])
+    outs = []
+    for k in (1, 2, 7, 64):
+        s, out, flags = _run(wl, splits=k)
+        assert flags == 0
+        outs.append(out)
+        s.close()
+    ref = oracle_decode(wl, oracle_values(wl, oracle_stored(wl)))
+    for o in outs:
+        assert compare(o, ref, BF16_TOL)[0] <= BF16_TOL
+        # the split changes only fp32 rounding: a couple of bf16 ulps at most
+        assert np.max(np.abs(o - outs[0])) <= 4 * 2.0 ** -8 * np.max(np.abs(outs[0]))
+
+
+def test_page_order_and_repeat_are_bit_identical():
+    ctx = [500, 64, 1234]
+    a = W.make_decode("order", 61, 128, ctx, shuffle=True)
+    b = W.make_decode("order", 61, 128, ctx, shuffle=False)
+    assert not np.array_equal(a.block_table, b.block_table)
+    sa, oa, _ = _run(a)
+    sb, ob, _ = _run(b)
+    assert np.array_equal(oa, ob)
+    again = bf16_out_to_f64(sa.decode())
+    assert np.array_equal(again, oa)
+    sa.close()
+    sb.close()
+
+
+def test_bad_lengths_and_pages_zero_only_their_sequence():
+    wl = W.make_decode("badlen", 71, 16, [100, 200, 300, 64])
+    s = DecodeSession(wl)
+    s.append_rows()
+    good = bf16_out_to_f64(s.decode())
+    assert s.status() == 0
+    ctx = s.ctx_len.clone()
+    ctx[1] = 0                                                      # empty context: invalid
+    ctx[2] = wl.max_ctx + 1                                         # longer than max_ctx
+    s.mla.decode(s.q, ctx, wl.max_ctx, s.block_table, s.cache, wl.num_pages, s.workspace, s.out)
+    out = bf16_out_to_f64(s.out)
+    assert s.status() == B.MLA_CHECK_CTX_LEN
+    assert np.all(out[1] == 0) and np.all(out[2] == 0)
+    assert np.array_equal(out[0], good[0]) and np.array_equal(out[3], good[3])
+    bt = s.block_table.clone()
+    bt[3, 0] = -7
+    s.mla.decode(s.q, s.ctx_len, wl.max_ctx, bt, s.cache, wl.num_pages, s.workspace, s.out)
+    out = bf16_out_to_f64(s.out)
+    assert s.status() == B.MLA_CHECK_PAGE_ID
+    assert np.all(out[3] == 0) and np.array_equal(out[:3], good[:3])
+    s.close()
+
+
+def test_decode_host_argument_errors():
+    wl = W.make_decode("args", 81, 16, [10, 20])
+    s = DecodeSession(wl)
+    with pytest.raises(B.MlaError) as e:
+        s.mla.decode(s.q, s.ctx_len, wl.max_ctx, s.block_table, s.cache, wl.num_pages, s.workspace[:16], s.out)
+    assert e.value.status == B.MLA_ERR_WORKSPACE
+    with pytest.raises(B.MlaError) as e:
+        s.mla.decode(s.q, s.ctx_len, 10 ** 6, s.block_table, s.cache, wl.num_pages, s.workspace, s.out)
+    assert e.value.status == B.MLA_ERR_INVALID_ARG
+    s.close()
