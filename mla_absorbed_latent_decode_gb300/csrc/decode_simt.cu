@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
 
 }  // namespace
 
-cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table,
+cudaError_t launch_decode_simt(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table,
                           int bt_stride, const void* cache, int num_pages, const Workspace& ws, cudaStream_t st) {
   (void)batch;
   (void)num_pages;

@@ -1,0 +1,460 @@
+// decode_tc.cu -- split-KV flash decode over the paged 576-wide latent cache on
+// the 5th-generation tensor cores (tcgen05 + Tensor Memory), TMA-fed.
+//
+// What one work unit computes (a page range of one sequence, all heads):
+//   s_t    = scale * ( q_lat[h] . c_t + q_pe'[h] . k_r,t )                 t in the unit
+//   o[h]   = sum_t softmax(s)_t c_t, with the unit's log-sum-exp when split
+// ("DeepSeek MLA 吸收式缓存：真实权重执行与 FlashMLA 架构边界" §2.2-§2.4: the
+// absorbed query is scored against the shared latent row, and the softmax
+// weights sum latent rows; "G5 MLA KV 访存建模设计规格" 附录 B: the KV stream is
+// consumed as it arrives -- flash decode).
+//
+// Design (one 2-CTA cluster per unit; heads are the 128-row M dimension, so one
+// cache tile serves every head of the sequence):
+//   * The 576 columns are split between the two CTAs of the cluster:
+//       CTA 0 ("lo"): latent columns [0, 256)
+//       CTA 1 ("hi"): latent columns [256, 512) and the RoPE key [512, 576)
+//     Each CTA TMA-loads only its columns of every 64-token page (32 / 40 KB),
+//     so the pair reads each cache byte from HBM once.
+//   * QK^T is split along K: each CTA computes a partial score tile
+//       S_r[128 heads x 64 tokens] = Q_r . C_r^T
+//     with Q_r's latent part resident in TMEM (A operand) and, on CTA 1, the
+//     RoPE part of the query in shared memory.  The two partials are exchanged
+//     through distributed shared memory (st.async, 32 KB per tile each way) and
+//     both CTAs form the same full score S = S_lo + S_hi, so both compute
+//     bit-identical softmax weights P.
+//   * P (bf16) is written back into TMEM over S and used as the A operand of
+//     O_r[128 x 256] += P . C_r[64 tokens x 256 latent]; the same shared-memory
+//     tile is the B operand, read MN-major.  Each CTA accumulates its half of
+//     the latent output in TMEM (256 columns).
+//   * TMEM per CTA (512 columns): O_r [0,256), Q_r [256,384), S/P buffers
+//     [384,448) and [448,512) (double-buffered so QK^T of tile j+1 overlaps the
+//     softmax of tile j).
+//   * Online softmax in the base-2 domain with a lazy rescale: the running max
+//     only moves (and O is rescaled in TMEM) when a tile's max exceeds it by more
+//     than 8, so P <= 2^8.
+//   * Warp roles per CTA: warps 0-3 softmax / epilogue (thread = head = TMEM
+//     lane), warp 4 TMA producer, warp 5 MMA issuer.  Every wait is bounded; on
+//     a timeout the kernel sets MLA_CHECK_TIMEOUT, drains and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kStages = 3;                 // cache tiles in flight per CTA
+constexpr int kChunkBytes = kPage * 128;   // one 64-token x 64-column bf16 box (SW128): 8 KB
+constexpr int kStageBytes = 5 * kChunkBytes;
+constexpr int kQpeBytes = kMaxHeads * 128;             // 128 heads x 64 bf16, SW128 K-major
+constexpr int kRecvBytes = kMaxHeads * kPage * 4;      // partial scores, 128 x 64 fp32
+constexpr int kOffStages = 0;
+constexpr int kOffQpe = kOffStages + kStages * kStageBytes;
+constexpr int kOffRecv = kOffQpe + kQpeBytes;
+constexpr int kOffBars = kOffRecv + 2 * kRecvBytes;
+constexpr int kSmemBytes = kOffBars + 1024 + 1024;    // + barriers / flags, + alignment slack
+constexpr int kThreads = 192;
+
+// TMEM column map
+constexpr uint32_t kTmO = 0;
+constexpr uint32_t kTmQ = 256;
+constexpr uint32_t kTmS = 384;             // buffer b at kTmS + 64 b
+
+struct Bars {                               // mbarriers (8 bytes each) and flags
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t sfull[2];
+  uint64_t pfull[2];
+  uint64_t odone;                           // one phase per P . C tile
+  uint64_t ofinal;                          // single phase: the last P . C tile has landed
+  uint64_t recvfull[2];
+  uint64_t peerfree[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 1024, "barrier block");
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void fail_timeout(Bars* bars, unsigned* check) {
+  if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __restrict__ ctx_len, int n_h,
+                 const int32_t* __restrict__ block_table, int bt_stride, float scale_log2, float out_scale,
+                 Workspace ws, unsigned* check) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned base: swizzle atoms and TMA destinations need it
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(smem);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
+  volatile int* abort_flag = &bars->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+  const int unit_idx = blockIdx.x >> 1;
+  if (unit_idx >= ws.counters[0]) return;   // both CTAs of the cluster leave together
+  const Unit unit = ws.units[unit_idx];
+  const int b = unit.b;
+  const int L = ctx_len[b];
+  const int t_end = min(unit.page_end * kPage, L);
+  const int n_tiles = unit.page_end - unit.page_begin;
+  const int n_chunks = rank == 0 ? 4 : 5;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(smem_u32(&bars->full[s]), 1); mbar_init(smem_u32(&bars->empty[s]), 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->sfull[i]), 1);
+      mbar_init(smem_u32(&bars->pfull[i]), 4);
+      mbar_init(smem_u32(&bars->recvfull[i]), 1);
+      mbar_init(smem_u32(&bars->peerfree[i]), 4);
+    }
+    mbar_init(smem_u32(&bars->odone), 1);
+    mbar_init(smem_u32(&bars->ofinal), 1);
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&bars->tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) prefetch_tmap(&tmap);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  // ---- absorbed query of this CTA: latent half -> TMEM (A operand), RoPE part -> smem (CTA 1)
+  if (warp < 4) {
+    const int h = tid;
+    const bool live = h < n_h;
+    const uint4* src = reinterpret_cast<const uint4*>(ws.q_abs + ((size_t)b * n_h + (live ? h : 0)) * kRow);
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+    for (int part = 0; part < 4; ++part) {        // 4 x 32 columns = 256 bf16
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = live ? src[rank * 32 + part * 8 + i] : make_uint4(0, 0, 0, 0);
+        r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+      }
+      tmem_st32(lane_addr + kTmQ + 32 * part, r);
+    }
+    if (rank == 1) {
+      uint8_t* qpe = smem + kOffQpe;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 v = live ? src[64 + k] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qpe + h * 128 + ((k ^ (h & 7)) * 16)) = v;
+      }
+      fence_proxy_async_smem();
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();              // peer barriers initialised before any remote arrive / st.async
+  tc_fence_after();
+
+  const uint32_t stage0 = sbase + kOffStages;
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int32_t* bt_row = block_table + (size_t)b * bt_stride + unit.page_begin;
+      const uint32_t bytes = (uint32_t)(n_chunks * kChunkBytes);
+      int issued = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages && !mbar_wait(smem_u32(&bars->empty[s]), ((j / kStages) & 1) ^ 1, abort_flag)) {
+          fail_timeout(bars, check);
+          break;
+        }
+        const int page = bt_row[j];
+        const uint32_t full = smem_u32(&bars->full[s]);
+        mbar_arrive_expect_tx(full, bytes);
+        for (int c = 0; c < n_chunks; ++c)
+          tma_load_2d(stage0 + s * kStageBytes + c * kChunkBytes, &tmap, (int)(rank * 256 + c * 64), page * kPage,
+                      full);
+        issued = j + 1;
+      }
+      // drain: every load issued has landed before the CTA may exit
+      for (int j = max(0, issued - kStages); j < issued; ++j) {
+        volatile int never = 0;
+        mbar_wait(smem_u32(&bars->full[j % kStages]), (j / kStages) & 1, &never);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16_f32(128, 64, false, false);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
+      const uint32_t qpe = sbase + kOffQpe;
+      bool ok = true;
+      for (int j = 0; j <= n_tiles && ok; ++j) {
+        if (j < n_tiles) {
+          const int s = j % kStages, bb = j & 1;
+          if (!mbar_wait(smem_u32(&bars->full[s]), (j / kStages) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = stage0 + s * kStageBytes;
+          const uint32_t d = tmem + kTmS + 64 * bb;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            mma_ts(d, tmem + kTmQ + 8 * k, sdesc_sw128(st + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024),
+                   idesc_qk, k > 0);
+          if (rank == 1) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(d, sdesc_sw128(qpe + 32 * k, 16, 1024), sdesc_sw128(st + 4 * kChunkBytes + 32 * k, 16, 1024),
+                     idesc_qk, 1);
+          }
+          mma_commit(smem_u32(&bars->sfull[bb]));
+        }
+        if (j >= 1) {
+          const int jj = j - 1, s = jj % kStages, bb = jj & 1;
+          if (!mbar_wait(smem_u32(&bars->pfull[bb]), (jj >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = stage0 + s * kStageBytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + kTmO, tmem + kTmS + 64 * bb + 8 * k, sdesc_sw128(st + 2048 * k, kChunkBytes, 1024),
+                   idesc_pv, (jj > 0 || k > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bars->empty[s]));
+          mma_commit(smem_u32(&bars->odone));
+          if (jj == n_tiles - 1) mma_commit(smem_u32(&bars->ofinal));
+        }
+      }
+      if (!ok) fail_timeout(bars, check);
+      mma_commit(smem_u32(&bars->drain));      // arrives once every MMA issued above has finished
+      volatile int never = 0;
+      mbar_wait(smem_u32(&bars->drain), 0, &never);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue (thread = head)
+    const int h = tid;
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t recv_local = sbase + kOffRecv;
+    const uint32_t recv_peer = map_to_rank(recv_local, peer);
+    float m_used = -INFINITY, l_sum = 0.0f;
+    bool ok = true;
+    int armed = 0;
+    // waits are made warp-uniform: tcgen05.ld / st below are .sync.aligned
+    auto wait_cta = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, abort_flag));
+    };
+    auto wait_cluster = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait<true>(smem_u32(bar), parity, abort_flag));
+    };
+    for (int j = 0; j < n_tiles; ++j) {
+      const int bb = j & 1;
+      const int valid = min(kPage, t_end - (unit.page_begin + j) * kPage);
+      if (!wait_cta(&bars->sfull[bb], (j >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      float sc[64];
+      {
+        uint32_t r[32];
+        tmem_ld32(lane_addr + kTmS + 64 * bb, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sc[i] = __uint_as_float(r[i]);
+        tmem_ld32(lane_addr + kTmS + 64 * bb + 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sc[32 + i] = __uint_as_float(r[i]);
+      }
+      // send this CTA's partial scores to the peer (row h, 16-byte chunks swizzled by h)
+      if (j >= 2 && !wait_cluster(&bars->peerfree[bb], ((j >> 1) & 1) ^ 1)) { ok = false; break; }
+      const uint32_t peer_bar = map_to_rank(smem_u32(&bars->recvfull[bb]), peer);
+      const uint32_t dst = recv_peer + bb * kRecvBytes + h * 256;
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        st_async_v4(dst + ((q ^ (h & 15)) * 16), sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3], peer_bar);
+      if (tid == 0) mbar_arrive_expect_tx(smem_u32(&bars->recvfull[bb]), (uint32_t)kRecvBytes);
+      armed = j + 1;
+      if (!wait_cluster(&bars->recvfull[bb], (j >> 1) & 1)) { ok = false; break; }
+      {
+        const float4* rp = reinterpret_cast<const float4*>(smem + kOffRecv + bb * kRecvBytes + h * 256);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const float4 v = rp[q ^ (h & 15)];
+          // S = S_lo + S_hi in the same order on both CTAs (IEEE addition commutes)
+          sc[4 * q] += v.x; sc[4 * q + 1] += v.y; sc[4 * q + 2] += v.z; sc[4 * q + 3] += v.w;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&bars->peerfree[bb]), peer));
+
+      // a partial last page: rows past the context hold stale data; zero this CTA's latent
+      // rows there so P = 0 meets finite values in P . C
+      if (valid < kPage) {
+        uint8_t* st = smem + kOffStages + (j % kStages) * kStageBytes;
+        const int rows = kPage - valid;
+        for (int i = tid; i < 4 * rows * 8; i += 128) {
+          const int c = i / (rows * 8), rr = valid + (i / 8) % rows, k = i % 8;
+          *reinterpret_cast<uint4*>(st + c * kChunkBytes + rr * 128 + k * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        sc[i] = i < valid ? sc[i] * scale_log2 : -INFINITY;
+        mt = fmaxf(mt, sc[i]);
+      }
+      const bool grow = mt > m_used + 8.0f;
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // rescale this warp's rows of O once P . C of the previous tile has landed
+        if (!wait_cta(&bars->odone, (j - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const float alpha = grow ? exp2f(m_used - mt) : 1.0f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(lane_addr + kTmO + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(lane_addr + kTmO + c0, r);
+        }
+        tmem_st_wait();
+      }
+      if (grow) {
+        l_sum *= exp2f(m_used - mt);
+        m_used = mt;
+      }
+      uint32_t pk[32];
+      float psum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = exp2f(sc[2 * i] - m_used), p1 = exp2f(sc[2 * i + 1] - m_used);
+        psum += p0 + p1;
+        pk[i] = bf16x2_bits(p0, p1);
+      }
+      l_sum += psum;
+      tmem_st32(lane_addr + kTmS + 64 * bb, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->pfull[bb]));
+    }
+    if (!ok) fail_timeout(bars, check);
+    // ---- epilogue: this CTA's 256 latent columns of every head
+    // (odone cannot be used here: when the last tile's softmax ends, P . C of the tile
+    // before it may still be pending, and a parity wait two phases behind is ambiguous)
+    if (ok && n_tiles > 0 && wait_cta(&bars->ofinal, 0)) {
+      tc_fence_after();
+      const float inv = out_scale / l_sum;
+      const bool live = h < n_h;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 256; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(lane_addr + kTmO + c0, r);
+        tmem_ld_wait();
+        if (!live) continue;
+        if (unit.part < 0) {
+          uint4* dst = reinterpret_cast<uint4*>(ws.o_lat + ((size_t)b * n_h + h) * kDc + rank * 256 + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float* f = reinterpret_cast<const float*>(r + 8 * i);
+            dst[i] = make_uint4(bf16x2_bits(f[0] * inv, f[1] * inv), bf16x2_bits(f[2] * inv, f[3] * inv),
+                                bf16x2_bits(f[4] * inv, f[5] * inv), bf16x2_bits(f[6] * inv, f[7] * inv));
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(ws.part_o + ((size_t)unit.part * n_h + h) * kDc + rank * 256 + c0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float* f = reinterpret_cast<const float*>(r + 4 * i);
+            dst[i] = make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+          }
+        }
+      }
+      if (live && unit.part >= 0 && rank == 0)
+        ws.part_lse[(size_t)unit.part * n_h + h] = (m_used + log2f(l_sum)) * 0.69314718055994531f;
+    } else if (ok && n_tiles > 0) {
+      fail_timeout(bars, check);
+    }
+    // a timed-out CTA still lets in-flight partial-score stores from the peer land
+    if (!ok && tid == 0 && armed > 0) {
+      volatile int never = 0;
+      mbar_wait<true>(smem_u32(&bars->recvfull[(armed - 1) & 1]), ((armed - 1) >> 1) & 1, &never);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// Tensor map of a bf16 cache [num_pages * 64 rows][576]: 64 x 64 boxes, 128-byte swizzle.
+cudaError_t make_cache_tensor_map(const void* cache, int num_pages, CUtensorMap* map) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)num_pages * kPage};
+  const cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+  const cuuint32_t elem[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, elem,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+namespace {
+cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, const int32_t* block_table, int bt_stride,
+                             const CUtensorMap& map, const Workspace& ws, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const float scale_log2 = h.scale * 1.4426950408889634f;
+  decode_tc_kernel<<<2 * ws.max_units, kThreads, kSmemBytes, st>>>(map, ctx_len, h.cfg.n_h, block_table, bt_stride,
+                                                                   scale_log2, 1.0f, ws, h.check_word);
+  return cudaGetLastError();
+}
+}  // namespace
+
+// Decode-kernel dispatch: the tensor-core kernel for a bf16 cache; the FP8 cache
+// still runs the CUDA-core kernel.
+cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table,
+                          int bt_stride, const void* cache, int num_pages, const Workspace& ws, cudaStream_t st) {
+  if (h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3)
+    return launch_decode_simt(h, ctx_len, batch, block_table, bt_stride, cache, num_pages, ws, st);
+  Handle& hm = const_cast<Handle&>(h);
+  if (hm.tmap_cache != cache || hm.tmap_pages != num_pages) {
+    cudaError_t e = make_cache_tensor_map(cache, num_pages, reinterpret_cast<CUtensorMap*>(hm.tmap));
+    if (e != cudaSuccess) return e;
+    hm.tmap_cache = cache;
+    hm.tmap_pages = num_pages;
+  }
+  return launch_decode_tc(h, ctx_len, block_table, bt_stride, *reinterpret_cast<const CUtensorMap*>(hm.tmap), ws, st);
+}
+
+}  // namespace mla
