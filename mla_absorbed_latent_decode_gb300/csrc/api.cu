@@ -198,6 +198,7 @@ mla_status_t mla_create(const mla_config_t* cfg, const void* w_uk, const void* w
     return cleanup(cuda_fail(e, "copy rope table"));
   for (int i = 0; i < 8; ++i)
     if ((e = cudaEventCreate(&h->ev[i])) != cudaSuccess) return cleanup(cuda_fail(e, "cudaEventCreate"));
+  if ((e = mla::prepare_weight_maps(*h)) != cudaSuccess) return cleanup(cuda_fail(e, "weight tensor maps"));
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cleanup(cuda_fail(e, "mla_create sync"));
   *out = reinterpret_cast<mla_handle_t>(h);
   return MLA_OK;

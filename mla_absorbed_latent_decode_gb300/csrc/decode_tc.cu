@@ -19,10 +19,12 @@
 //   * QK^T is split along K: each CTA computes a partial score tile
 //       S_r[128 heads x 64 tokens] = Q_r . C_r^T
 //     with Q_r's latent part resident in TMEM (A operand) and, on CTA 1, the
-//     RoPE part of the query in shared memory.  The two partials are exchanged
-//     through distributed shared memory (st.async, 32 KB per tile each way) and
-//     both CTAs form the same full score S = S_lo + S_hi, so both compute
-//     bit-identical softmax weights P.
+//     RoPE part of the query in shared memory.  Four "exchange" warps read S_r
+//     as soon as it lands, scale it to the base-2 softmax domain, round it to
+//     fp16 and st.async it into the peer's receive slot (16 KB per tile each
+//     way, 4 slots).  The softmax warps form x = fp16(x_lo) + fp16(x_hi) in the
+//     same order on both CTAs, so both compute bit-identical softmax weights.
+//     fp16 keeps 11 bits of a logit, finer than the bf16 P it feeds.
 //   * P (bf16) is written back into TMEM over S and used as the A operand of
 //     O_r[128 x 256] += P . C_r[64 tokens x 256 latent]; the same shared-memory
 //     tile is the B operand, read MN-major.  Each CTA accumulates its half of
@@ -34,10 +36,13 @@
 //     only moves (and O is rescaled in TMEM) when a tile's max exceeds it by more
 //     than 8, so P <= 2^8.
 //   * Warp roles per CTA: warps 0-3 softmax / epilogue (thread = head = TMEM
-//     lane), warp 4 TMA producer, warp 5 MMA issuer.  Every wait is bounded; on
-//     a timeout the kernel sets MLA_CHECK_TIMEOUT, drains and returns.
+//     lane), warps 4-7 score exchange, warp 8 TMA producer, warp 9 MMA issuer.
+//     Every wait is bounded; on a timeout the kernel sets MLA_CHECK_TIMEOUT,
+//     drains and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <cuda_fp16.h>
 
 #include "internal.cuh"
 #include "sm100_ptx.cuh"
@@ -51,13 +56,16 @@ constexpr int kStages = 3;                 // cache tiles in flight per CTA
 constexpr int kChunkBytes = kPage * 128;   // one 64-token x 64-column bf16 box (SW128): 8 KB
 constexpr int kStageBytes = 5 * kChunkBytes;
 constexpr int kQpeBytes = kMaxHeads * 128;             // 128 heads x 64 bf16, SW128 K-major
-constexpr int kRecvBytes = kMaxHeads * kPage * 4;      // partial scores, 128 x 64 fp32
+constexpr int kSlots = 4;                              // partial-score receive slots
+constexpr int kSlotBytes = kMaxHeads * kPage * 2;      // 128 x 64 fp16 = 16 KB
 constexpr int kOffStages = 0;
 constexpr int kOffQpe = kOffStages + kStages * kStageBytes;
 constexpr int kOffRecv = kOffQpe + kQpeBytes;
-constexpr int kOffBars = kOffRecv + 2 * kRecvBytes;
+constexpr int kOffBars = kOffRecv + kSlots * kSlotBytes;
 constexpr int kSmemBytes = kOffBars + 1024 + 1024;    // + barriers / flags, + alignment slack
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;                          // 4 softmax, 4 exchange, producer, MMA warps
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
 
 // TMEM column map
 constexpr uint32_t kTmO = 0;
@@ -65,14 +73,14 @@ constexpr uint32_t kTmQ = 256;
 constexpr uint32_t kTmS = 384;             // buffer b at kTmS + 64 b
 
 struct Bars {                               // mbarriers (8 bytes each) and flags
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t sfull[2];
-  uint64_t pfull[2];
-  uint64_t odone;                           // one phase per P . C tile
-  uint64_t ofinal;                          // single phase: the last P . C tile has landed
-  uint64_t recvfull[2];
-  uint64_t peerfree[2];
+  uint64_t full[kStages];                   // TMA tile landed                      (producer, tx)
+  uint64_t empty[kStages];                  // tile consumed by P . C               (MMA commit)
+  uint64_t sfull[2];                        // partial scores S_r(j) in TMEM        (MMA commit)
+  uint64_t xread[2];                        // exchange warps have read S_r(j)      (4 warps)
+  uint64_t pfull[2];                        // P(j) written over S_r(j)             (4 warps)
+  uint64_t odone;                           // one phase per P . C tile             (MMA commit)
+  uint64_t ofinal;                          // single phase: the last P . C landed  (MMA commit)
+  uint64_t recvfull[kSlots];                // peer's partial scores arrived        (1 + 16 KB tx)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -83,9 +91,25 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// (lo, hi) -> fp16x2, round to nearest, saturating at +-65504
+__device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 f16x2_to_f32(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
 
 __device__ __forceinline__ void fail_timeout(Bars* bars, unsigned* check) {
   if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+}
+
+// Load this thread's 64 partial scores of S buffer `bb` (two x32 loads, one wait).
+__device__ __forceinline__ void load_scores(uint32_t lane_addr, int bb, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+  tmem_ld32(lane_addr + kTmS + 64 * bb, r0);
+  tmem_ld32(lane_addr + kTmS + 64 * bb + 32, r1);
+  tmem_ld_wait();
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -116,21 +140,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
     for (int s = 0; s < kStages; ++s) { mbar_init(smem_u32(&bars->full[s]), 1); mbar_init(smem_u32(&bars->empty[s]), 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->sfull[i]), 1);
+      mbar_init(smem_u32(&bars->xread[i]), 4);
       mbar_init(smem_u32(&bars->pfull[i]), 4);
-      mbar_init(smem_u32(&bars->recvfull[i]), 1);
-      mbar_init(smem_u32(&bars->peerfree[i]), 4);
     }
+    for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&bars->recvfull[i]), 1);
     mbar_init(smem_u32(&bars->odone), 1);
     mbar_init(smem_u32(&bars->ofinal), 1);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) prefetch_tmap(&tmap);
+  if (warp == kWarpProducer && lane == 0) prefetch_tmap(&tmap);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -165,11 +189,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();              // peer barriers initialised before any remote arrive / st.async
+  cluster_sync();              // peer barriers initialised before any st.async into this CTA
   tc_fence_after();
 
   const uint32_t stage0 = sbase + kOffStages;
-  if (warp == 4) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const int32_t* bt_row = block_table + (size_t)b * bt_stride + unit.page_begin;
@@ -195,7 +219,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
         mbar_wait(smem_u32(&bars->full[j % kStages]), (j / kStages) & 1, &never);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 64, false, false);
@@ -240,12 +264,43 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
       volatile int never = 0;
       mbar_wait(smem_u32(&bars->drain), 0, &never);
     }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ exchange: S_r(j) -> peer
+    // As soon as QK^T of tile j lands, read this CTA's partial scores, scale them to the
+    // base-2 softmax domain, round to fp16 and store them into the peer's receive slot
+    // j % 4.  No "slot free" handshake is needed: this CTA's QK^T of tile j was issued
+    // only after its softmax finished tile j - 2, which had received the peer's tile
+    // j - 2, which the peer sent only after its own QK^T of tile j - 2, issued only after
+    // the peer's softmax finished tile j - 4 -- the last user of slot j % 4.
+    const int h = tid - 128;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    const uint32_t recv_peer = map_to_rank(sbase + kOffRecv, peer);
+    for (int j = 0; j < n_tiles; ++j) {
+      const int bb = j & 1, slot = j & (kSlots - 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sfull[bb]), (j >> 1) & 1, abort_flag))) break;
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      load_scores(lane_addr, bb, r0, r1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->xread[bb]));
+      uint32_t w[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        w[i] = f16x2_sat(__uint_as_float(r0[2 * i]) * scale_log2, __uint_as_float(r0[2 * i + 1]) * scale_log2);
+        w[16 + i] = f16x2_sat(__uint_as_float(r1[2 * i]) * scale_log2, __uint_as_float(r1[2 * i + 1]) * scale_log2);
+      }
+      const uint32_t dst = recv_peer + slot * kSlotBytes + h * 128;
+      const uint32_t peer_bar = map_to_rank(smem_u32(&bars->recvfull[slot]), peer);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_async_v4_b32(dst + ((q ^ (h & 7)) * 16), make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]),
+                        peer_bar);
+    }
   } else {
     // ------------------------------------------------------------ softmax + epilogue (thread = head)
     const int h = tid;
     const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t recv_local = sbase + kOffRecv;
-    const uint32_t recv_peer = map_to_rank(recv_local, peer);
     float m_used = -INFINITY, l_sum = 0.0f;
     bool ok = true;
     int armed = 0;
@@ -257,43 +312,42 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
       return __all_sync(0xffffffffu, mbar_wait<true>(smem_u32(bar), parity, abort_flag));
     };
     for (int j = 0; j < n_tiles; ++j) {
-      const int bb = j & 1;
+      const int bb = j & 1, slot = j & (kSlots - 1);
       const int valid = min(kPage, t_end - (unit.page_begin + j) * kPage);
+      if (tid == 0) mbar_arrive_expect_tx(smem_u32(&bars->recvfull[slot]), (uint32_t)kSlotBytes);
+      armed = j + 1;
       if (!wait_cta(&bars->sfull[bb], (j >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      float sc[64];
+      float x[64];
       {
-        uint32_t r[32];
-        tmem_ld32(lane_addr + kTmS + 64 * bb, r);
-        tmem_ld_wait();
+        uint32_t r0[32], r1[32];
+        load_scores(lane_addr, bb, r0, r1);
+        // own partial, rounded exactly as the exchange warps round the copy sent to the peer
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sc[i] = __uint_as_float(r[i]);
-        tmem_ld32(lane_addr + kTmS + 64 * bb + 32, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sc[32 + i] = __uint_as_float(r[i]);
-      }
-      // send this CTA's partial scores to the peer (row h, 16-byte chunks swizzled by h)
-      if (j >= 2 && !wait_cluster(&bars->peerfree[bb], ((j >> 1) & 1) ^ 1)) { ok = false; break; }
-      const uint32_t peer_bar = map_to_rank(smem_u32(&bars->recvfull[bb]), peer);
-      const uint32_t dst = recv_peer + bb * kRecvBytes + h * 256;
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        st_async_v4(dst + ((q ^ (h & 15)) * 16), sc[4 * q], sc[4 * q + 1], sc[4 * q + 2], sc[4 * q + 3], peer_bar);
-      if (tid == 0) mbar_arrive_expect_tx(smem_u32(&bars->recvfull[bb]), (uint32_t)kRecvBytes);
-      armed = j + 1;
-      if (!wait_cluster(&bars->recvfull[bb], (j >> 1) & 1)) { ok = false; break; }
-      {
-        const float4* rp = reinterpret_cast<const float4*>(smem + kOffRecv + bb * kRecvBytes + h * 256);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float4 v = rp[q ^ (h & 15)];
-          // S = S_lo + S_hi in the same order on both CTAs (IEEE addition commutes)
-          sc[4 * q] += v.x; sc[4 * q + 1] += v.y; sc[4 * q + 2] += v.z; sc[4 * q + 3] += v.w;
+        for (int i = 0; i < 16; ++i) {
+          float2 a = f16x2_to_f32(f16x2_sat(__uint_as_float(r0[2 * i]) * scale_log2,
+                                            __uint_as_float(r0[2 * i + 1]) * scale_log2));
+          float2 c = f16x2_to_f32(f16x2_sat(__uint_as_float(r1[2 * i]) * scale_log2,
+                                            __uint_as_float(r1[2 * i + 1]) * scale_log2));
+          x[2 * i] = a.x; x[2 * i + 1] = a.y; x[32 + 2 * i] = c.x; x[32 + 2 * i + 1] = c.y;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&bars->peerfree[bb]), peer));
+      if (!wait_cluster(&bars->recvfull[slot], (j >> 2) & 1)) { ok = false; break; }
+      {
+        // x = x_lo + x_hi in the same order on both CTAs (IEEE addition commutes)
+        const uint4* rp = reinterpret_cast<const uint4*>(smem + kOffRecv + slot * kSlotBytes + h * 128);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = rp[q ^ (h & 7)];
+          const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = f16x2_to_f32(ww[k]);
+            x[8 * q + 2 * k] += f.x;
+            x[8 * q + 2 * k + 1] += f.y;
+          }
+        }
+      }
 
       // a partial last page: rows past the context hold stale data; zero this CTA's latent
       // rows there so P = 0 meets finite values in P . C
@@ -310,15 +364,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
       float mt = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        sc[i] = i < valid ? sc[i] * scale_log2 : -INFINITY;
-        mt = fmaxf(mt, sc[i]);
+        if (i >= valid) x[i] = -INFINITY;
+        mt = fmaxf(mt, x[i]);
       }
       const bool grow = mt > m_used + 8.0f;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // rescale this warp's rows of O once P . C of the previous tile has landed
         if (!wait_cta(&bars->odone, (j - 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        const float alpha = grow ? exp2f(m_used - mt) : 1.0f;
+        const float alpha = grow ? ex2_approx(m_used - mt) : 1.0f;
 #pragma unroll 1
         for (int c0 = 0; c0 < 256; c0 += 32) {
           uint32_t r[32];
@@ -331,18 +385,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
         tmem_st_wait();
       }
       if (grow) {
-        l_sum *= exp2f(m_used - mt);
+        l_sum *= ex2_approx(m_used - mt);
         m_used = mt;
       }
       uint32_t pk[32];
       float psum = 0.0f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float p0 = exp2f(sc[2 * i] - m_used), p1 = exp2f(sc[2 * i + 1] - m_used);
+        const float p0 = ex2_approx(x[2 * i] - m_used), p1 = ex2_approx(x[2 * i + 1] - m_used);
         psum += p0 + p1;
         pk[i] = bf16x2_bits(p0, p1);
       }
       l_sum += psum;
+      // P overwrites S_r(j): the exchange warps must have read it
+      if (!wait_cta(&bars->xread[bb], (j >> 1) & 1)) { ok = false; break; }
       tmem_st32(lane_addr + kTmS + 64 * bb, pk);
       tmem_st_wait();
       tc_fence_before();
@@ -388,13 +444,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
     // a timed-out CTA still lets in-flight partial-score stores from the peer land
     if (!ok && tid == 0 && armed > 0) {
       volatile int never = 0;
-      mbar_wait<true>(smem_u32(&bars->recvfull[(armed - 1) & 1]), ((armed - 1) >> 1) & 1, &never);
+      mbar_wait<true>(smem_u32(&bars->recvfull[(armed - 1) & (kSlots - 1)]), ((armed - 1) >> 2) & 1, &never);
     }
   }
   tc_fence_before();
   __syncthreads();
   cluster_sync();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {

@@ -64,9 +64,14 @@ struct Handle {
   cudaEvent_t ev[8];
   int n_ev_recorded;
   alignas(64) unsigned char tmap[128];   // TMA descriptor (CUtensorMap) of the last cache seen
+  alignas(64) unsigned char tmap_wuk[128];  // TMA descriptors of the handle's weight copies
+  alignas(64) unsigned char tmap_wuv[128];
   const void* tmap_cache;
   int tmap_pages;
 };
+
+// TMA descriptors of the weights (built once in mla_create).
+cudaError_t prepare_weight_maps(Handle& h);
 
 // Workspace sizing and carving (host).
 size_t workspace_bytes(const Handle& h, int batch, Workspace* carve, char* base);

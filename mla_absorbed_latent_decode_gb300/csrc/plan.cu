@@ -8,8 +8,10 @@
 //                lies in [0, num_pages); otherwise the sequence gets no unit,
 //                its output is zeroed and a check bit is set.
 //   pages(b)   = ceil(ctx_len[b] / 64) for a valid sequence, else 0.
-//   target     = max(1, ceil(sum_b pages(b) / num_pairs)): pages one SM pair
-//                should stream so that every pair gets about the same share.
+//   target     = the smallest page count >= ceil(sum_b pages(b) / num_pairs) with
+//                sum_b ceil(pages(b) / target) <= max(num_pairs, valid sequences):
+//                pages one SM pair streams, chosen so that the units fit in one wave
+//                of SM pairs (no pair runs two units back to back while others idle).
 //   nsplit(b)  = ceil(pages(b) / target), or min(forced, pages(b)) when the
 //                split count is forced.
 //   unit j of b covers pages [j * pages(b) / nsplit(b), (j+1) * pages(b) / nsplit(b)).
@@ -74,14 +76,53 @@ __device__ int block_exclusive_scan(int v, int* red, int* total) {
   return r;
 }
 
+
+// Per-thread partial counts over this thread's sequences (pages(b) is parked in seqs[b].nsplit).
+__device__ int count_units(int B, const Workspace& ws, int target) {
+  int n = 0;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int np = ws.seqs[b].nsplit;
+    n += np == 0 ? 0 : (np + target - 1) / target;
+  }
+  return n;
+}
+__device__ int count_valid(int B, const Workspace& ws) {
+  int n = 0;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) n += ws.seqs[b].nsplit > 0;
+  return n;
+}
+__device__ int warp_max_pages(int B, const Workspace& ws) {
+  int m = 0;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) m = max(m, ws.seqs[b].nsplit);
+  return m;
+}
+__device__ int block_max(int v, int* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) t = max(t, __shfl_xor_sync(0xffffffffu, t, o));
+    if (threadIdx.x == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
     const int32_t* __restrict__ ctx_len, int B, int max_ctx, const int32_t* __restrict__ block_table,
     int bt_stride, int num_pages, int num_pairs, int forced, Workspace ws, unsigned* check) {
   __shared__ int red[64];
-  // 1. validate and count pages; pages(b) parked in seqs[b].nsplit
+  // 1. validate and count pages, one warp per sequence (lanes check page ids in parallel);
+  //    pages(b) is parked in seqs[b].nsplit
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   unsigned flags = 0;
   int my_pages = 0;
-  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+  for (int b = warp; b < B; b += nwarps) {
     const int L = ctx_len[b];
     int np = 0;
     if (L < 1 || L > max_ctx) {
@@ -89,17 +130,35 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
     } else {
       np = (L + kPage - 1) / kPage;
       const int32_t* row = block_table + (size_t)b * bt_stride;
-      for (int i = 0; i < np; ++i) {
+      bool bad = false;
+      for (int i = lane; i < np; i += 32) {
         const int pg = row[i];
-        if (pg < 0 || pg >= num_pages) { flags |= kCheckPageId; np = 0; break; }
+        bad |= (pg < 0 || pg >= num_pages);
       }
+      if (__any_sync(0xffffffffu, bad)) { flags |= kCheckPageId; np = 0; }
     }
-    ws.seqs[b].nsplit = np;
-    my_pages += np;
+    if (lane == 0) {
+      ws.seqs[b].nsplit = np;
+      my_pages += np;
+    }
   }
-  if (flags) atomicOr(check, flags);
+  if (flags && lane == 0) atomicOr(check, flags);
+  __syncthreads();   // seqs[].nsplit written by other warps is read below
   const int total_pages = block_sum(my_pages, red);
-  const int target = max(1, (total_pages + num_pairs - 1) / max(1, num_pairs));
+  const int max_pages = block_max(warp_max_pages(B, ws), red);
+  // Smallest page target whose split count fits in one wave of SM pairs: start from an
+  // even share of the pages and grow it (binary search) until sum_b ceil(pages_b / target)
+  // <= max(num_pairs, number of valid sequences).  With at least as many sequences as
+  // pairs nothing is split.
+  const int pairs = max(1, num_pairs);
+  int lo = max(1, (total_pages + pairs - 1) / pairs), hi = max(lo, max_pages);
+  const int valid_seqs = block_sum(count_valid(B, ws), red);
+  const int budget = max(pairs, valid_seqs);
+  while (lo < hi) {
+    const int mid = lo + (hi - lo) / 2;
+    if (block_sum(count_units(B, ws, mid), red) <= budget) hi = mid; else lo = mid + 1;
+  }
+  const int target = lo;
 
   // 2. split counts, prefix-summed chunk by chunk into first_unit
   int base = 0;

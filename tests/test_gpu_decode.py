@@ -68,7 +68,11 @@ def plan_reference(ctx_len, bt, num_pages, max_ctx, num_pairs, forced=0):
             if any(not (0 <= bt[b][i] < num_pages) for i in range(np_b)):
                 np_b = 0
         pages.append(np_b)
-    target = max(1, -(-sum(pages) // max(1, num_pairs)))
+    pairs = max(1, num_pairs)
+    budget = max(pairs, sum(1 for n in pages if n > 0))
+    target = max(1, -(-sum(pages) // pairs))
+    while sum(-(-n // target) for n in pages if n > 0) > budget:
+        target += 1
     units, seqs = [], []
     for b, np_b in enumerate(pages):
         ns = 0 if np_b == 0 else (min(forced, np_b) if forced else -(-np_b // target))
