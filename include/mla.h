@@ -94,7 +94,7 @@ typedef struct mla_config {
   int32_t d_v;          /* value width per head.  Built: 128.                             */
   int32_t page_size;    /* tokens per cache page.  Built: 64.                             */
   int32_t cache_dtype;  /* mla_cache_dtype_t.                                             */
-  int32_t max_position; /* size of the RoPE table: positions 0..max_position-1.  <= 2^22. */
+  int32_t max_position; /* size of the RoPE table: positions 0..max_position-1.  <= 2^20. */
   float rope_base;      /* RoPE base (10000 for the configurations here).                 */
   float softmax_scale;  /* EXCEPTION: 0 means 1/sqrt(d_nope + d_rope).                    */
   float fp8_scale;      /* EXCEPTION: mandatory (> 0) only for MLA_CACHE_FP8_E4M3, where a
@@ -113,7 +113,7 @@ typedef struct mla_config {
  *           so the caller may free w_uk / w_uv afterwards.
  *   out     receives the handle.
  *
- * The handle owns re-laid-out device copies of both weights, an fp32 RoPE
+ * The handle owns device copies of both weights (as given), an fp32 RoPE
  * cos/sin table (angles computed in float64 on the host) and a device check
  * word.  Errors: MLA_ERR_MISSING_FIELD, MLA_ERR_INVALID_ARG (NULL pointer),
  * MLA_ERR_UNSUPPORTED (shape other than the built ones, or not an sm_103
@@ -206,7 +206,7 @@ mla_status_t mla_set_option(mla_handle_t h, int32_t option, int64_t value);
 /*
  * mla_profile_read -- with MLA_OPT_PROFILE on, synchronize and return the
  * device time in milliseconds of each kernel of the last mla_decode call, in
- * launch order (plan, q-absorb, decode, combine + W_UV).  *count receives the
+ * launch order (q-absorb, plan, decode, combine + W_UV).  *count receives the
  * number of kernels; at most `capacity` values are written.  Names of the
  * kernels come from mla_profile_kernel_name.
  */

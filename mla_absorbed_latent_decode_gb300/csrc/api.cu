@@ -37,7 +37,7 @@ mla_status_t cuda_fail(cudaError_t e, const char* what) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-const char* kKernelNames[] = {"mla_plan", "mla_q_absorb", "mla_decode_splitkv", "mla_combine_uv"};
+const char* kKernelNames[] = {"mla_q_absorb", "mla_plan", "mla_decode_splitkv", "mla_combine_uv"};
 constexpr int kNumKernels = 4;
 
 mla_status_t check_config(const mla_config_t* c) {
@@ -284,12 +284,14 @@ mla_status_t mla_decode(mla_handle_t hh, const void* q, const int32_t* ctx_len, 
   int ev = 0;
   auto mark = [&]() { if (prof) cudaEventRecord(h->ev[ev++], st); };
   cudaError_t e;
-  mark();
-  if ((e = mla::launch_plan(*h, ctx_len, batch, max_ctx, block_table, bt_stride, num_pages, ws, st)) != cudaSuccess)
-    return cuda_fail(e, "plan launch");
+  // Kernel order: query absorption, then the planner (it overlaps the absorption; see
+  // plan.cu), then the split-KV decode, then the merge + value up-projection.
   mark();
   if ((e = mla::launch_q_absorb(*h, static_cast<const __nv_bfloat16*>(q), ctx_len, batch, ws, st)) != cudaSuccess)
     return cuda_fail(e, "q_absorb launch");
+  mark();
+  if ((e = mla::launch_plan(*h, ctx_len, batch, max_ctx, block_table, bt_stride, num_pages, ws, st)) != cudaSuccess)
+    return cuda_fail(e, "plan launch");
   mark();
   if ((e = mla::launch_decode(*h, ctx_len, batch, block_table, bt_stride, cache, num_pages, ws, st)) != cudaSuccess)
     return cuda_fail(e, "decode launch");

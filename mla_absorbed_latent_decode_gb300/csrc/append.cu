@@ -13,6 +13,7 @@
 #include <cuda_fp8.h>
 
 #include "internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace mla {
 namespace {
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     int max_position, float fp8_scale, unsigned* check) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  sm100::griddep_wait();
+  sm100::griddep_launch_dependents();
   if (warp >= n) return;
   const int s = seq[warp];
   const int p = pos[warp];
@@ -112,14 +115,12 @@ cudaError_t launch_kv_append(const Handle& h, const __nv_bfloat16* rows, const i
   const int threads = 256;
   const int blocks = (int)(((long long)n * 32 + threads - 1) / threads);
   if (h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3)
-    kv_append_kernel<true><<<blocks, threads, 0, st>>>(rows, seq, pos, n, block_table, bt_rows, bt_stride,
-                                                       static_cast<uint8_t*>(cache), num_pages, h.rope_cs,
-                                                       h.cfg.max_position, h.cfg.fp8_scale, h.check_word);
-  else
-    kv_append_kernel<false><<<blocks, threads, 0, st>>>(rows, seq, pos, n, block_table, bt_rows, bt_stride,
-                                                        static_cast<uint8_t*>(cache), num_pages, h.rope_cs,
-                                                        h.cfg.max_position, 0.0f, h.check_word);
-  return cudaGetLastError();
+    return launch_pdl(kv_append_kernel<true>, dim3(blocks), dim3(threads), 0, st, rows, seq, pos, n, block_table,
+                      bt_rows, bt_stride, static_cast<uint8_t*>(cache), num_pages, (const float2*)h.rope_cs,
+                      h.cfg.max_position, h.cfg.fp8_scale, h.check_word);
+  return launch_pdl(kv_append_kernel<false>, dim3(blocks), dim3(threads), 0, st, rows, seq, pos, n, block_table,
+                    bt_rows, bt_stride, static_cast<uint8_t*>(cache), num_pages, (const float2*)h.rope_cs,
+                    h.cfg.max_position, 0.0f, h.check_word);
 }
 
 }  // namespace mla

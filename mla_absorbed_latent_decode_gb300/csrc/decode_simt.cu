@@ -13,6 +13,7 @@
 #include <cuda_fp8.h>
 
 #include "internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace mla {
 namespace {
@@ -54,6 +55,8 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
   float* a_s = l_s + kHeadsPerCta;
 
   const int u = blockIdx.x;
+  sm100::griddep_wait();
+  sm100::griddep_launch_dependents();
   if (u >= ws.counters[0]) return;
   const Unit unit = ws.units[u];
   const int b = unit.b;
@@ -182,9 +185,8 @@ cudaError_t launch_decode_simt(const Handle& h, const int32_t* ctx_len, int batc
   const float sscale = h.scale * (fp8 ? h.cfg.fp8_scale : 1.0f);
   const float oscale = fp8 ? h.cfg.fp8_scale : 1.0f;
   dim3 grid(ws.max_units, (h.cfg.n_h + kHeadsPerCta - 1) / kHeadsPerCta);
-  kern<<<grid, kThreads, kSmemTotal, st>>>(ctx_len, h.cfg.n_h, block_table, bt_stride,
-                                           static_cast<const uint8_t*>(cache), sscale, oscale, ws);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads), kSmemTotal, st, ctx_len, h.cfg.n_h, block_table, bt_stride,
+                    static_cast<const uint8_t*>(cache), sscale, oscale, ws);
 }
 
 }  // namespace mla

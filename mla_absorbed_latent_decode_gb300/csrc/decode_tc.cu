@@ -128,6 +128,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int unit_idx = blockIdx.x >> 1;
+  griddep_wait();                           // plan, absorbed queries and cache rows are inputs
+  griddep_launch_dependents();
   if (unit_idx >= ws.counters[0]) return;   // both CTAs of the cluster leave together
   const Unit unit = ws.units[unit_idx];
   const int b = unit.b;
@@ -491,9 +493,8 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, const int3
     attr = true;
   }
   const float scale_log2 = h.scale * 1.4426950408889634f;
-  decode_tc_kernel<<<2 * ws.max_units, kThreads, kSmemBytes, st>>>(map, ctx_len, h.cfg.n_h, block_table, bt_stride,
-                                                                   scale_log2, 1.0f, ws, h.check_word);
-  return cudaGetLastError();
+  return launch_pdl(decode_tc_kernel, dim3(2 * ws.max_units), dim3(kThreads), kSmemBytes, st, map, ctx_len,
+                    h.cfg.n_h, block_table, bt_stride, scale_log2, 1.0f, ws, h.check_word);
 }
 }  // namespace
 

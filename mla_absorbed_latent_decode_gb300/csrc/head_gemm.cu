@@ -12,10 +12,11 @@
 // log-sum-exp into o_lat (a standard identity, not on the pages); invalid
 // sequences get a zero latent, hence a zero output.
 //
-// One CTA per (head, 128-row block of M, tile of up to 256 sequences).  Operands
-// arrive by TMA in 128-byte-swizzled 64-column chunks through a small ring of
-// stages; one thread issues the loads and the MMAs; warps 0-3 (one per 32 TMEM
-// lanes) run the epilogue.
+// One CTA per (head, tile of sequences): the whole weight matrix of the head
+// (128 KB) and the tile's rows arrive by TMA in 128-byte-swizzled 64-column
+// boxes, all issued up front; one thread issues the MMAs; warps 0-3 (one per 32
+// TMEM lanes) run the epilogue.  The merge of split sequences runs in the
+// up-projection kernel while its weight loads are in flight.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -28,18 +29,17 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 128;
-constexpr int kMaxN = 256;
-constexpr int kRing = 4;                               // K-chunk stages
-constexpr int kAChunk = 128 * 128;                     // 128 rows x 64 bf16 = 16 KB
-constexpr int kBChunk = kMaxN * 128;                   // up to 256 rows x 64 bf16 = 32 KB
-constexpr int kStage = kAChunk + kBChunk;
-constexpr int kSmem = kRing * kStage + 1024 + 1024;
+constexpr int kBox = 128 * 128;                        // one 64-column x 128-row bf16 box: 16 KB
 
-enum Mode { kQAbsorb = 0, kUpProject = 1 };
+// query absorption: one CTA per (head, tile of up to 128 sequences), all four 128-row M blocks
+constexpr int kQaN = 128;
+constexpr int kQaSmem = 8 * kBox + 2 * kQaN * 128 + 1024 + 1024;
+// value up-projection: one CTA per (head, tile of up to 64 sequences)
+constexpr int kUpN = 64;
+constexpr int kUpSmem = 8 * kBox + 8 * kUpN * 128 + 1024 + 1024;
 
 struct GemmBars {
-  uint64_t full[kRing];
-  uint64_t empty[kRing];
+  uint64_t full;
   uint64_t done;
   uint32_t tmem_base;
   int abort;
@@ -50,100 +50,194 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// grid: (n_h, M blocks, N tiles).  Mode kQAbsorb: A = W_UK (MN-major, K = 128, M = 512);
-// mode kUpProject: A = W_UV (K-major, K = 512, M = 128).  B = one 64-column chunk of
-// q_nope / o_lat rows per K chunk, K-major.
-template <int kMode>
+// 3-D TMA of one 64-column chunk of B rows (tensor [B][n_h][width]: column, head, sequence).
+__device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap* m, int col, int h, int n0, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(col), "r"(h), "r"(n0), "r"(bar)
+      : "memory");
+}
+
+// Q_lat^T[h] = W_UK[h]^T . q_nope[:, h]^T for the sequences n0 .. n0 + n_pad of this CTA.
+// A = W_UK[h] read MN-major: the box (64 latent columns c, 128 rows n) is K-rows of 128 B.
 __global__ void __launch_bounds__(kThreads, 1)
-head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int B, int n_h,
-                 int n_pad, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ ctx_len,
-                 const float2* __restrict__ rope_cs, int max_position, __nv_bfloat16* __restrict__ out,
-                 unsigned* check) {
+q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q, int B, int n_h,
+                int n_pad, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ ctx_len,
+                const float2* __restrict__ rope_cs, int max_position, __nv_bfloat16* __restrict__ q_abs,
+                unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(smem);
-  GemmBars* bars = reinterpret_cast<GemmBars*>(smem + kRing * kStage);
+  GemmBars* bars = reinterpret_cast<GemmBars*>(smem + 8 * kBox + 2 * kQaN * 128);
   volatile int* abort_flag = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x, mb = blockIdx.y, n0 = blockIdx.z * kMaxN;
-  const int n_here = min(n_pad, kMaxN);              // MMA N (multiple of 16)
+  const int h = blockIdx.x, n0 = blockIdx.z * kQaN;
+  // every tile uses the TMA box height (rows past B arrive as zeros), so the transaction
+  // count and the chunk offsets match what the copies write
+  const int n_here = min(n_pad, kQaN);                 // multiple of 16
   const uint32_t b_bytes = (uint32_t)n_here * 128;
-
   if (tid == 0) {
-    for (int s = 0; s < kRing; ++s) { mbar_init(smem_u32(&bars->full[s]), 1); mbar_init(smem_u32(&bars->empty[s]), 1); }
+    mbar_init(smem_u32(&bars->full), 1);
     mbar_init(smem_u32(&bars->done), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0) { tmem_alloc(smem_u32(&bars->tmem_base), 256); tmem_relinquish(); }
+  if (warp == 0) { tmem_alloc(smem_u32(&bars->tmem_base), 512); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-
+  const uint32_t a_st = sbase, b_st = sbase + 8 * kBox;
   if (tid == 0) {
-    const uint32_t idesc = idesc_bf16_f32(128, n_here, kMode == kQAbsorb, false);
-    bool ok = true;
-    auto load_b = [&](uint32_t dst, int col, uint32_t bar) {
-      // B: rows = sequences n0 .., 64 columns of head h (3-D map: column, head, sequence)
-      asm volatile(
-          "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-              dst),
-          "l"(reinterpret_cast<uint64_t>(&tm_b)), "r"(col), "r"(h), "r"(n0), "r"(bar)
-          : "memory");
-    };
-    if (kMode == kQAbsorb) {
-      // one stage: A = two MN-major boxes (c = 128 mb + [0, 64) and + [64, 128), all 128 K rows n),
-      // B = two K-chunks of q_nope (n = [0, 64), [64, 128))
-      const uint32_t full = smem_u32(&bars->full[0]);
-      const uint32_t a_st = sbase, b_st = sbase + 2 * kAChunk;
-      mbar_arrive_expect_tx(full, 2u * kAChunk + 2u * b_bytes);
-      tma_load_2d(a_st, &tm_a, 128 * mb, 128 * h, full);
-      tma_load_2d(a_st + kAChunk, &tm_a, 128 * mb + 64, 128 * h, full);
-      load_b(b_st, 0, full);
-      load_b(b_st + b_bytes, 64, full);
-      if (!mbar_wait(full, 0, abort_flag)) ok = false;
-      tc_fence_after();
+    const uint32_t full = smem_u32(&bars->full);
+    mbar_arrive_expect_tx(full, 8u * kBox + 2u * b_bytes);
+    for (int i = 0; i < 8; ++i) tma_load_2d(a_st + i * kBox, &tm_w, 64 * i, 128 * h, full);   // c = 64 i ..
+    griddep_wait();                        // the queries may come from the previous kernel
+    griddep_launch_dependents();
+    load_rows(b_st, &tm_q, 0, h, n0, full);
+    load_rows(b_st + b_bytes, &tm_q, 64, h, n0, full);
+    bool ok = mbar_wait(full, 0, abort_flag);
+    tc_fence_after();
+    const uint32_t idesc = idesc_bf16_f32(128, n_here, true, false);
+    for (int mb = 0; mb < 4 && ok; ++mb)   // M block mb = latent c in [128 mb, 128 mb + 128): boxes 2 mb, 2 mb + 1
 #pragma unroll
-      for (int k = 0; k < 8 && ok; ++k)   // A: 16 K-rows of 128 B per step; the M halves are kAChunk apart
-        mma_ss(tmem, sdesc_sw128(a_st + 2048 * k, kAChunk, 1024),
+      for (int k = 0; k < 8; ++k)          // 16 K-rows (n) of 128 B per step; the two 64-wide M halves kBox apart
+        mma_ss(tmem + mb * n_here, sdesc_sw128(a_st + 2 * mb * kBox + 2048 * k, kBox, 1024),
                sdesc_sw128(b_st + (k >> 2) * b_bytes + 32 * (k & 3), 16, 1024), idesc, k > 0 ? 1u : 0u);
-    } else {
-      // ring over the 8 K-chunks of 64: A = W_UV rows v (K-major), B = o_lat rows (K-major)
-      auto issue = [&](int c) {
-        const int s = c % kRing;
-        const uint32_t full = smem_u32(&bars->full[s]);
-        mbar_arrive_expect_tx(full, (uint32_t)kAChunk + b_bytes);
-        const uint32_t a_dst = sbase + s * kStage;
-        tma_load_2d(a_dst, &tm_a, 64 * c, 128 * h, full);
-        load_b(a_dst + kAChunk, 64 * c, full);
-      };
-      for (int c = 0; c < 8 && c < kRing; ++c) issue(c);
-      for (int c = 0; c < 8 && ok; ++c) {
-        const int s = c % kRing;
-        if (!mbar_wait(smem_u32(&bars->full[s]), (c / kRing) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t a_st = sbase + s * kStage, b_st = a_st + kAChunk;
+    if (!ok && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+    mma_commit(smem_u32(&bars->done));
+  }
+  griddep_wait();
+  __syncwarp();
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort_flag));
+  tc_fence_after();
+  const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+  if (ok) {
+    for (int mb = 0; mb < 4; ++mb) {
+      for (int c0 = 0; c0 < n_here; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(lane_addr + mb * n_here + c0, r);
+        tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tmem, sdesc_sw128(a_st + 32 * k, 16, 1024), sdesc_sw128(b_st + 32 * k, 16, 1024), idesc,
-                 (c > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bars->empty[s]));
-        if (c + kRing < 8) {
-          if (!mbar_wait(smem_u32(&bars->empty[s]), (c / kRing) & 1, abort_flag)) { ok = false; break; }
-          issue(c + kRing);
+        for (int i = 0; i < 32; ++i) {
+          const int b = n0 + c0 + i;
+          if (c0 + i >= n_here || b >= B) break;
+          q_abs[((size_t)b * n_h + h) * kRow + 128 * mb + 32 * warp + lane] = __float2bfloat16_rn(__uint_as_float(r[i]));
         }
       }
     }
+  }
+  // RoPE part of the query, rotated at position ctx_len - 1 (clamped into the table)
+  for (int i = tid; i < min(B - n0, kQaN) * (kDr / 2); i += kThreads) {
+    const int b = n0 + i / (kDr / 2), p = i % (kDr / 2);
+    const int pos = min(max(ctx_len[b] - 1, 0), max_position - 1);
+    const __nv_bfloat162 x = reinterpret_cast<const __nv_bfloat162*>(q + ((size_t)b * n_h + h) * kDq + kDn)[p];
+    const float2 cs = rope_cs[(size_t)pos * (kDr / 2) + p];
+    const float x0 = __bfloat162float(x.x), x1 = __bfloat162float(x.y);
+    reinterpret_cast<uint32_t*>(q_abs + ((size_t)b * n_h + h) * kRow + kDc)[p] =
+        bf16x2_bits(x0 * cs.x - x1 * cs.y, x1 * cs.x + x0 * cs.y);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// out^T[h] = W_UV[h] . o_lat[:, h]^T for the sequences n0 .. n0 + n_pad of this CTA, after
+// merging split sequences' partials of head h into o_lat by log-sum-exp (zero latent for an
+// invalid sequence; unsplit sequences already hold theirs).
+__global__ void __launch_bounds__(kThreads, 1)
+up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_o, int B, int n_h,
+                  int n_pad, Workspace ws, __nv_bfloat16* __restrict__ out, unsigned* check) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(smem);
+  GemmBars* bars = reinterpret_cast<GemmBars*>(smem + 8 * kBox + 8 * kUpN * 128);
+  volatile int* abort_flag = &bars->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x, n0 = blockIdx.z * kUpN;
+  const int n_here = min(n_pad, kUpN);                 // the TMA box height, as above
+  const uint32_t b_bytes = (uint32_t)n_here * 128;
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars->full), 1);
+    mbar_init(smem_u32(&bars->done), 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) { tmem_alloc(smem_u32(&bars->tmem_base), 64); tmem_relinquish(); }
+  // weights do not depend on the merge: start their loads at once
+  const uint32_t a_st = sbase, b_st = sbase + 8 * kBox;
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(smem_u32(&bars->full), 8u * kBox + 8u * b_bytes);
+    for (int i = 0; i < 8; ++i) tma_load_2d(a_st + i * kBox, &tm_w, 64 * i, 128 * h, smem_u32(&bars->full));
+  }
+  griddep_wait();                          // the plan and latent sums come from earlier kernels
+  griddep_launch_dependents();
+  // merge pass: one warp per split (or invalid) sequence of this tile
+  bool wrote = false;
+  for (int j = warp; j < min(B - n0, kUpN); j += kThreads / 32) {
+    const int b = n0 + j;
+    const SeqPlan sp = ws.seqs[b];
+    if (sp.nsplit == 1) continue;
+    wrote = true;
+    uint4* dst = reinterpret_cast<uint4*>(ws.o_lat + ((size_t)b * n_h + h) * kDc) + 2 * lane;   // 16 values
+    if (sp.nsplit == 0) {
+      dst[0] = make_uint4(0, 0, 0, 0);
+      dst[1] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    float m = -INFINITY;
+    for (int k = 0; k < sp.nsplit; ++k)
+      m = fmaxf(m, ws.part_lse[(size_t)ws.units[sp.first_unit + k].part * n_h + h]);
+    float acc[16], den = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+    for (int k = 0; k < sp.nsplit; ++k) {
+      const int part = ws.units[sp.first_unit + k].part;
+      const float w = expf(ws.part_lse[(size_t)part * n_h + h] - m);
+      den += w;
+      const float4* src = reinterpret_cast<const float4*>(ws.part_o + ((size_t)part * n_h + h) * kDc) + 4 * lane;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 v = src[i];
+        acc[4 * i] = fmaf(w, v.x, acc[4 * i]);
+        acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
+        acc[4 * i + 2] = fmaf(w, v.z, acc[4 * i + 2]);
+        acc[4 * i + 3] = fmaf(w, v.w, acc[4 * i + 3]);
+      }
+    }
+    const float inv = 1.0f / den;
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = bf16x2_bits(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  if (wrote) fence_proxy_async_global();       // these rows are read below by TMA (async proxy)
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  if (tid == 0) {
+    const uint32_t full = smem_u32(&bars->full);
+    for (int i = 0; i < 8; ++i) load_rows(b_st + i * b_bytes, &tm_o, 64 * i, h, n0, full);
+    bool ok = mbar_wait(full, 0, abort_flag);
+    tc_fence_after();
+    const uint32_t idesc = idesc_bf16_f32(128, n_here, false, false);
+    for (int c = 0; c < 8 && ok; ++c)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tmem, sdesc_sw128(a_st + c * kBox + 32 * k, 16, 1024), sdesc_sw128(b_st + c * b_bytes + 32 * k, 16, 1024),
+               idesc, (c > 0 || k > 0) ? 1u : 0u);
     if (!ok && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
     mma_commit(smem_u32(&bars->done));
   }
   __syncwarp();
   const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort_flag));
   tc_fence_after();
-  // epilogue: lane = output row (c within the block / v), column = sequence
-  const int row = 32 * warp + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
   if (ok) {
     for (int c0 = 0; c0 < n_here; c0 += 32) {
@@ -153,73 +247,14 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int b = n0 + c0 + i;
-        if (b >= B) break;
-        const __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(r[i]));
-        if (kMode == kQAbsorb)
-          out[((size_t)b * n_h + h) * kRow + 128 * mb + row] = v;
-        else
-          out[((size_t)b * n_h + h) * kDv + row] = v;
+        if (c0 + i >= n_here || b >= B) break;
+        out[((size_t)b * n_h + h) * kDv + 32 * warp + lane] = __float2bfloat16_rn(__uint_as_float(r[i]));
       }
-    }
-  }
-  if (kMode == kQAbsorb && mb == 0) {
-    // RoPE part of the query, rotated at position ctx_len - 1 (clamped into the table)
-    for (int i = tid; i < min(B - n0, kMaxN) * (kDr / 2); i += kThreads) {
-      const int b = n0 + i / (kDr / 2), p = i % (kDr / 2);
-      const int pos = min(max(ctx_len[b] - 1, 0), max_position - 1);
-      const __nv_bfloat162 x = reinterpret_cast<const __nv_bfloat162*>(q + ((size_t)b * n_h + h) * kDq + kDn)[p];
-      const float2 cs = rope_cs[(size_t)pos * (kDr / 2) + p];
-      const float x0 = __bfloat162float(x.x), x1 = __bfloat162float(x.y);
-      reinterpret_cast<uint32_t*>(out + ((size_t)b * n_h + h) * kRow + kDc)[p] =
-          bf16x2_bits(x0 * cs.x - x1 * cs.y, x1 * cs.x + x0 * cs.y);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
-}
-
-// Log-sum-exp merge of split sequences' partials into o_lat (bf16); zero latent for
-// invalid sequences; unsplit sequences already hold their latent.  One warp per (b, h).
-__global__ void __launch_bounds__(128) combine_kernel(int B, int n_h, Workspace ws) {
-  const int b = blockIdx.x;
-  const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (h >= n_h) return;
-  const SeqPlan sp = ws.seqs[b];
-  if (sp.nsplit == 1) return;
-  uint4* dst = reinterpret_cast<uint4*>(ws.o_lat + ((size_t)b * n_h + h) * kDc) + 2 * lane;   // 16 values
-  if (sp.nsplit == 0) {
-    dst[0] = make_uint4(0, 0, 0, 0);
-    dst[1] = make_uint4(0, 0, 0, 0);
-    return;
-  }
-  float m = -INFINITY;
-  for (int k = 0; k < sp.nsplit; ++k)
-    m = fmaxf(m, ws.part_lse[(size_t)ws.units[sp.first_unit + k].part * n_h + h]);
-  float acc[16], den = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-  for (int k = 0; k < sp.nsplit; ++k) {
-    const int part = ws.units[sp.first_unit + k].part;
-    const float w = expf(ws.part_lse[(size_t)part * n_h + h] - m);
-    den += w;
-    const float4* src = reinterpret_cast<const float4*>(ws.part_o + ((size_t)part * n_h + h) * kDc) + 4 * lane;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 v = src[i];
-      acc[4 * i] = fmaf(w, v.x, acc[4 * i]);
-      acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
-      acc[4 * i + 2] = fmaf(w, v.z, acc[4 * i + 2]);
-      acc[4 * i + 3] = fmaf(w, v.w, acc[4 * i + 3]);
-    }
-  }
-  const float inv = 1.0f / den;
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = bf16x2_bits(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -265,22 +300,6 @@ cudaError_t rows_map(const void* base, int B, int n_h, int width, int n_box, CUt
              : cudaErrorInvalidValue;
 }
 
-template <int kMode>
-cudaError_t launch_head_gemm(const Handle& h, const CUtensorMap& ta, const CUtensorMap& tb, int batch,
-                             const __nv_bfloat16* q, const int32_t* ctx_len, __nv_bfloat16* out, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(head_gemm_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  const int n_pad = ((batch + 15) / 16) * 16;
-  dim3 grid(h.cfg.n_h, kMode == kQAbsorb ? 4 : 1, (batch + kMaxN - 1) / kMaxN);
-  head_gemm_kernel<kMode><<<grid, kThreads, kSmem, st>>>(ta, tb, batch, h.cfg.n_h, n_pad, q, ctx_len, h.rope_cs,
-                                                         h.cfg.max_position, out, h.check_word);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t prepare_weight_maps(Handle& h) {
@@ -291,22 +310,37 @@ cudaError_t prepare_weight_maps(Handle& h) {
 
 cudaError_t launch_q_absorb(const Handle& h, const __nv_bfloat16* q, const int32_t* ctx_len, int batch,
                             const Workspace& ws, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(q_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQaSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int n_pad = ((batch + 15) / 16) * 16;
   alignas(64) CUtensorMap tq;
-  cudaError_t e = rows_map(q, batch, h.cfg.n_h, kDq, min(((batch + 15) / 16) * 16, kMaxN), &tq);
+  cudaError_t e = rows_map(q, batch, h.cfg.n_h, kDq, min(n_pad, kQaN), &tq);
   if (e != cudaSuccess) return e;
-  return launch_head_gemm<kQAbsorb>(h, *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk), tq, batch, q, ctx_len,
-                                    ws.q_abs, st);
+  dim3 grid(h.cfg.n_h, 1, (batch + kQaN - 1) / kQaN);
+  return launch_pdl(q_absorb_kernel, grid, dim3(kThreads), kQaSmem, st,
+                    *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk), tq, batch, h.cfg.n_h, n_pad, q, ctx_len,
+                    (const float2*)h.rope_cs, h.cfg.max_position, ws.q_abs, h.check_word);
 }
 
 cudaError_t launch_combine_uv(const Handle& h, int batch, const Workspace& ws, __nv_bfloat16* out, cudaStream_t st) {
-  combine_kernel<<<dim3(batch, (h.cfg.n_h + 3) / 4), 128, 0, st>>>(batch, h.cfg.n_h, ws);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(up_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUpSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int n_pad = ((batch + 15) / 16) * 16;
   alignas(64) CUtensorMap to;
-  e = rows_map(ws.o_lat, batch, h.cfg.n_h, kDc, min(((batch + 15) / 16) * 16, kMaxN), &to);
+  cudaError_t e = rows_map(ws.o_lat, batch, h.cfg.n_h, kDc, min(n_pad, kUpN), &to);
   if (e != cudaSuccess) return e;
-  return launch_head_gemm<kUpProject>(h, *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv), to, batch, nullptr,
-                                      nullptr, out, st);
+  dim3 grid(h.cfg.n_h, 1, (batch + kUpN - 1) / kUpN);
+  return launch_pdl(up_project_kernel, grid, dim3(kThreads), kUpSmem, st,
+                    *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv), to, batch, h.cfg.n_h, n_pad, ws, out,
+                    h.check_word);
 }
 
 }  // namespace mla

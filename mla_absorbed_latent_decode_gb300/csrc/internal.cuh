@@ -8,6 +8,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/mla.h"
 
 namespace mla {
@@ -93,6 +95,25 @@ cudaError_t launch_decode_simt(const Handle& h, const int32_t* ctx_len, int batc
                                int num_pages, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_combine_uv(const Handle& h, int batch, const Workspace& ws,
                               __nv_bfloat16* out, cudaStream_t st);
+
+// Launch a kernel as a programmatic dependent of the previous work in the stream: it may
+// be scheduled while that work finishes and must call griddep_wait() before touching
+// anything it produced.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Device check word bits (same values as the public MLA_CHECK_* macros).
 constexpr unsigned kCheckCtxLen = MLA_CHECK_CTX_LEN;

@@ -22,11 +22,13 @@
 // because one sequence's context (up to 65536 tokens here) is far more work
 // than one SM pair should take when the batch is small.
 #include "internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace mla {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanSmemSeqs = 16384;     // page counts of up to this many sequences stay in shared memory
 
 __device__ int block_sum(int v, int* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -77,23 +79,27 @@ __device__ int block_exclusive_scan(int v, int* red, int* total) {
 }
 
 
-// Per-thread partial counts over this thread's sequences (pages(b) is parked in seqs[b].nsplit).
-__device__ int count_units(int B, const Workspace& ws, int target) {
+// pages(b): from shared memory for the first kPlanSmemSeqs sequences, else parked in seqs[b].nsplit
+__device__ __forceinline__ int pages_of(int b, const int* pages_s, const Workspace& ws) {
+  return b < kPlanSmemSeqs ? pages_s[b] : ws.seqs[b].nsplit;
+}
+// Per-thread partial counts over this thread's sequences.
+__device__ int count_units(int B, const int* pages_s, const Workspace& ws, int target) {
   int n = 0;
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
-    const int np = ws.seqs[b].nsplit;
+    const int np = pages_of(b, pages_s, ws);
     n += np == 0 ? 0 : (np + target - 1) / target;
   }
   return n;
 }
-__device__ int count_valid(int B, const Workspace& ws) {
+__device__ int count_valid(int B, const int* pages_s, const Workspace& ws) {
   int n = 0;
-  for (int b = threadIdx.x; b < B; b += blockDim.x) n += ws.seqs[b].nsplit > 0;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) n += pages_of(b, pages_s, ws) > 0;
   return n;
 }
-__device__ int warp_max_pages(int B, const Workspace& ws) {
+__device__ int thread_max_pages(int B, const int* pages_s, const Workspace& ws) {
   int m = 0;
-  for (int b = threadIdx.x; b < B; b += blockDim.x) m = max(m, ws.seqs[b].nsplit);
+  for (int b = threadIdx.x; b < B; b += blockDim.x) m = max(m, pages_of(b, pages_s, ws));
   return m;
 }
 __device__ int block_max(int v, int* red) {
@@ -117,6 +123,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
     const int32_t* __restrict__ ctx_len, int B, int max_ctx, const int32_t* __restrict__ block_table,
     int bt_stride, int num_pages, int num_pairs, int forced, Workspace ws, unsigned* check) {
   __shared__ int red[64];
+  extern __shared__ int pages_s[];     // [min(B, kPlanSmemSeqs)]
+  // Runs as a programmatic dependent of the query-absorption kernel without waiting for it:
+  // it starts only after every CTA of that kernel passed its own griddepcontrol.wait, so the
+  // caller's inputs (context lengths, block table) are complete.  It waits for that kernel
+  // at its end, so the decode kernel after it sees both.
+  sm100::griddep_launch_dependents();
   // 1. validate and count pages, one warp per sequence (lanes check page ids in parallel);
   //    pages(b) is parked in seqs[b].nsplit
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -138,25 +150,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
       if (__any_sync(0xffffffffu, bad)) { flags |= kCheckPageId; np = 0; }
     }
     if (lane == 0) {
-      ws.seqs[b].nsplit = np;
+      if (b < kPlanSmemSeqs) pages_s[b] = np; else ws.seqs[b].nsplit = np;
       my_pages += np;
     }
   }
   if (flags && lane == 0) atomicOr(check, flags);
   __syncthreads();   // seqs[].nsplit written by other warps is read below
   const int total_pages = block_sum(my_pages, red);
-  const int max_pages = block_max(warp_max_pages(B, ws), red);
+  const int max_pages = block_max(thread_max_pages(B, pages_s, ws), red);
   // Smallest page target whose split count fits in one wave of SM pairs: start from an
   // even share of the pages and grow it (binary search) until sum_b ceil(pages_b / target)
   // <= max(num_pairs, number of valid sequences).  With at least as many sequences as
   // pairs nothing is split.
   const int pairs = max(1, num_pairs);
   int lo = max(1, (total_pages + pairs - 1) / pairs), hi = max(lo, max_pages);
-  const int valid_seqs = block_sum(count_valid(B, ws), red);
+  const int valid_seqs = block_sum(count_valid(B, pages_s, ws), red);
   const int budget = max(pairs, valid_seqs);
   while (lo < hi) {
     const int mid = lo + (hi - lo) / 2;
-    if (block_sum(count_units(B, ws, mid), red) <= budget) hi = mid; else lo = mid + 1;
+    if (block_sum(count_units(B, pages_s, ws, mid), red) <= budget) hi = mid; else lo = mid + 1;
   }
   const int target = lo;
 
@@ -166,13 +178,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
     const int b = b0 + threadIdx.x;
     int ns = 0;
     if (b < B) {
-      const int np = ws.seqs[b].nsplit;
+      const int np = pages_of(b, pages_s, ws);
       ns = np == 0 ? 0 : (forced > 0 ? min(forced, np) : (np + target - 1) / target);
     }
     int chunk_total = 0;
     const int off = block_exclusive_scan(ns, red, &chunk_total);
     if (b < B) {
-      const int np = ws.seqs[b].nsplit;
+      const int np = pages_of(b, pages_s, ws);
       const int first = base + off;
       for (int j = 0; j < ns; ++j) {
         Unit u;
@@ -193,6 +205,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
     ws.counters[0] = base;
     ws.counters[1] = base;
   }
+  sm100::griddep_wait();
 }
 
 }  // namespace
@@ -200,9 +213,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
 cudaError_t launch_plan(const Handle& h, const int32_t* ctx_len, int batch, int max_ctx,
                         const int32_t* block_table, int bt_stride, int num_pages, const Workspace& ws,
                         cudaStream_t st) {
-  plan_kernel<<<1, kPlanThreads, 0, st>>>(ctx_len, batch, max_ctx, block_table, bt_stride, num_pages,
-                                          h.num_pairs, h.force_splits, ws, h.check_word);
-  return cudaGetLastError();
+  const size_t smem = sizeof(int) * (size_t)min(batch, kPlanSmemSeqs);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(int) * kPlanSmemSeqs));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), smem, st, ctx_len, batch, max_ctx, block_table,
+                    bt_stride, num_pages, h.num_pairs, h.force_splits, ws, h.check_word);
 }
 
 }  // namespace mla
