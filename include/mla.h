@@ -187,6 +187,35 @@ mla_status_t mla_decode(mla_handle_t h, const void* q, const int32_t* ctx_len, i
                         const void* cache, int32_t num_pages, void* workspace,
                         size_t workspace_bytes, void* out, mla_stream_t stream);
 
+/* Size of the scratch array that mla_decode_fixed_scratch uses on each device. */
+#define MLA_FIXED_SCRATCH_BYTES (32u << 20)
+
+/*
+ * mla_decode_fixed_scratch -- mla_decode without a caller workspace.  The pages
+ * describing the method have no counterpart: this is a deployment convenience
+ * for callers that cannot allocate device memory at the point of the call.
+ *
+ * Arguments, output and device checks are those of mla_decode.  The scratch is
+ * one array of MLA_FIXED_SCRATCH_BYTES inside the library (one per device);
+ * nothing is allocated by the call.
+ *
+ *   - A batch whose mla_decode_workspace_size exceeds MLA_FIXED_SCRATCH_BYTES
+ *     fails with MLA_ERR_WORKSPACE before anything is enqueued (on a 152-SM GB300
+ *     up to 25 sequences fit at 128 heads, up to 458 at 16 heads).
+ *   - The handle's device must be current (else MLA_ERR_INVALID_ARG).
+ *   - Every call writes the scratch before reading it; it never needs clearing.
+ *   - All calls on one device share the array, whatever the handle or stream:
+ *     calls whose execution overlaps race and corrupt each other's results.
+ *     Order them on one stream, or with events.
+ *   - The first call on a device looks the array up (cudaGetSymbolAddress),
+ *     which may load the library's module there: make it before any stream
+ *     capture begins.
+ */
+mla_status_t mla_decode_fixed_scratch(mla_handle_t h, const void* q, const int32_t* ctx_len,
+                                      int32_t batch, int32_t max_ctx, const int32_t* block_table,
+                                      int32_t bt_stride, const void* cache, int32_t num_pages,
+                                      void* out, mla_stream_t stream);
+
 /*
  * mla_get_status -- synchronize `stream`, read and clear the device check word.
  * Returns MLA_OK when it was clear, else MLA_ERR_DEVICE_CHECK with the bits in

@@ -33,8 +33,11 @@ MLA_CHECK_TIMEOUT = 0x8
 MLA_OPT_SPLITS = 1
 MLA_OPT_PROFILE = 2
 
+MLA_FIXED_SCRATCH_BYTES = 32 << 20     # include/mla.h: scratch of mla_decode_fixed_scratch
+
 EXPORTED = [
     "mla_create", "mla_destroy", "mla_kv_append", "mla_decode_workspace_size", "mla_decode",
+    "mla_decode_fixed_scratch",
     "mla_get_status", "mla_set_option", "mla_profile_read", "mla_profile_kernel_name",
     "mla_last_error", "mla_status_string",
 ]
@@ -75,6 +78,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_kv_append.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, vp, i32, vp]
     lib.mla_decode_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
     lib.mla_decode.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, sz, vp, vp]
+    lib.mla_decode_fixed_scratch.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, vp]
     lib.mla_get_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_set_option.argtypes = [vp, i32, i64]
     lib.mla_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]
@@ -85,6 +89,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_status_string.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
     for name in ("mla_create", "mla_destroy", "mla_kv_append", "mla_decode_workspace_size", "mla_decode",
+                 "mla_decode_fixed_scratch",
                  "mla_get_status", "mla_set_option", "mla_profile_read"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
@@ -162,6 +167,13 @@ class Mla:
         _check(self._lib.mla_decode(self._h, _ptr(q), _ptr(ctx_len), batch, int(max_ctx), _ptr(block_table),
                                     int(block_table.shape[1]), _ptr(cache), int(num_pages), _ptr(workspace),
                                     ws_bytes, _ptr(out), _stream(stream)))
+
+    def decode_fixed_scratch(self, q, ctx_len, max_ctx: int, block_table, cache, num_pages: int, out,
+                             stream=None) -> None:
+        batch = int(ctx_len.shape[0])
+        _check(self._lib.mla_decode_fixed_scratch(self._h, _ptr(q), _ptr(ctx_len), batch, int(max_ctx),
+                                                  _ptr(block_table), int(block_table.shape[1]), _ptr(cache),
+                                                  int(num_pages), _ptr(out), _stream(stream)))
 
     def get_status(self, stream=None) -> int:
         flags = ctypes.c_uint32(0)

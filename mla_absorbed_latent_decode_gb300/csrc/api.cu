@@ -85,6 +85,13 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 namespace mla {
 
+void clear_last_error() { g_last_error.clear(); }
+
+mla_status_t set_last_error(mla_status_t s, const char* msg) {
+  g_last_error = msg;
+  return s;
+}
+
 size_t workspace_bytes(const Handle& h, int batch, Workspace* ws, char* base) {
   const int n_h = h.cfg.n_h;
   // The planner makes at most sum_b ceil(pages_b / target) <= batch + num_pairs units,

@@ -78,6 +78,10 @@ cudaError_t prepare_weight_maps(Handle& h);
 // Workspace sizing and carving (host).
 size_t workspace_bytes(const Handle& h, int batch, Workspace* carve, char* base);
 
+// The calling thread's message for mla_last_error (kept in api.cu).
+void clear_last_error();
+mla_status_t set_last_error(mla_status_t s, const char* msg);
+
 // Kernel launchers (each returns the launch error).
 cudaError_t launch_kv_append(const Handle& h, const __nv_bfloat16* rows, const int32_t* seq,
                              const int32_t* pos, int n, const int32_t* block_table, int bt_rows,

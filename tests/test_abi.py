@@ -95,6 +95,7 @@ def test_null_arguments(lib):
     assert lib.mla_decode_workspace_size(None, 1, 1, ctypes.byref(sz)) == B.MLA_ERR_INVALID_ARG
     assert lib.mla_kv_append(None, 1, 1, 1, 1, 1, 1, 1, 1, 1, None) == B.MLA_ERR_INVALID_ARG
     assert lib.mla_decode(None, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_fixed_scratch(None, 1, 1, 1, 1, 1, 1, 1, 1, 1, None) == B.MLA_ERR_INVALID_ARG
     assert lib.mla_get_status(None, None, None) == B.MLA_ERR_INVALID_ARG
     assert lib.mla_set_option(None, 1, 0) == B.MLA_ERR_INVALID_ARG
     n = ctypes.c_int32()
