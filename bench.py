@@ -42,7 +42,6 @@ sys.path.insert(0, ROOT)
 METRIC = "absorbed-MLA decode µs/step, latent-KV GB/s and % of roofline at B×s_ctx"
 DECODE_SOURCES = ["mla_absorbed_latent_decode_gb300/csrc/decode_simt.cu",
                   "mla_absorbed_latent_decode_gb300/csrc/decode_tc.cu"]
-DECODE_KERNEL_INDEX = 2          # position of the split-KV decode kernel in mla_profile_read
 
 
 def parse():

@@ -37,8 +37,8 @@ mla_status_t cuda_fail(cudaError_t e, const char* what) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-const char* kKernelNames[] = {"mla_q_absorb", "mla_plan", "mla_decode_splitkv", "mla_combine_uv"};
-constexpr int kNumKernels = 4;
+const char* kKernelNames[] = {"mla_q_absorb_plan", "mla_decode_splitkv", "mla_combine_uv"};
+constexpr int kNumKernels = 3;
 
 mla_status_t check_config(const mla_config_t* c) {
   // Mandatory fields: a zero means "not given" and is reported by name.
@@ -107,6 +107,7 @@ size_t workspace_bytes(const Handle& h, int batch, Workspace* ws, char* base) {
   char* o_lat = take(sizeof(__nv_bfloat16) * (size_t)batch * n_h * kDc);
   char* part_o = take(sizeof(float) * (size_t)max_parts * n_h * kDc);
   char* part_lse = take(sizeof(float) * (size_t)max_parts * n_h);
+  char* bad = take(sizeof(int32_t) * (size_t)batch);
   if (ws) {
     ws->counters = reinterpret_cast<int32_t*>(counters);
     ws->units = reinterpret_cast<Unit*>(units);
@@ -115,6 +116,7 @@ size_t workspace_bytes(const Handle& h, int batch, Workspace* ws, char* base) {
     ws->o_lat = reinterpret_cast<__nv_bfloat16*>(o_lat);
     ws->part_o = reinterpret_cast<float*>(part_o);
     ws->part_lse = reinterpret_cast<float*>(part_lse);
+    ws->bad = reinterpret_cast<int32_t*>(bad);
     ws->max_units = max_units;
     ws->max_parts = max_parts;
   }
@@ -291,14 +293,12 @@ mla_status_t mla_decode(mla_handle_t hh, const void* q, const int32_t* ctx_len, 
   int ev = 0;
   auto mark = [&]() { if (prof) cudaEventRecord(h->ev[ev++], st); };
   cudaError_t e;
-  // Kernel order: query absorption, then the planner (it overlaps the absorption; see
-  // plan.cu), then the split-KV decode, then the merge + value up-projection.
+  // Kernel order: query absorption (with the split planner in one extra CTA), the split-KV
+  // decode, then the merge + value up-projection.
   mark();
-  if ((e = mla::launch_q_absorb(*h, static_cast<const __nv_bfloat16*>(q), ctx_len, batch, ws, st)) != cudaSuccess)
+  if ((e = mla::launch_q_absorb(*h, static_cast<const __nv_bfloat16*>(q), ctx_len, batch, max_ctx, ws, st)) !=
+      cudaSuccess)
     return cuda_fail(e, "q_absorb launch");
-  mark();
-  if ((e = mla::launch_plan(*h, ctx_len, batch, max_ctx, block_table, bt_stride, num_pages, ws, st)) != cudaSuccess)
-    return cuda_fail(e, "plan launch");
   mark();
   if ((e = mla::launch_decode(*h, ctx_len, batch, block_table, bt_stride, cache, num_pages, ws, st)) != cudaSuccess)
     return cuda_fail(e, "decode launch");

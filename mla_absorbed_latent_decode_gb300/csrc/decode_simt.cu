@@ -45,7 +45,8 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 v) {
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
     const int32_t* __restrict__ ctx_len, int n_h, const int32_t* __restrict__ block_table, int bt_stride,
-    const uint8_t* __restrict__ cache, float score_scale, float out_scale, Workspace ws) {
+    int num_pages, const uint8_t* __restrict__ cache, float score_scale, float out_scale, Workspace ws,
+    unsigned* check) {
   extern __shared__ __align__(16) uint8_t smem[];
   float* q_s = reinterpret_cast<float*>(smem);
   __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem + kSmemQ);
@@ -77,7 +78,14 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
 
   const int32_t* bt_row = block_table + (size_t)b * bt_stride;
   for (int pi = unit.page_begin; pi < unit.page_end; ++pi) {
-    const int page = bt_row[pi];
+    int page = bt_row[pi];
+    if (page < 0 || page >= num_pages) {   // bad page id: read page 0 instead; the output is zeroed later
+      if (tid == 0) {
+        atomicOr(check, kCheckPageId);
+        ws.bad[b] = 1;
+      }
+      page = 0;
+    }
     const int valid = min(kPage, t_end - pi * kPage);
     __syncthreads();
     // stage the page: 64 rows x 72 chunks of 8 values, invalid rows zeroed
@@ -173,7 +181,6 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
 cudaError_t launch_decode_simt(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table,
                           int bt_stride, const void* cache, int num_pages, const Workspace& ws, cudaStream_t st) {
   (void)batch;
-  (void)num_pages;
   const bool fp8 = h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3;
   static bool attr_set[2] = {false, false};
   auto kern = fp8 ? decode_simt_kernel<true> : decode_simt_kernel<false>;
@@ -186,7 +193,7 @@ cudaError_t launch_decode_simt(const Handle& h, const int32_t* ctx_len, int batc
   const float oscale = fp8 ? h.cfg.fp8_scale : 1.0f;
   dim3 grid(ws.max_units, (h.cfg.n_h + kHeadsPerCta - 1) / kHeadsPerCta);
   return launch_pdl(kern, grid, dim3(kThreads), kSmemTotal, st, ctx_len, h.cfg.n_h, block_table, bt_stride,
-                    static_cast<const uint8_t*>(cache), sscale, oscale, ws);
+                    num_pages, static_cast<const uint8_t*>(cache), sscale, oscale, ws, h.check_word);
 }
 
 }  // namespace mla

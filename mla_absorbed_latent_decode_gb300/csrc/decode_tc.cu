@@ -114,8 +114,8 @@ __device__ __forceinline__ void load_scores(uint32_t lane_addr, int bb, uint32_t
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __restrict__ ctx_len, int n_h,
-                 const int32_t* __restrict__ block_table, int bt_stride, float scale_log2, float out_scale,
-                 Workspace ws, unsigned* check) {
+                 const int32_t* __restrict__ block_table, int bt_stride, int num_pages, float scale_log2,
+                 float out_scale, Workspace ws, unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base: swizzle atoms and TMA destinations need it
   const uint32_t raw = smem_u32(smem_raw);
@@ -207,7 +207,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
           fail_timeout(bars, check);
           break;
         }
-        const int page = bt_row[j];
+        int page = bt_row[j];
+        if (page < 0 || page >= num_pages) {   // bad page id: read page 0 instead; the output is zeroed later
+          if (rank == 0) {
+            atomicOr(check, kCheckPageId);
+            ws.bad[b] = 1;
+          }
+          page = 0;
+        }
         const uint32_t full = smem_u32(&bars->full[s]);
         mbar_arrive_expect_tx(full, bytes);
         for (int c = 0; c < n_chunks; ++c)
@@ -485,7 +492,7 @@ cudaError_t make_cache_tensor_map(const void* cache, int num_pages, CUtensorMap*
 
 namespace {
 cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, const int32_t* block_table, int bt_stride,
-                             const CUtensorMap& map, const Workspace& ws, cudaStream_t st) {
+                             int num_pages, const CUtensorMap& map, const Workspace& ws, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -494,7 +501,7 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, const int3
   }
   const float scale_log2 = h.scale * 1.4426950408889634f;
   return launch_pdl(decode_tc_kernel, dim3(2 * ws.max_units), dim3(kThreads), kSmemBytes, st, map, ctx_len,
-                    h.cfg.n_h, block_table, bt_stride, scale_log2, 1.0f, ws, h.check_word);
+                    h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, 1.0f, ws, h.check_word);
 }
 }  // namespace
 
@@ -511,7 +518,8 @@ cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, co
     hm.tmap_cache = cache;
     hm.tmap_pages = num_pages;
   }
-  return launch_decode_tc(h, ctx_len, block_table, bt_stride, *reinterpret_cast<const CUtensorMap*>(hm.tmap), ws, st);
+  return launch_decode_tc(h, ctx_len, block_table, bt_stride, num_pages, *reinterpret_cast<const CUtensorMap*>(hm.tmap),
+                          ws, st);
 }
 
 }  // namespace mla

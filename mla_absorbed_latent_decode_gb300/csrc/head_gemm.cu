@@ -3,24 +3,28 @@
 // from HBM once:
 //
 //   query absorption ("DeepSeek MLA 吸收式缓存：真实权重执行与 FlashMLA 架构边界" §2.2)
-//     Q_lat^T[h] [512 x B] = W_UK[h]^T [512 x 128] . q_nope[:, h]^T [128 x B]
+//     Q_lat[:, h] [B x 512] = q_nope[:, h] [B x 128] . W_UK[h] [128 x 512]
 //     plus the RoPE part of the query rotated at ctx_len - 1 (§2.4);
 //   value up-projection after the latent sum (§2.3)
 //     out^T[h]   [128 x B] = W_UV[h] [128 x 512] . o_lat[:, h]^T [512 x B].
 //
-// Before the up-projection, split sequences' partial latent sums are merged by
-// log-sum-exp into o_lat (a standard identity, not on the pages); invalid
-// sequences get a zero latent, hence a zero output.
+// The query-absorption launch has one extra CTA that runs the split planner
+// (plan.cuh) while the GEMM CTAs wait for their weights.  Before the
+// up-projection, split sequences' partial latent sums are merged by log-sum-exp
+// into o_lat (a standard identity, not on the pages); invalid sequences, and
+// sequences whose block table held a bad page id, get a zero latent, hence a zero
+// output.
 //
 // One CTA per (head, tile of sequences): the whole weight matrix of the head
 // (128 KB) and the tile's rows arrive by TMA in 128-byte-swizzled 64-column
-// boxes, all issued up front; one thread issues the MMAs; warps 0-3 (one per 32
-// TMEM lanes) run the epilogue.  The merge of split sequences runs in the
-// up-projection kernel while its weight loads are in flight.
+// boxes, all issued up front; one thread issues the MMAs from precomputed
+// descriptors; warps 0-3 (one per 32 TMEM lanes) run the epilogue with 16-byte
+// stores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include "internal.cuh"
+#include "plan.cuh"
 #include "sm100_ptx.cuh"
 
 namespace mla {
@@ -31,10 +35,10 @@ using namespace sm100;
 constexpr int kThreads = 128;
 constexpr int kBox = 128 * 128;                        // one 64-column x 128-row bf16 box: 16 KB
 
-// query absorption: one CTA per (head, tile of up to 128 sequences), all four 128-row M blocks
-constexpr int kQaN = 128;
-constexpr int kQaSmem = 8 * kBox + 2 * kQaN * 128 + 1024 + 1024;
-// value up-projection: one CTA per (head, tile of up to 64 sequences)
+// query absorption: one CTA per (head, tile of 128 sequences); sequences are the M rows
+constexpr int kQaM = 128;
+constexpr int kQaSmem = 8 * kBox + 2 * kBox + 1024 + 1024;
+// value up-projection: one CTA per (head, tile of up to 64 sequences); the 128 value rows are M
 constexpr int kUpN = 64;
 constexpr int kUpSmem = 8 * kBox + 8 * kUpN * 128 + 1024 + 1024;
 
@@ -59,25 +63,32 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap* m, in
       : "memory");
 }
 
-// Q_lat^T[h] = W_UK[h]^T . q_nope[:, h]^T for the sequences n0 .. n0 + n_pad of this CTA.
-// A = W_UK[h] read MN-major: the box (64 latent columns c, 128 rows n) is K-rows of 128 B.
+// Q_lat[n0 .. n0 + 128, h] = q_nope[n0 .., h] . W_UK[h]: M = 128 sequences (rows past B arrive
+// as zeros), N = 2 x 256 latent columns, K = 128.  A = the query rows, K-major; B = W_UK[h]
+// read MN-major (each box: 128 K-rows of 64 latent columns).  The CTA with blockIdx.x == n_h
+// runs the split planner instead.
 __global__ void __launch_bounds__(kThreads, 1)
-q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q, int B, int n_h,
-                int n_pad, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ ctx_len,
-                const float2* __restrict__ rope_cs, int max_position, __nv_bfloat16* __restrict__ q_abs,
+q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
+                const __grid_constant__ CUtensorMap tm_out, int B, int n_h,
+                int max_ctx, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ ctx_len,
+                const float2* __restrict__ rope_cs, int max_position, int num_pairs, int forced, Workspace ws,
                 unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int red[64];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  const uint32_t sbase = smem_u32(smem);
-  GemmBars* bars = reinterpret_cast<GemmBars*>(smem + 8 * kBox + 2 * kQaN * 128);
-  volatile int* abort_flag = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x, n0 = blockIdx.z * kQaN;
-  // every tile uses the TMA box height (rows past B arrive as zeros), so the transaction
-  // count and the chunk offsets match what the copies write
-  const int n_here = min(n_pad, kQaN);                 // multiple of 16
-  const uint32_t b_bytes = (uint32_t)n_here * 128;
+  if (blockIdx.x == n_h) {
+    // ---- the split planner (one CTA; context lengths are inputs of the step)
+    griddep_wait();
+    griddep_launch_dependents();
+    if (blockIdx.z == 0) plan_block(ctx_len, B, max_ctx, num_pairs, forced, ws, check, reinterpret_cast<int*>(smem), red);
+    return;
+  }
+  const uint32_t sbase = smem_u32(smem);
+  GemmBars* bars = reinterpret_cast<GemmBars*>(smem + 10 * kBox);
+  volatile int* abort_flag = &bars->abort;
+  const int h = blockIdx.x, n0 = blockIdx.z * kQaM;
   if (tid == 0) {
     mbar_init(smem_u32(&bars->full), 1);
     mbar_init(smem_u32(&bars->done), 1);
@@ -89,68 +100,108 @@ q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t a_st = sbase, b_st = sbase + 8 * kBox;
+  const uint32_t w_st = sbase, a_st = sbase + 8 * kBox;
   if (tid == 0) {
     const uint32_t full = smem_u32(&bars->full);
-    mbar_arrive_expect_tx(full, 8u * kBox + 2u * b_bytes);
-    for (int i = 0; i < 8; ++i) tma_load_2d(a_st + i * kBox, &tm_w, 64 * i, 128 * h, full);   // c = 64 i ..
+    mbar_arrive_expect_tx(full, 10u * kBox);
+    for (int i = 0; i < 8; ++i) tma_load_2d(w_st + i * kBox, &tm_w, 64 * i, 128 * h, full);   // latent 64 i ..
     griddep_wait();                        // the queries may come from the previous kernel
     griddep_launch_dependents();
-    load_rows(b_st, &tm_q, 0, h, n0, full);
-    load_rows(b_st + b_bytes, &tm_q, 64, h, n0, full);
+    load_rows(a_st, &tm_q, 0, h, n0, full);
+    load_rows(a_st + kBox, &tm_q, 64, h, n0, full);
     bool ok = mbar_wait(full, 0, abort_flag);
     tc_fence_after();
-    const uint32_t idesc = idesc_bf16_f32(128, n_here, true, false);
-    for (int mb = 0; mb < 4 && ok; ++mb)   // M block mb = latent c in [128 mb, 128 mb + 128): boxes 2 mb, 2 mb + 1
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 256, false, true);
+    const uint64_t a0 = sdesc_sw128(a_st, 16, 1024), b0 = sdesc_sw128(w_st, kBox, 1024);
+    if (ok) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k)          // 16 K-rows (n) of 128 B per step; the two 64-wide M halves kBox apart
-        mma_ss(tmem + mb * n_here, sdesc_sw128(a_st + 2 * mb * kBox + 2048 * k, kBox, 1024),
-               sdesc_sw128(b_st + (k >> 2) * b_bytes + 32 * (k & 3), 16, 1024), idesc, k > 0 ? 1u : 0u);
-    if (!ok && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+      for (int hh = 0; hh < 2; ++hh)       // latent columns [256 hh, 256 hh + 256): boxes 4 hh .. 4 hh + 3
+#pragma unroll
+        for (int k = 0; k < 8; ++k)        // K rows [16 k, 16 k + 16): A box k / 4 at 32 B steps; B 2 KB steps
+          mma_ss(tmem + 256 * hh, a0 + (uint64_t)(((k >> 2) * kBox + (k & 3) * 32) >> 4),
+                 b0 + (uint64_t)((hh * 4 * kBox + k * 2048) >> 4), idesc, k > 0 ? 1u : 0u);
+    } else if (atomicExch(&bars->abort, 1) == 0) {
+      atomicOr(check, kCheckTimeout);
+    }
     mma_commit(smem_u32(&bars->done));
   }
   griddep_wait();
-  __syncwarp();
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort_flag));
-  tc_fence_after();
-  const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-  if (ok) {
-    for (int mb = 0; mb < 4; ++mb) {
-      for (int c0 = 0; c0 < n_here; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(lane_addr + mb * n_here + c0, r);
-        tmem_ld_wait();
+  // RoPE part of the query, rotated at position ctx_len - 1 (clamped into the table): one
+  // sequence per thread of warps 1-3 (warp 0 issues the copies and MMAs meanwhile), every
+  // load of a sequence issued before any is used
+  if (warp > 0) {
+    for (int j = tid - 32; j < min(B - n0, kQaM); j += kThreads - 32) {
+      const int b = n0 + j;
+      const int pos = min(max(ctx_len[b] - 1, 0), max_position - 1);
+      const uint4* qs = reinterpret_cast<const uint4*>(q + ((size_t)b * n_h + h) * kDq + kDn);
+      const float4* cs = reinterpret_cast<const float4*>(rope_cs + (size_t)pos * (kDr / 2));
+      uint4 qv[8];
+      float4 cv[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int b = n0 + c0 + i;
-          if (c0 + i >= n_here || b >= B) break;
-          q_abs[((size_t)b * n_h + h) * kRow + 128 * mb + 32 * warp + lane] = __float2bfloat16_rn(__uint_as_float(r[i]));
+      for (int i = 0; i < 8; ++i) qv[i] = qs[i];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) cv[i] = cs[i];
+      uint4* dst = reinterpret_cast<uint4*>(ws.q_abs + ((size_t)b * n_h + h) * kRow + kDc);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {            // pairs 4 i .. 4 i + 3
+        const uint32_t w[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+        const float4 c01 = cv[2 * i], c23 = cv[2 * i + 1];
+        const float cs_c[4] = {c01.x, c01.z, c23.x, c23.z}, cs_s[4] = {c01.y, c01.w, c23.y, c23.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float x0 = __uint_as_float(w[k] << 16), x1 = __uint_as_float(w[k] & 0xFFFF0000u);
+          o[k] = bf16x2_bits(x0 * cs_c[k] - x1 * cs_s[k], x1 * cs_c[k] + x0 * cs_s[k]);
         }
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
   }
-  // RoPE part of the query, rotated at position ctx_len - 1 (clamped into the table)
-  for (int i = tid; i < min(B - n0, kQaN) * (kDr / 2); i += kThreads) {
-    const int b = n0 + i / (kDr / 2), p = i % (kDr / 2);
-    const int pos = min(max(ctx_len[b] - 1, 0), max_position - 1);
-    const __nv_bfloat162 x = reinterpret_cast<const __nv_bfloat162*>(q + ((size_t)b * n_h + h) * kDq + kDn)[p];
-    const float2 cs = rope_cs[(size_t)pos * (kDr / 2) + p];
-    const float x0 = __bfloat162float(x.x), x1 = __bfloat162float(x.y);
-    reinterpret_cast<uint32_t*>(q_abs + ((size_t)b * n_h + h) * kRow + kDc)[p] =
-        bf16x2_bits(x0 * cs.x - x1 * cs.y, x1 * cs.x + x0 * cs.y);
+  __syncwarp();
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort_flag));
+  tc_fence_after();
+  // epilogue: thread = sequence (TMEM lane), 32 latent values per load.  The tile is staged
+  // in the (now free) weight region as eight 128-byte-swizzled boxes of 64 columns x 128
+  // rows and written out by TMA stores (rows past B are not written).
+  const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+  const int r = 32 * warp + lane;
+  if (ok) {
+#pragma unroll 1
+    for (int g = 0; g < 16; ++g) {
+      uint32_t v[32];
+      tmem_ld32(lane_addr + 32 * g, v);
+      tmem_ld_wait();
+      uint8_t* row = smem + (g >> 1) * kBox + r * 128;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = (g & 1) * 4 + i;             // 16-byte chunk of the box row
+        *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) * 16)) =
+            make_uint4(bf16x2_bits(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
+                       bf16x2_bits(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                       bf16x2_bits(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                       bf16x2_bits(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+      }
+    }
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
+  if (ok && tid == 0) {
+    for (int i = 0; i < 8; ++i) tma_store_3d(&tm_out, sbase + i * kBox, 64 * i, h, n0);
+    bulk_commit_group();
+    bulk_wait_all();
+  }
 }
 
 // out^T[h] = W_UV[h] . o_lat[:, h]^T for the sequences n0 .. n0 + n_pad of this CTA, after
 // merging split sequences' partials of head h into o_lat by log-sum-exp (zero latent for an
-// invalid sequence; unsplit sequences already hold theirs).
+// invalid sequence or one with a bad page id; unsplit sequences already hold theirs).
 __global__ void __launch_bounds__(kThreads, 1)
 up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_o, int B, int n_h,
                   int n_pad, Workspace ws, __nv_bfloat16* __restrict__ out, unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int2 plan_s[kUpN];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(smem);
@@ -158,7 +209,7 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
   volatile int* abort_flag = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, n0 = blockIdx.z * kUpN;
-  const int n_here = min(n_pad, kUpN);                 // the TMA box height, as above
+  const int n_here = min(n_pad, kUpN);                 // the TMA box height (rows past B arrive as zeros)
   const uint32_t b_bytes = (uint32_t)n_here * 128;
   if (tid == 0) {
     mbar_init(smem_u32(&bars->full), 1);
@@ -176,27 +227,34 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
   }
   griddep_wait();                          // the plan and latent sums come from earlier kernels
   griddep_launch_dependents();
-  // merge pass: one warp per split (or invalid) sequence of this tile
+  // merge pass: one warp per split, invalid or bad-page sequence of this tile.  The plan
+  // entries of the tile are loaded together first (one per thread); a split sequence's
+  // partial slots are its unit indices first_unit .. first_unit + nsplit - 1.
+  const int n_seq = min(B - n0, kUpN);
+  if (tid < n_seq) {
+    const SeqPlan sp = ws.seqs[n0 + tid];
+    plan_s[tid] = make_int2(sp.first_unit, ws.bad[n0 + tid] ? 0 : sp.nsplit);
+  }
+  __syncthreads();
   bool wrote = false;
-  for (int j = warp; j < min(B - n0, kUpN); j += kThreads / 32) {
+  for (int j = warp; j < n_seq; j += kThreads / 32) {
     const int b = n0 + j;
-    const SeqPlan sp = ws.seqs[b];
-    if (sp.nsplit == 1) continue;
+    const int first = plan_s[j].x, nsplit = plan_s[j].y;
+    if (nsplit == 1) continue;
     wrote = true;
     uint4* dst = reinterpret_cast<uint4*>(ws.o_lat + ((size_t)b * n_h + h) * kDc) + 2 * lane;   // 16 values
-    if (sp.nsplit == 0) {
+    if (nsplit == 0) {
       dst[0] = make_uint4(0, 0, 0, 0);
       dst[1] = make_uint4(0, 0, 0, 0);
       continue;
     }
     float m = -INFINITY;
-    for (int k = 0; k < sp.nsplit; ++k)
-      m = fmaxf(m, ws.part_lse[(size_t)ws.units[sp.first_unit + k].part * n_h + h]);
+    for (int k = 0; k < nsplit; ++k) m = fmaxf(m, ws.part_lse[(size_t)(first + k) * n_h + h]);
     float acc[16], den = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-    for (int k = 0; k < sp.nsplit; ++k) {
-      const int part = ws.units[sp.first_unit + k].part;
+    for (int k = 0; k < nsplit; ++k) {
+      const int part = first + k;
       const float w = expf(ws.part_lse[(size_t)part * n_h + h] - m);
       den += w;
       const float4* src = reinterpret_cast<const float4*>(ws.part_o + ((size_t)part * n_h + h) * kDc) + 4 * lane;
@@ -227,29 +285,42 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
     bool ok = mbar_wait(full, 0, abort_flag);
     tc_fence_after();
     const uint32_t idesc = idesc_bf16_f32(128, n_here, false, false);
-    for (int c = 0; c < 8 && ok; ++c)
+    const uint64_t a0 = sdesc_sw128(a_st, 16, 1024), b0 = sdesc_sw128(b_st, 16, 1024);
+    if (ok) {
+      for (int c = 0; c < 8; ++c)
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tmem, sdesc_sw128(a_st + c * kBox + 32 * k, 16, 1024), sdesc_sw128(b_st + c * b_bytes + 32 * k, 16, 1024),
-               idesc, (c > 0 || k > 0) ? 1u : 0u);
-    if (!ok && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tmem, a0 + (uint64_t)((c * kBox + 32 * k) >> 4), b0 + (uint64_t)((c * b_bytes + 32 * k) >> 4), idesc,
+                 (c > 0 || k > 0) ? 1u : 0u);
+    } else if (atomicExch(&bars->abort, 1) == 0) {
+      atomicOr(check, kCheckTimeout);
+    }
     mma_commit(smem_u32(&bars->done));
   }
   __syncwarp();
   const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort_flag));
   tc_fence_after();
+  // epilogue: thread = value row v (TMEM lane) holding up to 64 sequences; transposed through
+  // shared memory (the weight region is free now) into [sequence][128 v] bf16 rows, then
+  // written with 16-byte stores, one 256-byte row per sequence
   const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+  __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem);     // [64][128]
+  const int v = 32 * warp + lane;
   if (ok) {
     for (int c0 = 0; c0 < n_here; c0 += 32) {
       uint32_t r[32];
       tmem_ld32(lane_addr + c0, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int b = n0 + c0 + i;
-        if (c0 + i >= n_here || b >= B) break;
-        out[((size_t)b * n_h + h) * kDv + 32 * warp + lane] = __float2bfloat16_rn(__uint_as_float(r[i]));
-      }
+      for (int i = 0; i < 32; ++i) tile[(c0 + i) * kDv + v] = __float2bfloat16_rn(__uint_as_float(r[i]));
+    }
+  }
+  __syncthreads();
+  if (ok) {
+    for (int i = tid; i < n_seq * (kDv / 8); i += kThreads) {
+      const int j = i / (kDv / 8), c = i % (kDv / 8);
+      reinterpret_cast<uint4*>(out + ((size_t)(n0 + j) * n_h + h) * kDv)[c] =
+          reinterpret_cast<const uint4*>(tile + j * kDv)[c];
     }
   }
   tc_fence_before();
@@ -309,21 +380,22 @@ cudaError_t prepare_weight_maps(Handle& h) {
 }
 
 cudaError_t launch_q_absorb(const Handle& h, const __nv_bfloat16* q, const int32_t* ctx_len, int batch,
-                            const Workspace& ws, cudaStream_t st) {
+                            int max_ctx, const Workspace& ws, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(q_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQaSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int n_pad = ((batch + 15) / 16) * 16;
-  alignas(64) CUtensorMap tq;
-  cudaError_t e = rows_map(q, batch, h.cfg.n_h, kDq, min(n_pad, kQaN), &tq);
+  static_assert(kQaSmem - 2048 >= (int)sizeof(int) * plan_detail::kPlanSmemSeqs, "planner page counts");
+  alignas(64) CUtensorMap tq, tout;
+  cudaError_t e = rows_map(q, batch, h.cfg.n_h, kDq, kQaM, &tq);
   if (e != cudaSuccess) return e;
-  dim3 grid(h.cfg.n_h, 1, (batch + kQaN - 1) / kQaN);
+  if ((e = rows_map(ws.q_abs, batch, h.cfg.n_h, kRow, kQaM, &tout)) != cudaSuccess) return e;
+  dim3 grid(h.cfg.n_h + 1, 1, (batch + kQaM - 1) / kQaM);     // + 1: the planner CTA
   return launch_pdl(q_absorb_kernel, grid, dim3(kThreads), kQaSmem, st,
-                    *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk), tq, batch, h.cfg.n_h, n_pad, q, ctx_len,
-                    (const float2*)h.rope_cs, h.cfg.max_position, ws.q_abs, h.check_word);
+                    *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk), tq, tout, batch, h.cfg.n_h, max_ctx, q, ctx_len,
+                    (const float2*)h.rope_cs, h.cfg.max_position, h.num_pairs, h.force_splits, ws, h.check_word);
 }
 
 cudaError_t launch_combine_uv(const Handle& h, int batch, const Workspace& ws, __nv_bfloat16* out, cudaStream_t st) {

@@ -47,6 +47,7 @@ struct Workspace {
   __nv_bfloat16* o_lat;     // [B][n_h][512]: normalised latent sum of unsplit sequences
   float* part_o;            // [max_parts][n_h][512]: normalised partial latent sums
   float* part_lse;          // [max_parts][n_h]: natural-log normaliser of each partial
+  int32_t* bad;             // [B]: set by the decode kernel when a page id is out of range
   int max_units;
   int max_parts;
 };
@@ -86,11 +87,9 @@ mla_status_t set_last_error(mla_status_t s, const char* msg);
 cudaError_t launch_kv_append(const Handle& h, const __nv_bfloat16* rows, const int32_t* seq,
                              const int32_t* pos, int n, const int32_t* block_table, int bt_rows,
                              int bt_stride, void* cache, int num_pages, cudaStream_t st);
-cudaError_t launch_plan(const Handle& h, const int32_t* ctx_len, int batch, int max_ctx,
-                        const int32_t* block_table, int bt_stride, int num_pages,
-                        const Workspace& ws, cudaStream_t st);
+// Query absorption; one extra CTA of the same launch runs the split planner.
 cudaError_t launch_q_absorb(const Handle& h, const __nv_bfloat16* q, const int32_t* ctx_len,
-                            int batch, const Workspace& ws, cudaStream_t st);
+                            int batch, int max_ctx, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch,
                           const int32_t* block_table, int bt_stride, const void* cache,
                           int num_pages, const Workspace& ws, cudaStream_t st);

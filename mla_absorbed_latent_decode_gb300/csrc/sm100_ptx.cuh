@@ -173,6 +173,18 @@ __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uin
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+// 3-D tiled TMA store from this CTA's shared memory (rows past the tensor's end are not
+// written); tracked by the issuing thread's bulk-async group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every bulk-async group this thread committed has completed (writes done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Arrive on a cluster peer's mbarrier without release semantics (pure signalling).
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");

@@ -101,8 +101,9 @@ def test_null_arguments(lib):
     n = ctypes.c_int32()
     assert lib.mla_profile_read(None, None, 0, ctypes.byref(n)) == B.MLA_ERR_INVALID_ARG
     assert lib.mla_status_string(B.MLA_ERR_WORKSPACE) == b"MLA_ERR_WORKSPACE"
-    assert lib.mla_profile_kernel_name(2) == b"mla_decode_splitkv"
-    assert lib.mla_profile_kernel_name(0) == b"mla_q_absorb"
+    assert lib.mla_profile_kernel_name(1) == b"mla_decode_splitkv"
+    assert lib.mla_profile_kernel_name(0) == b"mla_q_absorb_plan"
+    assert lib.mla_profile_kernel_name(3) == b""
 
 
 def test_valid_config_without_gpu_fails_cleanly(lib):
