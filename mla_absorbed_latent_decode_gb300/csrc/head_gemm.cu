@@ -17,9 +17,9 @@
 //
 // One CTA per (head, tile of sequences): the whole weight matrix of the head
 // (128 KB) and the tile's rows arrive by TMA in 128-byte-swizzled 64-column
-// boxes, all issued up front; one thread issues the MMAs from precomputed
-// descriptors; warps 0-3 (one per 32 TMEM lanes) run the epilogue with 16-byte
-// stores.
+// boxes, all issued up front, each group of boxes on its own mbarrier so the MMAs
+// over a group start as soon as it lands; one thread issues the MMAs from
+// precomputed descriptors; warps 0-3 (one per 32 TMEM lanes) run the epilogue.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,8 +43,8 @@ constexpr int kUpN = 64;
 constexpr int kUpSmem = 8 * kBox + 8 * kUpN * 128 + 1024 + 1024;
 
 struct GemmBars {
-  uint64_t full;
-  uint64_t done;
+  uint64_t full[8];          // per 64-column box (up-projection: weight box + latent box)
+  uint64_t done[2];          // MMAs of a half (query absorption) / of the whole tile (up-projection)
   uint32_t tmem_base;
   int abort;
 };
@@ -89,9 +89,10 @@ q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
   GemmBars* bars = reinterpret_cast<GemmBars*>(smem + 10 * kBox);
   volatile int* abort_flag = &bars->abort;
   const int h = blockIdx.x, n0 = blockIdx.z * kQaM;
+  // barriers: full[0] = the query rows, full[1 + hh] = weight boxes of latent half hh
   if (tid == 0) {
-    mbar_init(smem_u32(&bars->full), 1);
-    mbar_init(smem_u32(&bars->done), 1);
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&bars->full[i]), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->done[i]), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -102,28 +103,39 @@ q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
   const uint32_t tmem = bars->tmem_base;
   const uint32_t w_st = sbase, a_st = sbase + 8 * kBox;
   if (tid == 0) {
-    const uint32_t full = smem_u32(&bars->full);
-    mbar_arrive_expect_tx(full, 10u * kBox);
-    for (int i = 0; i < 8; ++i) tma_load_2d(w_st + i * kBox, &tm_w, 64 * i, 128 * h, full);   // latent 64 i ..
+    for (int hh = 0; hh < 2; ++hh) {        // each latent half on its own barrier: its MMAs start as it lands
+      const uint32_t wf = smem_u32(&bars->full[1 + hh]);
+      mbar_arrive_expect_tx(wf, 4u * kBox);
+      for (int i = 4 * hh; i < 4 * hh + 4; ++i) tma_load_2d(w_st + i * kBox, &tm_w, 64 * i, 128 * h, wf);
+    }
     griddep_wait();                        // the queries may come from the previous kernel
     griddep_launch_dependents();
-    load_rows(a_st, &tm_q, 0, h, n0, full);
-    load_rows(a_st + kBox, &tm_q, 64, h, n0, full);
-    bool ok = mbar_wait(full, 0, abort_flag);
-    tc_fence_after();
+    const uint32_t qf = smem_u32(&bars->full[0]);
+    mbar_arrive_expect_tx(qf, 2u * kBox);
+    load_rows(a_st, &tm_q, 0, h, n0, qf);
+    load_rows(a_st + kBox, &tm_q, 64, h, n0, qf);
+    bool ok = mbar_wait(qf, 0, abort_flag);
     constexpr uint32_t idesc = idesc_bf16_f32(128, 256, false, true);
     const uint64_t a0 = sdesc_sw128(a_st, 16, 1024), b0 = sdesc_sw128(w_st, kBox, 1024);
-    if (ok) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)       // latent columns [256 hh, 256 hh + 256): boxes 4 hh .. 4 hh + 3
+    for (int hh = 0; hh < 2; ++hh) {       // latent columns [256 hh, 256 hh + 256): boxes 4 hh .. 4 hh + 3
+      ok = ok && mbar_wait(smem_u32(&bars->full[1 + hh]), 0, abort_flag);
+      tc_fence_after();
+      if (ok) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)        // K rows [16 k, 16 k + 16): A box k / 4 at 32 B steps; B 2 KB steps
           mma_ss(tmem + 256 * hh, a0 + (uint64_t)(((k >> 2) * kBox + (k & 3) * 32) >> 4),
                  b0 + (uint64_t)((hh * 4 * kBox + k * 2048) >> 4), idesc, k > 0 ? 1u : 0u);
-    } else if (atomicExch(&bars->abort, 1) == 0) {
-      atomicOr(check, kCheckTimeout);
+      }
+      mma_commit(smem_u32(&bars->done[hh]));
     }
-    mma_commit(smem_u32(&bars->done));
+    if (!ok) {
+      if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+      for (int i = 0; i < 3; ++i) {           // let every copy in flight land before the CTA exits
+        volatile int never = 0;
+        mbar_wait(smem_u32(&bars->full[i]), 0, &never);
+      }
+    }
   }
   griddep_wait();
   // RoPE part of the query, rotated at position ctx_len - 1 (clamped into the table): one
@@ -158,40 +170,46 @@ q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     }
   }
   __syncwarp();
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort_flag));
-  tc_fence_after();
-  // epilogue: thread = sequence (TMEM lane), 32 latent values per load.  The tile is staged
-  // in the (now free) weight region as eight 128-byte-swizzled boxes of 64 columns x 128
-  // rows and written out by TMA stores (rows past B are not written).
+  // epilogue, one latent half at a time (half 1's MMAs overlap half 0's epilogue): thread =
+  // sequence (TMEM lane), 32 latent values per load.  The half is staged in its (now free)
+  // weight boxes, 64 columns x 128 rows each, 128-byte swizzled, and written out by TMA
+  // stores (rows past B are not written).
   const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
   const int r = 32 * warp + lane;
-  if (ok) {
+  bool ok = true;
 #pragma unroll 1
-    for (int g = 0; g < 16; ++g) {
-      uint32_t v[32];
-      tmem_ld32(lane_addr + 32 * g, v);
-      tmem_ld_wait();
-      uint8_t* row = smem + (g >> 1) * kBox + r * 128;
+  for (int hh = 0; hh < 2; ++hh) {
+    ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done[hh]), 0, abort_flag));
+    tc_fence_after();
+    if (ok) {
+#pragma unroll 1
+      for (int g = 8 * hh; g < 8 * hh + 8; ++g) {
+        uint32_t v[32];
+        tmem_ld32(lane_addr + 32 * g, v);
+        tmem_ld_wait();
+        uint8_t* row = smem + (g >> 1) * kBox + r * 128;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = (g & 1) * 4 + i;             // 16-byte chunk of the box row
-        *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) * 16)) =
-            make_uint4(bf16x2_bits(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
-                       bf16x2_bits(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
-                       bf16x2_bits(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
-                       bf16x2_bits(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+        for (int i = 0; i < 4; ++i) {
+          const int c = (g & 1) * 4 + i;             // 16-byte chunk of the box row
+          *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) * 16)) =
+              make_uint4(bf16x2_bits(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
+                         bf16x2_bits(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                         bf16x2_bits(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                         bf16x2_bits(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+        }
       }
+      fence_proxy_async_smem();
     }
-    fence_proxy_async_smem();
+    __syncthreads();
+    if (ok && tid == 0) {
+      for (int i = 4 * hh; i < 4 * hh + 4; ++i) tma_store_3d(&tm_out, sbase + i * kBox, 64 * i, h, n0);
+      bulk_commit_group();
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
-  if (ok && tid == 0) {
-    for (int i = 0; i < 8; ++i) tma_store_3d(&tm_out, sbase + i * kBox, 64 * i, h, n0);
-    bulk_commit_group();
-    bulk_wait_all();
-  }
+  if (tid == 0) bulk_wait_all();
 }
 
 // out^T[h] = W_UV[h] . o_lat[:, h]^T for the sequences n0 .. n0 + n_pad of this CTA, after
@@ -212,18 +230,21 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
   const int n_here = min(n_pad, kUpN);                 // the TMA box height (rows past B arrive as zeros)
   const uint32_t b_bytes = (uint32_t)n_here * 128;
   if (tid == 0) {
-    mbar_init(smem_u32(&bars->full), 1);
-    mbar_init(smem_u32(&bars->done), 1);
+    for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars->full[i]), 1);
+    mbar_init(smem_u32(&bars->done[0]), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
   if (warp == 0) { tmem_alloc(smem_u32(&bars->tmem_base), 64); tmem_relinquish(); }
-  // weights do not depend on the merge: start their loads at once
+  // weights do not depend on the merge: start their loads at once.  Box i of the weights and
+  // box i of the latent rows complete one barrier, so the MMAs over K box i start as it lands.
   const uint32_t a_st = sbase, b_st = sbase + 8 * kBox;
   __syncthreads();
   if (tid == 0) {
-    mbar_arrive_expect_tx(smem_u32(&bars->full), 8u * kBox + 8u * b_bytes);
-    for (int i = 0; i < 8; ++i) tma_load_2d(a_st + i * kBox, &tm_w, 64 * i, 128 * h, smem_u32(&bars->full));
+    for (int i = 0; i < 8; ++i) {
+      mbar_arrive_expect_tx(smem_u32(&bars->full[i]), (uint32_t)kBox + b_bytes);
+      tma_load_2d(a_st + i * kBox, &tm_w, 64 * i, 128 * h, smem_u32(&bars->full[i]));
+    }
   }
   griddep_wait();                          // the plan and latent sums come from earlier kernels
   griddep_launch_dependents();
@@ -280,25 +301,31 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   if (tid == 0) {
-    const uint32_t full = smem_u32(&bars->full);
-    for (int i = 0; i < 8; ++i) load_rows(b_st + i * b_bytes, &tm_o, 64 * i, h, n0, full);
-    bool ok = mbar_wait(full, 0, abort_flag);
-    tc_fence_after();
+    for (int i = 0; i < 8; ++i) load_rows(b_st + i * b_bytes, &tm_o, 64 * i, h, n0, smem_u32(&bars->full[i]));
     const uint32_t idesc = idesc_bf16_f32(128, n_here, false, false);
     const uint64_t a0 = sdesc_sw128(a_st, 16, 1024), b0 = sdesc_sw128(b_st, 16, 1024);
-    if (ok) {
-      for (int c = 0; c < 8; ++c)
+    bool ok = true;
+    for (int c = 0; c < 8 && ok; ++c) {
+      ok = mbar_wait(smem_u32(&bars->full[c]), 0, abort_flag);
+      tc_fence_after();
+      if (ok) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_ss(tmem, a0 + (uint64_t)((c * kBox + 32 * k) >> 4), b0 + (uint64_t)((c * b_bytes + 32 * k) >> 4), idesc,
                  (c > 0 || k > 0) ? 1u : 0u);
-    } else if (atomicExch(&bars->abort, 1) == 0) {
-      atomicOr(check, kCheckTimeout);
+      }
     }
-    mma_commit(smem_u32(&bars->done));
+    if (!ok) {
+      if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+      for (int c = 0; c < 8; ++c) {           // let every copy in flight land before the CTA exits
+        volatile int never = 0;
+        mbar_wait(smem_u32(&bars->full[c]), 0, &never);
+      }
+    }
+    mma_commit(smem_u32(&bars->done[0]));
   }
   __syncwarp();
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort_flag));
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done[0]), 0, abort_flag));
   tc_fence_after();
   // epilogue: thread = value row v (TMEM lane) holding up to 64 sequences; transposed through
   // shared memory (the weight region is free now) into [sequence][128 v] bf16 rows, then
