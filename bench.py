@@ -40,8 +40,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "absorbed-MLA decode µs/step, latent-KV GB/s and % of roofline at B×s_ctx"
-DECODE_SOURCES = ["mla_absorbed_latent_decode_gb300/csrc/decode_simt.cu",
-                  "mla_absorbed_latent_decode_gb300/csrc/decode_tc.cu"]
+DECODE_SOURCES = ["mla_absorbed_latent_decode_gb300/csrc/decode_tc.cu"]
 
 
 def parse():

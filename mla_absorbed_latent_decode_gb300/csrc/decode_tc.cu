@@ -74,6 +74,8 @@ constexpr uint32_t kTmS = 384;             // buffer b at kTmS + 64 b
 
 struct Bars {                               // mbarriers (8 bytes each) and flags
   uint64_t full[kStages];                   // TMA tile landed                      (producer, tx)
+  uint64_t conv[kStages];                   // FP8 cache: tile converted to bf16    (4 exchange warps)
+  uint64_t cread[kStages];                  // FP8 cache: every code of the tile read (4 exchange warps)
   uint64_t empty[kStages];                  // tile consumed by P . C               (MMA commit)
   uint64_t sfull[2];                        // partial scores S_r(j) in TMEM        (MMA commit)
   uint64_t xread[2];                        // exchange warps have read S_r(j)      (4 warps)
@@ -112,6 +114,28 @@ __device__ __forceinline__ void load_scores(uint32_t lane_addr, int bb, uint32_t
   tmem_ld_wait();
 }
 
+// FP8 cache: e4m3 -> bf16, exact (every e4m3 value is a normal fp16 or zero, and a bf16).  Two
+// e4m3 codes -> fp16 pair by cvt; fp16 -> bf16 by moving the exponent bias from 15 to 127 and
+// dropping three mantissa bits that are zero for these values.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_exact(uint32_t w) {
+  const uint32_t t = (w >> 3) & 0x0FFF0FFFu;                  // magnitudes, realigned
+  const uint32_t add = ((t & 0x0000FFFFu) ? 0x00003800u : 0u) | ((t & 0xFFFF0000u) ? 0x38000000u : 0u);
+  return (w & 0x80008000u) | (t + add);
+}
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
+  uint32_t h0, h1;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(h0), "=r"(h1)
+      : "r"(w));
+  return make_uint2(f16x2_to_bf16x2_exact(h0), f16x2_to_bf16x2_exact(h1));
+}
+
+// kFp8: the cache holds e4m3 codes.  The producer TMA-loads each 64 x 64 code box into the
+// upper half of the 8 KB slot its bf16 chunk will occupy; the exchange warps convert the
+// tile in place (all reads, a barrier, then all writes) before QK^T may use it.  The tensor
+// scale is folded into the softmax scale and the output scale by the launcher.
+template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __restrict__ ctx_len, int n_h,
                  const int32_t* __restrict__ block_table, int bt_stride, int num_pages, float scale_log2,
@@ -139,7 +163,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
   const int n_chunks = rank == 0 ? 4 : 5;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(smem_u32(&bars->full[s]), 1); mbar_init(smem_u32(&bars->empty[s]), 1); }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->empty[s]), 1);
+      mbar_init(smem_u32(&bars->conv[s]), 4);
+      mbar_init(smem_u32(&bars->cread[s]), 4);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->sfull[i]), 1);
       mbar_init(smem_u32(&bars->xread[i]), 4);
@@ -199,7 +228,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const int32_t* bt_row = block_table + (size_t)b * bt_stride + unit.page_begin;
-      const uint32_t bytes = (uint32_t)(n_chunks * kChunkBytes);
+      const uint32_t bytes = (uint32_t)(n_chunks * (kFp8 ? kChunkBytes / 2 : kChunkBytes));
       int issued = 0;
       for (int j = 0; j < n_tiles; ++j) {
         const int s = j % kStages;
@@ -217,9 +246,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
         }
         const uint32_t full = smem_u32(&bars->full[s]);
         mbar_arrive_expect_tx(full, bytes);
-        for (int c = 0; c < n_chunks; ++c)
-          tma_load_2d(stage0 + s * kStageBytes + c * kChunkBytes, &tmap, (int)(rank * 256 + c * 64), page * kPage,
-                      full);
+        for (int c = 0; c < n_chunks; ++c)   // FP8: the 4 KB code box into the upper half of its chunk slot
+          tma_load_2d(stage0 + s * kStageBytes + c * kChunkBytes + (kFp8 ? kChunkBytes / 2 : 0), &tmap,
+                      (int)(rank * 256 + c * 64), page * kPage, full);
         issued = j + 1;
       }
       // drain: every load issued has landed before the CTA may exit
@@ -238,7 +267,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
       for (int j = 0; j <= n_tiles && ok; ++j) {
         if (j < n_tiles) {
           const int s = j % kStages, bb = j & 1;
-          if (!mbar_wait(smem_u32(&bars->full[s]), (j / kStages) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(kFp8 ? &bars->conv[s] : &bars->full[s]), (j / kStages) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t st = stage0 + s * kStageBytes;
           const uint32_t d = tmem + kTmS + 64 * bb;
@@ -284,8 +316,50 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
     const int h = tid - 128;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
     const uint32_t recv_peer = map_to_rank(sbase + kOffRecv, peer);
+    // FP8 cache: convert tile t in place, thread = (row h / 2, 32-column half h % 2) of every chunk
+    // (every wait bounded: a warp that gives up returns false, and the kernel aborts)
+    auto convert = [&](int t) {
+      const int s = t % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (t / kStages) & 1, abort_flag))) return false;
+      uint8_t* st = smem + kOffStages + s * kStageBytes;
+      const int r = h >> 1, hf = h & 1;
+      uint4 v[10];
+#pragma unroll
+      for (int c = 0; c < 5; ++c) {
+        if (c < n_chunks) {
+          const uint4* src = reinterpret_cast<const uint4*>(st + c * kChunkBytes + kChunkBytes / 2 + r * 64 + hf * 32);
+          v[2 * c] = src[0];
+          v[2 * c + 1] = src[1];
+        }
+      }
+      // every code of the tile read (by all four warps) before any is overwritten
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->cread[s]));
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->cread[s]), (t / kStages) & 1, abort_flag))) return false;
+#pragma unroll
+      for (int c = 0; c < 5; ++c) {
+        if (c < n_chunks) {
+          uint8_t* row = st + c * kChunkBytes + r * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {       // 16-byte chunk 4 hf + i of the row: 8 codes
+            const uint4 w = v[2 * c + (i >> 1)];
+            const uint2 lo = e4m3x4_to_bf16x4((i & 1) ? w.z : w.x), hi = e4m3x4_to_bf16x4((i & 1) ? w.w : w.y);
+            *reinterpret_cast<uint4*>(row + (((4 * hf + i) ^ (r & 7)) * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->conv[s]));
+      return true;
+    };
+    if (kFp8 && n_tiles > 0 && !convert(0)) fail_timeout(bars, check);
     for (int j = 0; j < n_tiles; ++j) {
       const int bb = j & 1, slot = j & (kSlots - 1);
+      if (kFp8 && j + 1 < n_tiles && !convert(j + 1)) {
+        fail_timeout(bars, check);
+        break;
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sfull[bb]), (j >> 1) & 1, abort_flag))) break;
       tc_fence_after();
       uint32_t r0[32], r1[32];
@@ -490,36 +564,56 @@ cudaError_t make_cache_tensor_map(const void* cache, int num_pages, CUtensorMap*
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor map of an e4m3 cache [num_pages * 64 rows][576 bytes]: 64 x 64-byte boxes, no swizzle
+// (the kernel converts them into 128-byte-swizzled bf16 chunks).
+cudaError_t make_cache_tensor_map_fp8(const void* cache, int num_pages, CUtensorMap* map) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)num_pages * kPage};
+  const cuuint64_t strides[1] = {(cuuint64_t)kRow};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+  const cuuint32_t elem[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims, strides, box, elem,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 namespace {
+template <bool kFp8>
 cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, const int32_t* block_table, int bt_stride,
                              int num_pages, const CUtensorMap& map, const Workspace& ws, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_tc_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const float scale_log2 = h.scale * 1.4426950408889634f;
-  return launch_pdl(decode_tc_kernel, dim3(2 * ws.max_units), dim3(kThreads), kSmemBytes, st, map, ctx_len,
-                    h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, 1.0f, ws, h.check_word);
+  // an FP8 cache holds codes of value / fp8_scale: the scale multiplies every score and the output
+  const float cache_scale = kFp8 ? h.cfg.fp8_scale : 1.0f;
+  const float scale_log2 = h.scale * cache_scale * 1.4426950408889634f;
+  return launch_pdl(decode_tc_kernel<kFp8>, dim3(2 * ws.max_units), dim3(kThreads), kSmemBytes, st, map, ctx_len,
+                    h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, ws, h.check_word);
 }
 }  // namespace
 
-// Decode-kernel dispatch: the tensor-core kernel for a bf16 cache; the FP8 cache
-// still runs the CUDA-core kernel.
+// Decode-kernel dispatch: the tensor-core kernel, with in-shared-memory e4m3 -> bf16
+// conversion for an FP8 cache.
 cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table,
                           int bt_stride, const void* cache, int num_pages, const Workspace& ws, cudaStream_t st) {
-  if (h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3)
-    return launch_decode_simt(h, ctx_len, batch, block_table, bt_stride, cache, num_pages, ws, st);
+  const bool fp8 = h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3;
   Handle& hm = const_cast<Handle&>(h);
   if (hm.tmap_cache != cache || hm.tmap_pages != num_pages) {
-    cudaError_t e = make_cache_tensor_map(cache, num_pages, reinterpret_cast<CUtensorMap*>(hm.tmap));
+    cudaError_t e = fp8 ? make_cache_tensor_map_fp8(cache, num_pages, reinterpret_cast<CUtensorMap*>(hm.tmap))
+                        : make_cache_tensor_map(cache, num_pages, reinterpret_cast<CUtensorMap*>(hm.tmap));
     if (e != cudaSuccess) return e;
     hm.tmap_cache = cache;
     hm.tmap_pages = num_pages;
   }
-  return launch_decode_tc(h, ctx_len, block_table, bt_stride, num_pages, *reinterpret_cast<const CUtensorMap*>(hm.tmap),
-                          ws, st);
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(hm.tmap);
+  return fp8 ? launch_decode_tc<true>(h, ctx_len, block_table, bt_stride, num_pages, map, ws, st)
+             : launch_decode_tc<false>(h, ctx_len, block_table, bt_stride, num_pages, map, ws, st);
 }
 
 }  // namespace mla

@@ -93,9 +93,6 @@ cudaError_t launch_q_absorb(const Handle& h, const __nv_bfloat16* q, const int32
 cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch,
                           const int32_t* block_table, int bt_stride, const void* cache,
                           int num_pages, const Workspace& ws, cudaStream_t st);
-cudaError_t launch_decode_simt(const Handle& h, const int32_t* ctx_len, int batch,
-                               const int32_t* block_table, int bt_stride, const void* cache,
-                               int num_pages, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_combine_uv(const Handle& h, int batch, const Workspace& ws,
                               __nv_bfloat16* out, cudaStream_t st);
 
