@@ -12,14 +12,16 @@
 // Design (one 2-CTA cluster per unit; heads are the 128-row M dimension, so one
 // cache tile serves every head of the sequence):
 //   * The 576 columns are split between the two CTAs of the cluster:
-//       CTA 0 ("lo"): latent columns [0, 256)
-//       CTA 1 ("hi"): latent columns [256, 512) and the RoPE key [512, 576)
-//     Each CTA TMA-loads only its columns of every 64-token page (32 / 40 KB),
-//     so the pair reads each cache byte from HBM once.
+//       CTA 0: latent columns [0, 256)   and RoPE-key columns [512, 544)
+//       CTA 1: latent columns [256, 512) and RoPE-key columns [544, 576)
+//     Each CTA TMA-loads only its columns of every 64-token page (32 KB of latent
+//     in 128-byte-swizzled boxes, 4 KB of RoPE key in a 64-byte-swizzled box) into
+//     a 4-deep ring, so the pair reads each cache byte from HBM once and both CTAs
+//     carry the same QK^T work.
 //   * QK^T is split along K: each CTA computes a partial score tile
 //       S_r[128 heads x 64 tokens] = Q_r . C_r^T
-//     with Q_r's latent part resident in TMEM (A operand) and, on CTA 1, the
-//     RoPE part of the query in shared memory.  Four "exchange" warps read S_r
+//     with Q_r's latent part resident in TMEM (A operand) and its half of the
+//     RoPE query in shared memory.  Four "exchange" warps read S_r
 //     as soon as it lands, scale it to the base-2 softmax domain, round it to
 //     fp16 and st.async it into the peer's receive slot (16 KB per tile each
 //     way, 4 slots).  The softmax warps form x = fp16(x_lo) + fp16(x_hi) in the
@@ -52,10 +54,11 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 3;                 // cache tiles in flight per CTA
+constexpr int kStages = 4;                 // cache tiles in flight per CTA
 constexpr int kChunkBytes = kPage * 128;   // one 64-token x 64-column bf16 box (SW128): 8 KB
-constexpr int kStageBytes = 5 * kChunkBytes;
-constexpr int kQpeBytes = kMaxHeads * 128;             // 128 heads x 64 bf16, SW128 K-major
+constexpr int kRopeBytes = kPage * 64;     // one 64-token x 32-column bf16 box of the RoPE key (SW64): 4 KB
+constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes;
+constexpr int kQpeBytes = kMaxHeads * 64;              // 128 heads x 32 bf16 of the RoPE query, SW64 K-major
 constexpr int kSlots = 4;                              // partial-score receive slots
 constexpr int kSlotBytes = kMaxHeads * kPage * 2;      // 128 x 64 fp16 = 16 KB
 constexpr int kOffStages = 0;
@@ -137,7 +140,8 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
 // scale is folded into the softmax scale and the output scale by the launcher.
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __restrict__ ctx_len, int n_h,
+decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_rope,
+                 const int32_t* __restrict__ ctx_len, int n_h,
                  const int32_t* __restrict__ block_table, int bt_stride, int num_pages, float scale_log2,
                  float out_scale, Workspace ws, unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
@@ -160,7 +164,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
   const int L = ctx_len[b];
   const int t_end = min(unit.page_end * kPage, L);
   const int n_tiles = unit.page_end - unit.page_begin;
-  const int n_chunks = rank == 0 ? 4 : 5;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -185,7 +188,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
     tmem_relinquish();
   }
-  if (warp == kWarpProducer && lane == 0) prefetch_tmap(&tmap);
+  if (warp == kWarpProducer && lane == 0) {
+    prefetch_tmap(&tmap);
+    prefetch_tmap(&tmap_rope);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -207,12 +213,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
       }
       tmem_st32(lane_addr + kTmQ + 32 * part, r);
     }
-    if (rank == 1) {
+    {
+      // this CTA's 32 RoPE query values: 64-byte rows in the 64-byte swizzle
       uint8_t* qpe = smem + kOffQpe;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 v = live ? src[64 + k] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qpe + h * 128 + ((k ^ (h & 7)) * 16)) = v;
+      for (int k = 0; k < 4; ++k) {
+        const uint4 v = live ? src[64 + rank * 4 + k] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qpe + h * 64 + ((k ^ ((h >> 1) & 3)) * 16)) = v;
       }
       fence_proxy_async_smem();
     }
@@ -228,7 +235,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const int32_t* bt_row = block_table + (size_t)b * bt_stride + unit.page_begin;
-      const uint32_t bytes = (uint32_t)(n_chunks * (kFp8 ? kChunkBytes / 2 : kChunkBytes));
+      const uint32_t bytes = (uint32_t)(kFp8 ? kStageBytes / 2 : kStageBytes);
       int issued = 0;
       for (int j = 0; j < n_tiles; ++j) {
         const int s = j % kStages;
@@ -246,9 +253,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
         }
         const uint32_t full = smem_u32(&bars->full[s]);
         mbar_arrive_expect_tx(full, bytes);
-        for (int c = 0; c < n_chunks; ++c)   // FP8: the 4 KB code box into the upper half of its chunk slot
+        for (int c = 0; c < 4; ++c)          // FP8: each code box into the upper half of its chunk slot
           tma_load_2d(stage0 + s * kStageBytes + c * kChunkBytes + (kFp8 ? kChunkBytes / 2 : 0), &tmap,
                       (int)(rank * 256 + c * 64), page * kPage, full);
+        tma_load_2d(stage0 + s * kStageBytes + 4 * kChunkBytes + (kFp8 ? kRopeBytes / 2 : 0), &tmap_rope,
+                    (int)(kDc + rank * 32), page * kPage, full);
         issued = j + 1;
       }
       // drain: every load issued has landed before the CTA may exit
@@ -278,12 +287,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
           for (int k = 0; k < 16; ++k)
             mma_ts(d, tmem + kTmQ + 8 * k, sdesc_sw128(st + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024),
                    idesc_qk, k > 0);
-          if (rank == 1) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(d, sdesc_sw128(qpe + 32 * k, 16, 1024), sdesc_sw128(st + 4 * kChunkBytes + 32 * k, 16, 1024),
-                     idesc_qk, 1);
-          }
+          for (int k = 0; k < 2; ++k)
+            mma_ss(d, sdesc_sw64(qpe + 32 * k, 16, 512), sdesc_sw64(st + 4 * kChunkBytes + 32 * k, 16, 512), idesc_qk,
+                   1);
           mma_commit(smem_u32(&bars->sfull[bb]));
         }
         if (j >= 1) {
@@ -323,29 +330,35 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const int32_t* __rest
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (t / kStages) & 1, abort_flag))) return false;
       uint8_t* st = smem + kOffStages + s * kStageBytes;
       const int r = h >> 1, hf = h & 1;
-      uint4 v[10];
+      uint4 v[9];
 #pragma unroll
-      for (int c = 0; c < 5; ++c) {
-        if (c < n_chunks) {
-          const uint4* src = reinterpret_cast<const uint4*>(st + c * kChunkBytes + kChunkBytes / 2 + r * 64 + hf * 32);
-          v[2 * c] = src[0];
-          v[2 * c + 1] = src[1];
-        }
+      for (int c = 0; c < 4; ++c) {
+        const uint4* src = reinterpret_cast<const uint4*>(st + c * kChunkBytes + kChunkBytes / 2 + r * 64 + hf * 32);
+        v[2 * c] = src[0];
+        v[2 * c + 1] = src[1];
       }
+      v[8] = *reinterpret_cast<const uint4*>(st + 4 * kChunkBytes + kRopeBytes / 2 + r * 32 + hf * 16);
       // every code of the tile read (by all four warps) before any is overwritten
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->cread[s]));
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->cread[s]), (t / kStages) & 1, abort_flag))) return false;
 #pragma unroll
-      for (int c = 0; c < 5; ++c) {
-        if (c < n_chunks) {
-          uint8_t* row = st + c * kChunkBytes + r * 128;
+      for (int c = 0; c < 4; ++c) {           // latent: 128-byte rows, 128-byte swizzle
+        uint8_t* row = st + c * kChunkBytes + r * 128;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {       // 16-byte chunk 4 hf + i of the row: 8 codes
-            const uint4 w = v[2 * c + (i >> 1)];
-            const uint2 lo = e4m3x4_to_bf16x4((i & 1) ? w.z : w.x), hi = e4m3x4_to_bf16x4((i & 1) ? w.w : w.y);
-            *reinterpret_cast<uint4*>(row + (((4 * hf + i) ^ (r & 7)) * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-          }
+        for (int i = 0; i < 4; ++i) {         // 16-byte chunk 4 hf + i of the row: 8 codes
+          const uint4 w = v[2 * c + (i >> 1)];
+          const uint2 lo = e4m3x4_to_bf16x4((i & 1) ? w.z : w.x), hi = e4m3x4_to_bf16x4((i & 1) ? w.w : w.y);
+          *reinterpret_cast<uint4*>(row + (((4 * hf + i) ^ (r & 7)) * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        }
+      }
+      {                                       // RoPE key: 64-byte rows, 64-byte swizzle
+        uint8_t* row = st + 4 * kChunkBytes + r * 64;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {         // 16-byte chunk 2 hf + i of the row: 8 codes
+          const uint32_t a = i ? v[8].z : v[8].x, c2 = i ? v[8].w : v[8].y;
+          const uint2 lo = e4m3x4_to_bf16x4(a), hi = e4m3x4_to_bf16x4(c2);
+          *reinterpret_cast<uint4*>(row + (((2 * hf + i) ^ ((r >> 1) & 3)) * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
         }
       }
       fence_proxy_async_smem();
@@ -550,28 +563,29 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
-// Tensor map of a bf16 cache [num_pages * 64 rows][576]: 64 x 64 boxes, 128-byte swizzle.
-cudaError_t make_cache_tensor_map(const void* cache, int num_pages, CUtensorMap* map) {
+// Tensor map of a bf16 cache [num_pages * 64 rows][576]: boxes of `width` columns x 64 rows,
+// 128-byte swizzle for 64 columns (latent), 64-byte swizzle for 32 (RoPE key).
+cudaError_t make_cache_tensor_map(const void* cache, int num_pages, int width, CUtensorMap* map) {
   auto enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)num_pages * kPage};
   const cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+  const cuuint32_t box[2] = {(cuuint32_t)width, (cuuint32_t)kPage};
   const cuuint32_t elem[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, elem,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, width == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Tensor map of an e4m3 cache [num_pages * 64 rows][576 bytes]: 64 x 64-byte boxes, no swizzle
-// (the kernel converts them into 128-byte-swizzled bf16 chunks).
-cudaError_t make_cache_tensor_map_fp8(const void* cache, int num_pages, CUtensorMap* map) {
+// Tensor map of an e4m3 cache [num_pages * 64 rows][576 bytes]: boxes of `width` bytes x 64
+// rows, no swizzle (the kernel converts them into swizzled bf16 chunks).
+cudaError_t make_cache_tensor_map_fp8(const void* cache, int num_pages, int width, CUtensorMap* map) {
   auto enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)num_pages * kPage};
   const cuuint64_t strides[1] = {(cuuint64_t)kRow};
-  const cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+  const cuuint32_t box[2] = {(cuuint32_t)width, (cuuint32_t)kPage};
   const cuuint32_t elem[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims, strides, box, elem,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -582,7 +596,8 @@ cudaError_t make_cache_tensor_map_fp8(const void* cache, int num_pages, CUtensor
 namespace {
 template <bool kFp8>
 cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, const int32_t* block_table, int bt_stride,
-                             int num_pages, const CUtensorMap& map, const Workspace& ws, cudaStream_t st) {
+                             int num_pages, const CUtensorMap& map, const CUtensorMap& map_rope, const Workspace& ws,
+                             cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e =
@@ -593,7 +608,8 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, const int3
   // an FP8 cache holds codes of value / fp8_scale: the scale multiplies every score and the output
   const float cache_scale = kFp8 ? h.cfg.fp8_scale : 1.0f;
   const float scale_log2 = h.scale * cache_scale * 1.4426950408889634f;
-  return launch_pdl(decode_tc_kernel<kFp8>, dim3(2 * ws.max_units), dim3(kThreads), kSmemBytes, st, map, ctx_len,
+  return launch_pdl(decode_tc_kernel<kFp8>, dim3(2 * ws.max_units), dim3(kThreads), kSmemBytes, st, map, map_rope,
+                    ctx_len,
                     h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, ws, h.check_word);
 }
 }  // namespace
@@ -605,15 +621,19 @@ cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, co
   const bool fp8 = h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3;
   Handle& hm = const_cast<Handle&>(h);
   if (hm.tmap_cache != cache || hm.tmap_pages != num_pages) {
-    cudaError_t e = fp8 ? make_cache_tensor_map_fp8(cache, num_pages, reinterpret_cast<CUtensorMap*>(hm.tmap))
-                        : make_cache_tensor_map(cache, num_pages, reinterpret_cast<CUtensorMap*>(hm.tmap));
+    CUtensorMap* m = reinterpret_cast<CUtensorMap*>(hm.tmap);
+    CUtensorMap* mr = reinterpret_cast<CUtensorMap*>(hm.tmap_rope);
+    cudaError_t e = fp8 ? make_cache_tensor_map_fp8(cache, num_pages, 64, m) : make_cache_tensor_map(cache, num_pages, 64, m);
+    if (e == cudaSuccess)
+      e = fp8 ? make_cache_tensor_map_fp8(cache, num_pages, 32, mr) : make_cache_tensor_map(cache, num_pages, 32, mr);
     if (e != cudaSuccess) return e;
     hm.tmap_cache = cache;
     hm.tmap_pages = num_pages;
   }
   const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(hm.tmap);
-  return fp8 ? launch_decode_tc<true>(h, ctx_len, block_table, bt_stride, num_pages, map, ws, st)
-             : launch_decode_tc<false>(h, ctx_len, block_table, bt_stride, num_pages, map, ws, st);
+  const CUtensorMap& map_rope = *reinterpret_cast<const CUtensorMap*>(hm.tmap_rope);
+  return fp8 ? launch_decode_tc<true>(h, ctx_len, block_table, bt_stride, num_pages, map, map_rope, ws, st)
+             : launch_decode_tc<false>(h, ctx_len, block_table, bt_stride, num_pages, map, map_rope, ws, st);
 }
 
 }  // namespace mla

@@ -67,6 +67,7 @@ struct Handle {
   cudaEvent_t ev[8];
   int n_ev_recorded;
   alignas(64) unsigned char tmap[128];   // TMA descriptor (CUtensorMap) of the last cache seen
+  alignas(64) unsigned char tmap_rope[128];  // same cache, RoPE-key columns (32-column boxes)
   alignas(64) unsigned char tmap_wuk[128];  // TMA descriptors of the handle's weight copies
   alignas(64) unsigned char tmap_wuv[128];
   const void* tmap_cache;

@@ -254,6 +254,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
+// Same for the 64-byte swizzle (the layout a TMA load with CU_TENSOR_MAP_SWIZZLE_64B
+// writes: 64-byte rows, 16-byte chunk c of row r at c ^ ((r >> 1) & 3)), layout type 4.
+// The start address lies in a 512-byte aligned atom and may advance by 32 bytes inside a row.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
+
 // Tensor Memory loads / stores, 32 lanes x 32 bits, `x32`: 32 consecutive columns
 // per thread (thread i of the warp owns lane (warp % 4) * 32 + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
