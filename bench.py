@@ -373,13 +373,15 @@ def run_ours(args):
             "us_per_step": round(ms * 1000.0, 2), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
             "roofline_us": round(roof_us, 2), "roofline_frac_step": round(roof_us / (ms * 1000.0), 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "s_ctx": wl.max_ctx, "n_h": wl.n_h, "d_c": wl.d_c,
                        "d_rope": wl.d_rope, "cache": "fp8_e4m3" if wl.cache_dtype == 2 else "bf16",
                        "total_tokens": wl.total_tokens,
                        "l2": f"flushed between steps (write of {flush.numel() >> 20} MiB, outside the timed events)",
                        "timing": "value from K steps without per-kernel events; per_kernel_us and roofline "
                                  "from a second K-step pass with per-kernel events (which serialise the kernels)",
+                       "arithmetic": "bf16 MMA operands (an FP8 cache is converted to bf16 in shared memory), "
+                                     "fp32 accumulation and softmax, fp16 partial scores between the CTA pair",
                        "parallelism": f"replicas x{world}"},
             "per_kernel_us": per_kernel,
             "roofline": {"bound": "hbm", "kernel": "mla_decode_splitkv", "achieved": round(achieved, 1),
