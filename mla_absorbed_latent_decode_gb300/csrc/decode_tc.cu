@@ -27,13 +27,14 @@
 //     way, 4 slots).  The softmax warps form x = fp16(x_lo) + fp16(x_hi) in the
 //     same order on both CTAs, so both compute bit-identical softmax weights.
 //     fp16 keeps 11 bits of a logit, finer than the bf16 P it feeds.
-//   * P (bf16) is written back into TMEM over S and used as the A operand of
-//     O_r[128 x 256] += P . C_r[64 tokens x 256 latent]; the same shared-memory
+//   * P (bf16) is written into one of two P slots in TMEM and used as the A operand
+//     of O_r[128 x 256] += P . C_r[64 tokens x 256 latent]; the same shared-memory
 //     tile is the B operand, read MN-major.  Each CTA accumulates its half of
 //     the latent output in TMEM (256 columns).
-//   * TMEM per CTA (512 columns): O_r [0,256), Q_r [256,384), S/P buffers
-//     [384,448) and [448,512) (double-buffered so QK^T of tile j+1 overlaps the
-//     softmax of tile j).
+//   * TMEM per CTA (512 columns): O_r [0,256), Q_r [256,384), S [384,448), P slots
+//     [448,480) and [480,512).  The score buffer is free as soon as the softmax and
+//     exchange warps have loaded it, so QK^T of tile j+1 is issued when tile j's
+//     softmax starts, not when it ends; P(j) keeps its own slot until P . C reads it.
 //   * Online softmax in the base-2 domain with a lazy rescale: the running max
 //     only moves (and O is rescaled in TMEM) when a tile's max exceeds it by more
 //     than 8, so P <= 2^8.
@@ -73,16 +74,17 @@ constexpr int kWarpMma = 9;
 // TMEM column map
 constexpr uint32_t kTmO = 0;
 constexpr uint32_t kTmQ = 256;
-constexpr uint32_t kTmS = 384;             // buffer b at kTmS + 64 b
+constexpr uint32_t kTmS = 384;             // 64 columns of fp32 partial scores
+constexpr uint32_t kTmP = 448;             // P slot b (64 bf16 per lane) at kTmP + 32 b
 
 struct Bars {                               // mbarriers (8 bytes each) and flags
   uint64_t full[kStages];                   // TMA tile landed                      (producer, tx)
   uint64_t conv[kStages];                   // FP8 cache: tile converted to bf16    (4 exchange warps)
   uint64_t cread[kStages];                  // FP8 cache: every code of the tile read (4 exchange warps)
   uint64_t empty[kStages];                  // tile consumed by P . C               (MMA commit)
-  uint64_t sfull[2];                        // partial scores S_r(j) in TMEM        (MMA commit)
-  uint64_t xread[2];                        // exchange warps have read S_r(j)      (4 warps)
-  uint64_t pfull[2];                        // P(j) written over S_r(j)             (4 warps)
+  uint64_t sfull;                           // partial scores S_r(j) in TMEM        (MMA commit)
+  uint64_t sfree;                           // S_r(j) loaded by softmax + exchange  (8 warps)
+  uint64_t pfull[2];                        // P(j) written into P slot j % 2       (4 warps)
   uint64_t odone;                           // one phase per P . C tile             (MMA commit)
   uint64_t ofinal;                          // single phase: the last P . C landed  (MMA commit)
   uint64_t recvfull[kSlots];                // peer's partial scores arrived        (1 + 16 KB tx)
@@ -110,10 +112,10 @@ __device__ __forceinline__ void fail_timeout(Bars* bars, unsigned* check) {
   if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
 }
 
-// Load this thread's 64 partial scores of S buffer `bb` (two x32 loads, one wait).
-__device__ __forceinline__ void load_scores(uint32_t lane_addr, int bb, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
-  tmem_ld32(lane_addr + kTmS + 64 * bb, r0);
-  tmem_ld32(lane_addr + kTmS + 64 * bb + 32, r1);
+// Load this thread's 64 partial scores (two x32 loads, one wait).
+__device__ __forceinline__ void load_scores(uint32_t lane_addr, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+  tmem_ld32(lane_addr + kTmS, r0);
+  tmem_ld32(lane_addr + kTmS + 32, r1);
   tmem_ld_wait();
 }
 
@@ -172,11 +174,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       mbar_init(smem_u32(&bars->conv[s]), 4);
       mbar_init(smem_u32(&bars->cread[s]), 4);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bars->sfull[i]), 1);
-      mbar_init(smem_u32(&bars->xread[i]), 4);
-      mbar_init(smem_u32(&bars->pfull[i]), 4);
-    }
+    mbar_init(smem_u32(&bars->sfull), 1);
+    mbar_init(smem_u32(&bars->sfree), 8);
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->pfull[i]), 4);
     for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&bars->recvfull[i]), 1);
     mbar_init(smem_u32(&bars->odone), 1);
     mbar_init(smem_u32(&bars->ofinal), 1);
@@ -275,14 +275,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       bool ok = true;
       for (int j = 0; j <= n_tiles && ok; ++j) {
         if (j < n_tiles) {
-          const int s = j % kStages, bb = j & 1;
-          if (!mbar_wait(smem_u32(kFp8 ? &bars->conv[s] : &bars->full[s]), (j / kStages) & 1, abort_flag)) {
+          const int s = j % kStages;
+          // the tile has landed (and been converted), and S(j - 1) has been loaded by both readers
+          if (!mbar_wait(smem_u32(kFp8 ? &bars->conv[s] : &bars->full[s]), (j / kStages) & 1, abort_flag) ||
+              (j > 0 && !mbar_wait(smem_u32(&bars->sfree), (j - 1) & 1, abort_flag))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t st = stage0 + s * kStageBytes;
-          const uint32_t d = tmem + kTmS + 64 * bb;
+          const uint32_t d = tmem + kTmS;
 #pragma unroll
           for (int k = 0; k < 16; ++k)
             mma_ts(d, tmem + kTmQ + 8 * k, sdesc_sw128(st + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024),
@@ -291,7 +293,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
           for (int k = 0; k < 2; ++k)
             mma_ss(d, sdesc_sw64(qpe + 32 * k, 16, 512), sdesc_sw64(st + 4 * kChunkBytes + 32 * k, 16, 512), idesc_qk,
                    1);
-          mma_commit(smem_u32(&bars->sfull[bb]));
+          mma_commit(smem_u32(&bars->sfull));
         }
         if (j >= 1) {
           const int jj = j - 1, s = jj % kStages, bb = jj & 1;
@@ -300,7 +302,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
           const uint32_t st = stage0 + s * kStageBytes;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + kTmO, tmem + kTmS + 64 * bb + 8 * k, sdesc_sw128(st + 2048 * k, kChunkBytes, 1024),
+            mma_ts(tmem + kTmO, tmem + kTmP + 32 * bb + 8 * k, sdesc_sw128(st + 2048 * k, kChunkBytes, 1024),
                    idesc_pv, (jj > 0 || k > 0) ? 1u : 0u);
           mma_commit(smem_u32(&bars->empty[s]));
           mma_commit(smem_u32(&bars->odone));
@@ -316,10 +318,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // ------------------------------------------------------------ exchange: S_r(j) -> peer
     // As soon as QK^T of tile j lands, read this CTA's partial scores, scale them to the
     // base-2 softmax domain, round to fp16 and store them into the peer's receive slot
-    // j % 4.  No "slot free" handshake is needed: this CTA's QK^T of tile j was issued
-    // only after its softmax finished tile j - 2, which had received the peer's tile
-    // j - 2, which the peer sent only after its own QK^T of tile j - 2, issued only after
-    // the peer's softmax finished tile j - 4 -- the last user of slot j % 4.
+    // j % 4.  No "slot free" handshake is needed: the peer sends tile j only after its
+    // QK^T of tile j, which it issues only after its softmax has started tile j - 1, hence
+    // finished tile j - 2, which needed this CTA's tile j - 2, sent only after this CTA's
+    // QK^T of tile j - 2, issued only after this CTA's softmax had started tile j - 3,
+    // hence finished tile j - 4 -- the last user of slot j % 4.
     const int h = tid - 128;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
     const uint32_t recv_peer = map_to_rank(sbase + kOffRecv, peer);
@@ -368,18 +371,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     };
     if (kFp8 && n_tiles > 0 && !convert(0)) fail_timeout(bars, check);
     for (int j = 0; j < n_tiles; ++j) {
-      const int bb = j & 1, slot = j & (kSlots - 1);
+      const int slot = j & (kSlots - 1);
       if (kFp8 && j + 1 < n_tiles && !convert(j + 1)) {
         fail_timeout(bars, check);
         break;
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sfull[bb]), (j >> 1) & 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sfull), j & 1, abort_flag))) break;
       tc_fence_after();
       uint32_t r0[32], r1[32];
-      load_scores(lane_addr, bb, r0, r1);
+      load_scores(lane_addr, r0, r1);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->xread[bb]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->sfree));
       uint32_t w[32];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -412,12 +415,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       const int valid = min(kPage, t_end - (unit.page_begin + j) * kPage);
       if (tid == 0) mbar_arrive_expect_tx(smem_u32(&bars->recvfull[slot]), (uint32_t)kSlotBytes);
       armed = j + 1;
-      if (!wait_cta(&bars->sfull[bb], (j >> 1) & 1)) { ok = false; break; }
+      if (!wait_cta(&bars->sfull, j & 1)) { ok = false; break; }
       tc_fence_after();
       float x[64];
       {
         uint32_t r0[32], r1[32];
-        load_scores(lane_addr, bb, r0, r1);
+        load_scores(lane_addr, r0, r1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->sfree));   // QK^T of tile j + 1 may overwrite S
         // own partial, rounded exactly as the exchange warps round the copy sent to the peer
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -493,9 +499,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         pk[i] = bf16x2_bits(p0, p1);
       }
       l_sum += psum;
-      // P overwrites S_r(j): the exchange warps must have read it
-      if (!wait_cta(&bars->xread[bb], (j >> 1) & 1)) { ok = false; break; }
-      tmem_st32(lane_addr + kTmS + 64 * bb, pk);
+      // P slot j % 2: its previous user, P . C of tile j - 2, was issued before QK^T of tile j
+      // (which this warp has seen complete), so it has finished reading the slot
+      tmem_st32(lane_addr + kTmP + 32 * bb, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
