@@ -16,15 +16,17 @@
 //       CTA 1: latent columns [256, 512) and RoPE-key columns [544, 576)
 //     Each CTA TMA-loads only its columns of every 64-token page (32 KB of latent
 //     in 128-byte-swizzled boxes, 4 KB of RoPE key in a 64-byte-swizzled box) into
-//     a 4-deep ring, so the pair reads each cache byte from HBM once and both CTAs
+//     a 3-deep ring, so the pair reads each cache byte from HBM once and both CTAs
 //     carry the same QK^T work.
 //   * QK^T is split along K: each CTA computes a partial score tile
 //       S_r[128 heads x 64 tokens] = Q_r . C_r^T
 //     with Q_r's latent part resident in TMEM (A operand) and its half of the
 //     RoPE query in shared memory.  Four "exchange" warps read S_r
 //     as soon as it lands, scale it to the base-2 softmax domain, round it to
-//     fp16 and st.async it into the peer's receive slot (16 KB per tile each
-//     way, 4 slots).  The softmax warps form x = fp16(x_lo) + fp16(x_hi) in the
+//     fp16, stage it in local shared memory and move it into the peer's receive
+//     slot with one 4 KB bulk copy per warp (16 KB per tile each way, 4 slots):
+//     under load, bulk copies move distributed shared memory faster than
+//     16-byte remote stores.  The softmax warps form x = fp16(x_lo) + fp16(x_hi) in the
 //     same order on both CTAs, so both compute bit-identical softmax weights.
 //     fp16 keeps 11 bits of a logit, finer than the bf16 P it feeds.
 //   * P (bf16) is written into one of two P slots in TMEM and used as the A operand
@@ -55,7 +57,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 4;                 // cache tiles in flight per CTA
+constexpr int kStages = 3;                 // cache tiles in flight per CTA
 constexpr int kChunkBytes = kPage * 128;   // one 64-token x 64-column bf16 box (SW128): 8 KB
 constexpr int kRopeBytes = kPage * 64;     // one 64-token x 32-column bf16 box of the RoPE key (SW64): 4 KB
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes;
@@ -65,7 +67,8 @@ constexpr int kSlotBytes = kMaxHeads * kPage * 2;      // 128 x 64 fp16 = 16 KB
 constexpr int kOffStages = 0;
 constexpr int kOffQpe = kOffStages + kStages * kStageBytes;
 constexpr int kOffRecv = kOffQpe + kQpeBytes;
-constexpr int kOffBars = kOffRecv + kSlots * kSlotBytes;
+constexpr int kOffStg = kOffRecv + kSlots * kSlotBytes;   // 2 staging buffers of this CTA's fp16 partials
+constexpr int kOffBars = kOffStg + 2 * kSlotBytes;
 constexpr int kSmemBytes = kOffBars + 1024 + 1024;    // + barriers / flags, + alignment slack
 constexpr int kThreads = 320;                          // 4 softmax, 4 exchange, producer, MMA warps
 constexpr int kWarpProducer = 8;
@@ -389,13 +392,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         w[i] = f16x2_sat(__uint_as_float(r0[2 * i]) * scale_log2, __uint_as_float(r0[2 * i + 1]) * scale_log2);
         w[16 + i] = f16x2_sat(__uint_as_float(r1[2 * i]) * scale_log2, __uint_as_float(r1[2 * i + 1]) * scale_log2);
       }
-      const uint32_t dst = recv_peer + slot * kSlotBytes + h * 128;
-      const uint32_t peer_bar = map_to_rank(smem_u32(&bars->recvfull[slot]), peer);
+      // stage this warp's 32 rows locally, then one 4 KB bulk copy into the peer's slot
+      const int q4 = warp - 4;
+      uint8_t* stg = smem + kOffStg + (j & 1) * kSlotBytes;
+      if (j >= 2) {
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+      }
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        st_async_v4_b32(dst + ((q ^ (h & 7)) * 16), make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]),
-                        peer_bar);
+        *reinterpret_cast<uint4*>(stg + h * 128 + ((q ^ (h & 7)) * 16)) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t dst = recv_peer + slot * kSlotBytes + q4 * 32 * 128;
+        const uint32_t peer_bar = map_to_rank(smem_u32(&bars->recvfull[slot]), peer);
+        asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(dst), "r"(smem_u32(stg + q4 * 32 * 128)), "r"(32 * 128), "r"(peer_bar) : "memory");
+        bulk_commit_group();
+      }
     }
+    if (lane == 0) bulk_wait_all();        // every copy landed before the CTA may exit
   } else {
     // ------------------------------------------------------------ softmax + epilogue (thread = head)
     const int h = tid;
