@@ -16,14 +16,14 @@
 //       CTA 1: latent columns [256, 512) and RoPE-key columns [544, 576)
 //     Each CTA TMA-loads only its columns of every 64-token page (32 KB of latent
 //     in 128-byte-swizzled boxes, 4 KB of RoPE key in a 64-byte-swizzled box) into
-//     a 3-deep ring, so the pair reads each cache byte from HBM once and both CTAs
+//     a 4-deep ring, so the pair reads each cache byte from HBM once and both CTAs
 //     carry the same QK^T work.
 //   * QK^T is split along K: each CTA computes a partial score tile
 //       S_r[128 heads x 64 tokens] = Q_r . C_r^T
 //     with Q_r's latent part resident in TMEM (A operand) and its half of the
 //     RoPE query in shared memory.  Four "exchange" warps read S_r
 //     as soon as it lands, scale it to the base-2 softmax domain, round it to
-//     fp16, stage it in local shared memory and move it into the peer's receive
+//     fp16, stage it in a free receive slot of its own and move it into the peer's receive
 //     slot with one 4 KB bulk copy per warp (16 KB per tile each way, 4 slots):
 //     under load, bulk copies move distributed shared memory faster than
 //     16-byte remote stores.  The softmax warps form x = fp16(x_lo) + fp16(x_hi) in the
@@ -57,7 +57,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 3;                 // cache tiles in flight per CTA
+constexpr int kStages = 4;                 // cache tiles in flight per CTA
 constexpr int kChunkBytes = kPage * 128;   // one 64-token x 64-column bf16 box (SW128): 8 KB
 constexpr int kRopeBytes = kPage * 64;     // one 64-token x 32-column bf16 box of the RoPE key (SW64): 4 KB
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes;
@@ -67,8 +67,7 @@ constexpr int kSlotBytes = kMaxHeads * kPage * 2;      // 128 x 64 fp16 = 16 KB
 constexpr int kOffStages = 0;
 constexpr int kOffQpe = kOffStages + kStages * kStageBytes;
 constexpr int kOffRecv = kOffQpe + kQpeBytes;
-constexpr int kOffStg = kOffRecv + kSlots * kSlotBytes;   // 2 staging buffers of this CTA's fp16 partials
-constexpr int kOffBars = kOffStg + 2 * kSlotBytes;
+constexpr int kOffBars = kOffRecv + kSlots * kSlotBytes;
 constexpr int kSmemBytes = kOffBars + 1024 + 1024;    // + barriers / flags, + alignment slack
 constexpr int kThreads = 320;                          // 4 softmax, 4 exchange, producer, MMA warps
 constexpr int kWarpProducer = 8;
@@ -392,13 +391,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         w[i] = f16x2_sat(__uint_as_float(r0[2 * i]) * scale_log2, __uint_as_float(r0[2 * i + 1]) * scale_log2);
         w[16 + i] = f16x2_sat(__uint_as_float(r1[2 * i]) * scale_log2, __uint_as_float(r1[2 * i + 1]) * scale_log2);
       }
-      // stage this warp's 32 rows locally, then one 4 KB bulk copy into the peer's slot
+      // stage this warp's 32 rows locally, then one 4 KB bulk copy into the peer's slot.
+      // The staging area is this CTA's own receive slot (j + 2) % 4: its last tile, j - 2,
+      // has been consumed (this CTA's softmax finished tile j - 2 before QK^T of tile j
+      // was issued), and the peer fills it with tile j + 2 only after it has received
+      // tile j, i.e. after this copy has read it.
       const int q4 = warp - 4;
-      uint8_t* stg = smem + kOffStg + (j & 1) * kSlotBytes;
-      if (j >= 2) {
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        __syncwarp();
-      }
+      uint8_t* stg = smem + kOffRecv + ((j + 2) & (kSlots - 1)) * kSlotBytes;
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         *reinterpret_cast<uint4*>(stg + h * 128 + ((q ^ (h & 7)) * 16)) =
