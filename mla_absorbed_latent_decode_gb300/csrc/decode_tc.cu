@@ -21,14 +21,14 @@
 //   * QK^T is split along K: each CTA computes a partial score tile
 //       S_r[128 heads x 64 tokens] = Q_r . C_r^T
 //     with Q_r's latent part resident in TMEM (A operand) and its half of the
-//     RoPE query in shared memory.  Four "exchange" warps read S_r
-//     as soon as it lands, scale it to the base-2 softmax domain, round it to
-//     fp16, stage it in a free receive slot of its own and move it into the peer's receive
-//     slot with one 4 KB bulk copy per warp (16 KB per tile each way, 4 slots):
-//     under load, bulk copies move distributed shared memory faster than
-//     16-byte remote stores.  The softmax warps form x = fp16(x_lo) + fp16(x_hi) in the
-//     same order on both CTAs, so both compute bit-identical softmax weights.
-//     fp16 keeps 11 bits of a logit, finer than the bf16 P it feeds.
+//     RoPE query in shared memory.  Four "exchange" warps read S_r as soon as it
+//     lands, scale it to the base-2 softmax domain, round it to fp16, stage it in
+//     a free receive slot of their own CTA and move it into the peer's receive slot
+//     with one 4 KB bulk copy per warp (16 KB per tile each way, 4 slots): under
+//     load, bulk copies move distributed shared memory faster than 16-byte remote
+//     stores.  The softmax warps form x = x_own + fp16(x_peer); fp16 keeps 11 bits
+//     of a logit, finer than the bf16 P it feeds.  The two CTAs' logits agree up to
+//     that rounding, and each normalises its half of the output with its own sum.
 //   * P (bf16) is written into one of two P slots in TMEM and used as the A operand
 //     of O_r[128 x 256] += P . C_r[64 tokens x 256 latent]; the same shared-memory
 //     tile is the B operand, read MN-major.  Each CTA accumulates its half of
@@ -441,19 +441,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->sfree));   // QK^T of tile j + 1 may overwrite S
-        // own partial, rounded exactly as the exchange warps round the copy sent to the peer
+        // own partial in fp32 (the peer receives an fp16 copy)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float2 a = f16x2_to_f32(f16x2_sat(__uint_as_float(r0[2 * i]) * scale_log2,
-                                            __uint_as_float(r0[2 * i + 1]) * scale_log2));
-          float2 c = f16x2_to_f32(f16x2_sat(__uint_as_float(r1[2 * i]) * scale_log2,
-                                            __uint_as_float(r1[2 * i + 1]) * scale_log2));
-          x[2 * i] = a.x; x[2 * i + 1] = a.y; x[32 + 2 * i] = c.x; x[32 + 2 * i + 1] = c.y;
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(r0[i]) * scale_log2;
+          x[32 + i] = __uint_as_float(r1[i]) * scale_log2;
         }
       }
       if (!wait_cluster(&bars->recvfull[slot], (j >> 2) & 1)) { ok = false; break; }
       {
-        // x = x_lo + x_hi in the same order on both CTAs (IEEE addition commutes)
+        // x = x_own + x_peer
         const uint4* rp = reinterpret_cast<const uint4*>(smem + kOffRecv + slot * kSlotBytes + h * 128);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -480,12 +477,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         fence_proxy_async_smem();
       }
 
-      float mt = -INFINITY;
+      if (valid < kPage) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        if (i >= valid) x[i] = -INFINITY;
-        mt = fmaxf(mt, x[i]);
+        for (int i = 0; i < 64; ++i)
+          if (i >= valid) x[i] = -INFINITY;
       }
+      // tile max as a tree (short dependency chains)
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(x[i], x[i + 8]), fmaxf(x[i + 16], x[i + 24]));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], fmaxf(fmaxf(x[i + 32], x[i + 40]), fmaxf(x[i + 48], x[i + 56])));
+      const float mt =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const bool grow = mt > m_used + 8.0f;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // rescale this warp's rows of O once P . C of the previous tile has landed
@@ -508,14 +512,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         m_used = mt;
       }
       uint32_t pk[32];
-      float psum = 0.0f;
+      float ps[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ps[i] = 0.0f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float p0 = ex2_approx(x[2 * i] - m_used), p1 = ex2_approx(x[2 * i + 1] - m_used);
-        psum += p0 + p1;
+        ps[i & 7] += p0 + p1;
         pk[i] = bf16x2_bits(p0, p1);
       }
-      l_sum += psum;
+      l_sum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       // P slot j % 2: its previous user, P . C of tile j - 2, was issued before QK^T of tile j
       // (which this warp has seen complete), so it has finished reading the slot
       tmem_st32(lane_addr + kTmP + 32 * bb, pk);
