@@ -41,7 +41,8 @@
 //     only moves (and O is rescaled in TMEM) when a tile's max exceeds it by more
 //     than 8, so P <= 2^8.
 //   * Warp roles per CTA: warps 0-3 softmax / epilogue (thread = head = TMEM
-//     lane), warps 4-7 score exchange, warp 8 TMA producer, warp 9 MMA issuer.
+//     lane), warps 4-7 score exchange, warp 8 TMA producer, warp 9 issues QK^T,
+//     warp 10 issues P . C.
 //     Every wait is bounded; on a timeout the kernel sets MLA_CHECK_TIMEOUT,
 //     drains and returns.
 #include <cuda.h>
@@ -69,9 +70,10 @@ constexpr int kOffQpe = kOffStages + kStages * kStageBytes;
 constexpr int kOffRecv = kOffQpe + kQpeBytes;
 constexpr int kOffBars = kOffRecv + kSlots * kSlotBytes;
 constexpr int kSmemBytes = kOffBars + 1024 + 1024;    // + barriers / flags, + alignment slack
-constexpr int kThreads = 320;                          // 4 softmax, 4 exchange, producer, MMA warps
+constexpr int kThreads = 352;                          // 4 softmax, 4 exchange, producer, 2 MMA warps
 constexpr int kWarpProducer = 8;
-constexpr int kWarpMma = 9;
+constexpr int kWarpMma = 9;                            // QK^T issuer (allocates TMEM)
+constexpr int kWarpPv = 10;                            // P . C issuer
 
 // TMEM column map
 constexpr uint32_t kTmO = 0;
@@ -87,10 +89,10 @@ struct Bars {                               // mbarriers (8 bytes each) and flag
   uint64_t sfull;                           // partial scores S_r(j) in TMEM        (MMA commit)
   uint64_t sfree;                           // S_r(j) loaded by softmax + exchange  (8 warps)
   uint64_t pfull[2];                        // P(j) written into P slot j % 2       (4 warps)
-  uint64_t odone;                           // one phase per P . C tile             (MMA commit)
+  uint64_t pdone[2];                        // P . C of a tile in P slot b done     (MMA commit)
   uint64_t ofinal;                          // single phase: the last P . C landed  (MMA commit)
   uint64_t recvfull[kSlots];                // peer's partial scores arrived        (1 + 16 KB tx)
-  uint64_t drain;
+  uint64_t drain[2];                        // every MMA of the QK^T / P . C issuer done
   uint32_t tmem_base;
   int abort;
 };
@@ -180,9 +182,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     mbar_init(smem_u32(&bars->sfree), 8);
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->pfull[i]), 4);
     for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&bars->recvfull[i]), 1);
-    mbar_init(smem_u32(&bars->odone), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->pdone[i]), 1);
     mbar_init(smem_u32(&bars->ofinal), 1);
-    mbar_init(smem_u32(&bars->drain), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->drain[i]), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -269,52 +271,61 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       }
     }
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK^T issuer
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 64, false, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
-      const uint32_t qpe = sbase + kOffQpe;
+      const uint64_t qpe_desc = sdesc_sw64(sbase + kOffQpe, 16, 512);
       bool ok = true;
-      for (int j = 0; j <= n_tiles && ok; ++j) {
-        if (j < n_tiles) {
-          const int s = j % kStages;
-          // the tile has landed (and been converted), and S(j - 1) has been loaded by both readers
-          if (!mbar_wait(smem_u32(kFp8 ? &bars->conv[s] : &bars->full[s]), (j / kStages) & 1, abort_flag) ||
-              (j > 0 && !mbar_wait(smem_u32(&bars->sfree), (j - 1) & 1, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t st = stage0 + s * kStageBytes;
-          const uint32_t d = tmem + kTmS;
-#pragma unroll
-          for (int k = 0; k < 16; ++k)
-            mma_ts(d, tmem + kTmQ + 8 * k, sdesc_sw128(st + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024),
-                   idesc_qk, k > 0);
-#pragma unroll
-          for (int k = 0; k < 2; ++k)
-            mma_ss(d, sdesc_sw64(qpe + 32 * k, 16, 512), sdesc_sw64(st + 4 * kChunkBytes + 32 * k, 16, 512), idesc_qk,
-                   1);
-          mma_commit(smem_u32(&bars->sfull));
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % kStages;
+        // the tile has landed (and been converted), and S(j - 1) has been loaded by both readers
+        if (!mbar_wait(smem_u32(kFp8 ? &bars->conv[s] : &bars->full[s]), (j / kStages) & 1, abort_flag) ||
+            (j > 0 && !mbar_wait(smem_u32(&bars->sfree), (j - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
         }
-        if (j >= 1) {
-          const int jj = j - 1, s = jj % kStages, bb = jj & 1;
-          if (!mbar_wait(smem_u32(&bars->pfull[bb]), (jj >> 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t st = stage0 + s * kStageBytes;
+        tc_fence_after();
+        const uint32_t st = stage0 + s * kStageBytes;
+        const uint64_t lat_desc = sdesc_sw128(st, 16, 1024), rope_desc = sdesc_sw64(st + 4 * kChunkBytes, 16, 512);
+        const uint32_t d = tmem + kTmS;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + kTmO, tmem + kTmP + 32 * bb + 8 * k, sdesc_sw128(st + 2048 * k, kChunkBytes, 1024),
-                   idesc_pv, (jj > 0 || k > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&bars->empty[s]));
-          mma_commit(smem_u32(&bars->odone));
-          if (jj == n_tiles - 1) mma_commit(smem_u32(&bars->ofinal));
-        }
+        for (int k = 0; k < 16; ++k)         // latent chunk k / 4, 32-byte step k % 4 inside the 128-byte row
+          mma_ts(d, tmem + kTmQ + 8 * k, lat_desc + (uint64_t)((((k >> 2) * kChunkBytes) + (k & 3) * 32) >> 4),
+                 idesc_qk, k > 0);
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          mma_ss(d, qpe_desc + (uint64_t)(2 * k), rope_desc + (uint64_t)(2 * k), idesc_qk, 1);
+        mma_commit(smem_u32(&bars->sfull));
       }
       if (!ok) fail_timeout(bars, check);
-      mma_commit(smem_u32(&bars->drain));      // arrives once every MMA issued above has finished
+      mma_commit(smem_u32(&bars->drain[0]));   // arrives once every MMA issued above has finished
       volatile int never = 0;
-      mbar_wait(smem_u32(&bars->drain), 0, &never);
+      mbar_wait(smem_u32(&bars->drain[0]), 0, &never);
+    }
+  } else if (warp == kWarpPv) {
+    // ------------------------------------------------------------ P . C issuer (tile order)
+    // A separate issuer: a P . C never waits behind the issue of a QK^T (they use disjoint
+    // TMEM: P slots and O, against the score buffer).
+    if (lane == 0) {
+      const uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
+      bool ok = true;
+      for (int jj = 0; jj < n_tiles; ++jj) {
+        const int s = jj % kStages, bb = jj & 1;
+        if (!mbar_wait(smem_u32(&bars->pfull[bb]), (jj >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t c_desc = sdesc_sw128(stage0 + s * kStageBytes, kChunkBytes, 1024);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ts(tmem + kTmO, tmem + kTmP + 32 * bb + 8 * k, c_desc + (uint64_t)(128 * k), idesc_pv,
+                 (jj > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bars->empty[s]));
+        mma_commit(smem_u32(&bars->pdone[bb]));
+        if (jj == n_tiles - 1) mma_commit(smem_u32(&bars->ofinal));
+      }
+      if (!ok) fail_timeout(bars, check);
+      mma_commit(smem_u32(&bars->drain[1]));
+      volatile int never = 0;
+      mbar_wait(smem_u32(&bars->drain[1]), 0, &never);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ exchange: S_r(j) -> peer
@@ -493,7 +504,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       const bool grow = mt > m_used + 8.0f;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // rescale this warp's rows of O once P . C of the previous tile has landed
-        if (!wait_cta(&bars->odone, (j - 1) & 1)) { ok = false; break; }
+        if (!wait_cta(&bars->pdone[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const float alpha = grow ? ex2_approx(m_used - mt) : 1.0f;
 #pragma unroll 1
@@ -522,8 +533,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         pk[i] = bf16x2_bits(p0, p1);
       }
       l_sum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      // P slot j % 2: its previous user, P . C of tile j - 2, was issued before QK^T of tile j
-      // (which this warp has seen complete), so it has finished reading the slot
+      // P slot j % 2 once its previous user, P . C of tile j - 2, has finished reading it
+      if (j >= 2 && !wait_cta(&bars->pdone[bb], ((j - 2) >> 1) & 1)) { ok = false; break; }
       tmem_st32(lane_addr + kTmP + 32 * bb, pk);
       tmem_st_wait();
       tc_fence_before();
@@ -532,8 +543,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     }
     if (!ok) fail_timeout(bars, check);
     // ---- epilogue: this CTA's 256 latent columns of every head
-    // (odone cannot be used here: when the last tile's softmax ends, P . C of the tile
-    // before it may still be pending, and a parity wait two phases behind is ambiguous)
+    // (a single-phase barrier: a parity wait on pdone here could be two phases behind)
     if (ok && n_tiles > 0 && wait_cta(&bars->ofinal, 0)) {
       tc_fence_after();
       const float inv = out_scale / l_sum;
