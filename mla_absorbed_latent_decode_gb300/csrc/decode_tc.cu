@@ -112,6 +112,25 @@ __device__ __forceinline__ float2 f16x2_to_f32(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
+// three-input maximum (one instruction on sm_100 and later)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// maximum of 64 values in 32 three-input steps, as a tree of depth 5
+__device__ __forceinline__ float max64(const float2 (&x2)[32]) {
+  const float* v = reinterpret_cast<const float*>(x2);
+  float a[22], b[8];
+#pragma unroll
+  for (int i = 0; i < 21; ++i) a[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  a[21] = v[63];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) b[i] = max3f(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  b[7] = a[21];
+  return max3f(max3f(b[0], b[1], b[2]), max3f(b[3], b[4], b[5]), fmaxf(b[6], b[7]));
+}
+
 __device__ __forceinline__ void fail_timeout(Bars* bars, unsigned* check) {
   if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
 }
@@ -397,10 +416,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->sfree));
       uint32_t w[32];
+      const float2 sc2 = make_float2(scale_log2, scale_log2), zero2 = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        w[i] = f16x2_sat(__uint_as_float(r0[2 * i]) * scale_log2, __uint_as_float(r0[2 * i + 1]) * scale_log2);
-        w[16 + i] = f16x2_sat(__uint_as_float(r1[2 * i]) * scale_log2, __uint_as_float(r1[2 * i + 1]) * scale_log2);
+        const float2 a = __ffma2_rn(make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])), sc2, zero2);
+        const float2 c = __ffma2_rn(make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), sc2, zero2);
+        w[i] = f16x2_sat(a.x, a.y);
+        w[16 + i] = f16x2_sat(c.x, c.y);
       }
       // stage this warp's 32 rows locally, then one 4 KB bulk copy into the peer's slot.
       // The staging area is this CTA's own receive slot (j + 2) % 4: its last tile, j - 2,
@@ -445,23 +467,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       armed = j + 1;
       if (!wait_cta(&bars->sfull, j & 1)) { ok = false; break; }
       tc_fence_after();
-      float x[64];
+      // x2[i] = scores 2i, 2i + 1 in the log2 domain, as pairs for the packed fp32 ops
+      float2 x2[32];
       {
         uint32_t r0[32], r1[32];
-        load_scores(lane_addr, r0, r1);
+        load_scores(lane_addr, r0, r1);   // own partial, kept in fp32 (the peer gets fp16)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->sfree));   // QK^T of tile j + 1 may overwrite S
-        // own partial in fp32 (the peer receives an fp16 copy)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] = __uint_as_float(r0[i]) * scale_log2;
-          x[32 + i] = __uint_as_float(r1[i]) * scale_log2;
-        }
-      }
-      if (!wait_cluster(&bars->recvfull[slot], (j >> 2) & 1)) { ok = false; break; }
-      {
-        // x = x_own + x_peer
+        if (!wait_cluster(&bars->recvfull[slot], (j >> 2) & 1)) { ok = false; break; }
+        // x = x_own * scale_log2 + x_peer
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
         const uint4* rp = reinterpret_cast<const uint4*>(smem + kOffRecv + slot * kSlotBytes + h * 128);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -469,9 +485,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
           const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float2 f = f16x2_to_f32(ww[k]);
-            x[8 * q + 2 * k] += f.x;
-            x[8 * q + 2 * k + 1] += f.y;
+            const int i = 4 * q + k;
+            const uint32_t* r = i < 16 ? r0 + 2 * i : r1 + 2 * (i - 16);
+            x2[i] = __ffma2_rn(make_float2(__uint_as_float(r[0]), __uint_as_float(r[1])), sc2, f16x2_to_f32(ww[k]));
           }
         }
       }
@@ -490,17 +506,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
 
       if (valid < kPage) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i >= valid) x[i] = -INFINITY;
+        for (int i = 0; i < 32; ++i) {
+          if (2 * i >= valid) x2[i].x = -INFINITY;
+          if (2 * i + 1 >= valid) x2[i].y = -INFINITY;
+        }
       }
-      // tile max as a tree (short dependency chains)
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(x[i], x[i + 8]), fmaxf(x[i + 16], x[i + 24]));
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], fmaxf(fmaxf(x[i + 32], x[i + 40]), fmaxf(x[i + 48], x[i + 56])));
-      const float mt =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float mt = max64(x2);
       const bool grow = mt > m_used + 8.0f;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // rescale this warp's rows of O once P . C of the previous tile has landed
@@ -523,16 +534,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         m_used = mt;
       }
       uint32_t pk[32];
-      float ps[8];
+      float2 ps[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ps[i] = 0.0f;
+      for (int i = 0; i < 4; ++i) ps[i] = make_float2(0.0f, 0.0f);
+      const float2 negm2 = make_float2(-m_used, -m_used);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float p0 = ex2_approx(x[2 * i] - m_used), p1 = ex2_approx(x[2 * i + 1] - m_used);
-        ps[i & 7] += p0 + p1;
-        pk[i] = bf16x2_bits(p0, p1);
+        const float2 d = __fadd2_rn(x2[i], negm2);
+        const float2 p = make_float2(ex2_approx(d.x), ex2_approx(d.y));
+        ps[i & 3] = __fadd2_rn(ps[i & 3], p);
+        pk[i] = bf16x2_bits(p.x, p.y);
       }
-      l_sum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      {
+        const float2 s2 = __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3]));
+        l_sum += s2.x + s2.y;
+      }
       // P slot j % 2 once its previous user, P . C of tile j - 2, has finished reading it
       if (j >= 2 && !wait_cta(&bars->pdone[bb], ((j - 2) >> 1) & 1)) { ok = false; break; }
       tmem_st32(lane_addr + kTmP + 32 * bb, pk);
