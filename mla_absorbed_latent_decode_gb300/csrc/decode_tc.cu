@@ -21,28 +21,33 @@
 //   * QK^T is split along K: each CTA computes a partial score tile
 //       S_r[128 heads x 64 tokens] = Q_r . C_r^T
 //     with Q_r's latent part resident in TMEM (A operand) and its half of the
-//     RoPE query in shared memory.  Four "exchange" warps read S_r as soon as it
-//     lands, scale it to the base-2 softmax domain, round it to fp16, stage it in
-//     a free receive slot of their own CTA and move it into the peer's receive slot
-//     with one 4 KB bulk copy per warp (16 KB per tile each way, 4 slots): under
-//     load, bulk copies move distributed shared memory faster than 16-byte remote
-//     stores.  The softmax warps form x = x_own + fp16(x_peer); fp16 keeps 11 bits
-//     of a logit, finer than the bf16 P it feeds.  The two CTAs' logits agree up to
-//     that rounding, and each normalises its half of the output with its own sum.
+//     RoPE query in shared memory.  Two groups of four warps take the tiles in
+//     turn (group j % 2 takes tile j; thread = head = TMEM lane).  A group reads
+//     S_r as soon as it lands, scales it to the base-2 softmax domain, rounds it
+//     to fp16, stages it in a free receive slot of its own CTA and moves it into
+//     the peer's receive slot with one 4 KB bulk copy per warp (16 KB per tile
+//     each way, 4 slots): under load, bulk copies move distributed shared memory
+//     faster than 16-byte remote stores.  It then forms x = x_own + fp16(x_peer);
+//     fp16 keeps 11 bits of a logit, finer than the bf16 P it feeds.  The two CTAs'
+//     logits agree up to that rounding, and each normalises its half of the output
+//     with its own sum.  One tile's chain (read, send, wait for the peer, softmax,
+//     write P) is longer than the QK^T that feeds it; two groups run two chains at
+//     once, handing the running max from tile to tile through shared memory and
+//     keeping separate sums, reconciled at the end.
 //   * P (bf16) is written into one of two P slots in TMEM and used as the A operand
 //     of O_r[128 x 256] += P . C_r[64 tokens x 256 latent]; the same shared-memory
 //     tile is the B operand, read MN-major.  Each CTA accumulates its half of
 //     the latent output in TMEM (256 columns).
 //   * TMEM per CTA (512 columns): O_r [0,256), Q_r [256,384), S [384,448), P slots
-//     [448,480) and [480,512).  The score buffer is free as soon as the softmax and
-//     exchange warps have loaded it, so QK^T of tile j+1 is issued when tile j's
+//     [448,480) and [480,512).  The score buffer is free as soon as the tile's
+//     group has loaded it, so QK^T of tile j+1 is issued when tile j's
 //     softmax starts, not when it ends; P(j) keeps its own slot until P . C reads it.
 //   * Online softmax in the base-2 domain with a lazy rescale: the running max
 //     only moves (and O is rescaled in TMEM) when a tile's max exceeds it by more
 //     than 8, so P <= 2^8.
-//   * Warp roles per CTA: warps 0-3 softmax / epilogue (thread = head = TMEM
-//     lane), warps 4-7 score exchange, warp 8 TMA producer, warp 9 issues QK^T,
-//     warp 10 issues P . C.
+//   * Warp roles per CTA: warps 0-3 and 4-7 the two tile groups (score exchange,
+//     softmax, epilogue), warp 8 TMA producer, warp 9 issues QK^T, warp 10 issues
+//     P . C; with an FP8 cache, warps 11-14 convert each tile to bf16 in place.
 //     Every wait is bounded; on a timeout the kernel sets MLA_CHECK_TIMEOUT,
 //     drains and returns.
 #include <cuda.h>
@@ -69,11 +74,15 @@ constexpr int kOffStages = 0;
 constexpr int kOffQpe = kOffStages + kStages * kStageBytes;
 constexpr int kOffRecv = kOffQpe + kQpeBytes;
 constexpr int kOffBars = kOffRecv + kSlots * kSlotBytes;
-constexpr int kSmemBytes = kOffBars + 1024 + 1024;    // + barriers / flags, + alignment slack
-constexpr int kThreads = 352;                          // 4 softmax, 4 exchange, producer, 2 MMA warps
+constexpr int kOffXchg = kOffBars + 1024;             // running maxima / final sums of the two tile groups
+constexpr int kXchgBytes = 3 * 2 * kMaxHeads * 4;
+constexpr int kSmemBytes = kOffXchg + kXchgBytes + 1024;   // + alignment slack
+constexpr int kThreads = 352;                          // 2 tile groups of 4 warps, producer, 2 MMA warps
+constexpr int kThreadsFp8 = 480;                       // + 4 FP8 conversion warps
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;                            // QK^T issuer (allocates TMEM)
 constexpr int kWarpPv = 10;                            // P . C issuer
+constexpr int kWarpConv = 11;                          // FP8 cache: warps 11-14 convert tiles
 
 // TMEM column map
 constexpr uint32_t kTmO = 0;
@@ -83,11 +92,13 @@ constexpr uint32_t kTmP = 448;             // P slot b (64 bf16 per lane) at kTm
 
 struct Bars {                               // mbarriers (8 bytes each) and flags
   uint64_t full[kStages];                   // TMA tile landed                      (producer, tx)
-  uint64_t conv[kStages];                   // FP8 cache: tile converted to bf16    (4 exchange warps)
-  uint64_t cread[kStages];                  // FP8 cache: every code of the tile read (4 exchange warps)
+  uint64_t conv[kStages];                   // FP8 cache: tile converted to bf16    (4 conversion warps)
+  uint64_t cread[kStages];                  // FP8 cache: every code of the tile read (4 conversion warps)
   uint64_t empty[kStages];                  // tile consumed by P . C               (MMA commit)
-  uint64_t sfull;                           // partial scores S_r(j) in TMEM        (MMA commit)
-  uint64_t sfree;                           // S_r(j) loaded by softmax + exchange  (8 warps)
+  uint64_t sfull[2];                        // S_r(j) in TMEM, tile group j % 2     (MMA commit)
+  uint64_t sfree[2];                        // S_r(j) loaded by its tile group      (4 warps)
+  uint64_t mready[2];                       // a group's running max published     (4 warps)
+  uint64_t efin;                            // single phase: both groups' sums out  (8 warps)
   uint64_t pfull[2];                        // P(j) written into P slot j % 2       (4 warps)
   uint64_t pdone[2];                        // P . C of a tile in P slot b done     (MMA commit)
   uint64_t ofinal;                          // single phase: the last P . C landed  (MMA commit)
@@ -135,13 +146,6 @@ __device__ __forceinline__ void fail_timeout(Bars* bars, unsigned* check) {
   if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
 }
 
-// Load this thread's 64 partial scores (two x32 loads, one wait).
-__device__ __forceinline__ void load_scores(uint32_t lane_addr, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
-  tmem_ld32(lane_addr + kTmS, r0);
-  tmem_ld32(lane_addr + kTmS + 32, r1);
-  tmem_ld_wait();
-}
-
 // FP8 cache: e4m3 -> bf16, exact (every e4m3 value is a normal fp16 or zero, and a bf16).  Two
 // e4m3 codes -> fp16 pair by cvt; fp16 -> bf16 by moving the exponent bias from 15 to 127 and
 // dropping three mantissa bits that are zero for these values.
@@ -160,11 +164,11 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
 }
 
 // kFp8: the cache holds e4m3 codes.  The producer TMA-loads each 64 x 64 code box into the
-// upper half of the 8 KB slot its bf16 chunk will occupy; the exchange warps convert the
+// upper half of the 8 KB slot its bf16 chunk will occupy; the conversion warps convert the
 // tile in place (all reads, a barrier, then all writes) before QK^T may use it.  The tensor
 // scale is folded into the softmax scale and the output scale by the launcher.
 template <bool kFp8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_rope,
                  const int32_t* __restrict__ ctx_len, int n_h,
                  const int32_t* __restrict__ block_table, int bt_stride, int num_pages, float scale_log2,
@@ -197,9 +201,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       mbar_init(smem_u32(&bars->conv[s]), 4);
       mbar_init(smem_u32(&bars->cread[s]), 4);
     }
-    mbar_init(smem_u32(&bars->sfull), 1);
-    mbar_init(smem_u32(&bars->sfree), 8);
-    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->pfull[i]), 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->sfull[i]), 1);
+      mbar_init(smem_u32(&bars->sfree[i]), 4);
+      mbar_init(smem_u32(&bars->mready[i]), 4);
+      mbar_init(smem_u32(&bars->pfull[i]), 4);
+    }
+    mbar_init(smem_u32(&bars->efin), 8);
     for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&bars->recvfull[i]), 1);
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->pdone[i]), 1);
     mbar_init(smem_u32(&bars->ofinal), 1);
@@ -297,9 +305,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       bool ok = true;
       for (int j = 0; j < n_tiles; ++j) {
         const int s = j % kStages;
-        // the tile has landed (and been converted), and S(j - 1) has been loaded by both readers
+        // the tile has landed (and been converted), and S(j - 1) has been loaded by its group
         if (!mbar_wait(smem_u32(kFp8 ? &bars->conv[s] : &bars->full[s]), (j / kStages) & 1, abort_flag) ||
-            (j > 0 && !mbar_wait(smem_u32(&bars->sfree), (j - 1) & 1, abort_flag))) {
+            (j > 0 && !mbar_wait(smem_u32(&bars->sfree[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
@@ -314,7 +322,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
 #pragma unroll
         for (int k = 0; k < 2; ++k)
           mma_ss(d, qpe_desc + (uint64_t)(2 * k), rope_desc + (uint64_t)(2 * k), idesc_qk, 1);
-        mma_commit(smem_u32(&bars->sfull));
+        mma_commit(smem_u32(&bars->sfull[j & 1]));
       }
       if (!ok) fail_timeout(bars, check);
       mma_commit(smem_u32(&bars->drain[0]));   // arrives once every MMA issued above has finished
@@ -346,111 +354,76 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       volatile int never = 0;
       mbar_wait(smem_u32(&bars->drain[1]), 0, &never);
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ exchange: S_r(j) -> peer
-    // As soon as QK^T of tile j lands, read this CTA's partial scores, scale them to the
-    // base-2 softmax domain, round to fp16 and store them into the peer's receive slot
-    // j % 4.  No "slot free" handshake is needed: the peer sends tile j only after its
-    // QK^T of tile j, which it issues only after its softmax has started tile j - 1, hence
-    // finished tile j - 2, which needed this CTA's tile j - 2, sent only after this CTA's
-    // QK^T of tile j - 2, issued only after this CTA's softmax had started tile j - 3,
-    // hence finished tile j - 4 -- the last user of slot j % 4.
-    const int h = tid - 128;
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
-    const uint32_t recv_peer = map_to_rank(sbase + kOffRecv, peer);
-    // FP8 cache: convert tile t in place, thread = (row h / 2, 32-column half h % 2) of every chunk
-    // (every wait bounded: a warp that gives up returns false, and the kernel aborts)
-    auto convert = [&](int t) {
-      const int s = t % kStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (t / kStages) & 1, abort_flag))) return false;
-      uint8_t* st = smem + kOffStages + s * kStageBytes;
+  } else if (warp >= kWarpConv) {
+    // ------------------------------------------------------------ FP8 cache: e4m3 -> bf16 in place
+    // (launched only with an FP8 cache) thread = (row h / 2, 32-column half h % 2) of every
+    // chunk of a tile; every code of the tile is read, by all four warps, before any is
+    // overwritten.  Every wait is bounded: a warp that gives up aborts the kernel.
+    if constexpr (kFp8) {
+      const int h = tid - kWarpConv * 32;
       const int r = h >> 1, hf = h & 1;
-      uint4 v[9];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4* src = reinterpret_cast<const uint4*>(st + c * kChunkBytes + kChunkBytes / 2 + r * 64 + hf * 32);
-        v[2 * c] = src[0];
-        v[2 * c + 1] = src[1];
-      }
-      v[8] = *reinterpret_cast<const uint4*>(st + 4 * kChunkBytes + kRopeBytes / 2 + r * 32 + hf * 16);
-      // every code of the tile read (by all four warps) before any is overwritten
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->cread[s]));
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->cread[s]), (t / kStages) & 1, abort_flag))) return false;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {           // latent: 128-byte rows, 128-byte swizzle
-        uint8_t* row = st + c * kChunkBytes + r * 128;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {         // 16-byte chunk 4 hf + i of the row: 8 codes
-          const uint4 w = v[2 * c + (i >> 1)];
-          const uint2 lo = e4m3x4_to_bf16x4((i & 1) ? w.z : w.x), hi = e4m3x4_to_bf16x4((i & 1) ? w.w : w.y);
-          *reinterpret_cast<uint4*>(row + (((4 * hf + i) ^ (r & 7)) * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+      bool ok = true;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % kStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (t / kStages) & 1, abort_flag))) {
+          ok = false;
+          break;
         }
-      }
-      {                                       // RoPE key: 64-byte rows, 64-byte swizzle
-        uint8_t* row = st + 4 * kChunkBytes + r * 64;
+        uint8_t* st = smem + kOffStages + s * kStageBytes;
+        uint4 v[9];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {         // 16-byte chunk 2 hf + i of the row: 8 codes
-          const uint32_t a = i ? v[8].z : v[8].x, c2 = i ? v[8].w : v[8].y;
-          const uint2 lo = e4m3x4_to_bf16x4(a), hi = e4m3x4_to_bf16x4(c2);
-          *reinterpret_cast<uint4*>(row + (((2 * hf + i) ^ ((r >> 1) & 3)) * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        for (int c = 0; c < 4; ++c) {
+          const uint4* src = reinterpret_cast<const uint4*>(st + c * kChunkBytes + kChunkBytes / 2 + r * 64 + hf * 32);
+          v[2 * c] = src[0];
+          v[2 * c + 1] = src[1];
         }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->conv[s]));
-      return true;
-    };
-    if (kFp8 && n_tiles > 0 && !convert(0)) fail_timeout(bars, check);
-    for (int j = 0; j < n_tiles; ++j) {
-      const int slot = j & (kSlots - 1);
-      if (kFp8 && j + 1 < n_tiles && !convert(j + 1)) {
-        fail_timeout(bars, check);
-        break;
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sfull), j & 1, abort_flag))) break;
-      tc_fence_after();
-      uint32_t r0[32], r1[32];
-      load_scores(lane_addr, r0, r1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->sfree));
-      uint32_t w[32];
-      const float2 sc2 = make_float2(scale_log2, scale_log2), zero2 = make_float2(0.0f, 0.0f);
+        v[8] = *reinterpret_cast<const uint4*>(st + 4 * kChunkBytes + kRopeBytes / 2 + r * 32 + hf * 16);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->cread[s]));
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->cread[s]), (t / kStages) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float2 a = __ffma2_rn(make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])), sc2, zero2);
-        const float2 c = __ffma2_rn(make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), sc2, zero2);
-        w[i] = f16x2_sat(a.x, a.y);
-        w[16 + i] = f16x2_sat(c.x, c.y);
-      }
-      // stage this warp's 32 rows locally, then one 4 KB bulk copy into the peer's slot.
-      // The staging area is this CTA's own receive slot (j + 2) % 4: its last tile, j - 2,
-      // has been consumed (this CTA's softmax finished tile j - 2 before QK^T of tile j
-      // was issued), and the peer fills it with tile j + 2 only after it has received
-      // tile j, i.e. after this copy has read it.
-      const int q4 = warp - 4;
-      uint8_t* stg = smem + kOffRecv + ((j + 2) & (kSlots - 1)) * kSlotBytes;
+        for (int c = 0; c < 4; ++c) {           // latent: 128-byte rows, 128-byte swizzle
+          uint8_t* row = st + c * kChunkBytes + r * 128;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(stg + h * 128 + ((q ^ (h & 7)) * 16)) =
-            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const uint32_t dst = recv_peer + slot * kSlotBytes + q4 * 32 * 128;
-        const uint32_t peer_bar = map_to_rank(smem_u32(&bars->recvfull[slot]), peer);
-        asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(dst), "r"(smem_u32(stg + q4 * 32 * 128)), "r"(32 * 128), "r"(peer_bar) : "memory");
-        bulk_commit_group();
+          for (int i = 0; i < 4; ++i) {         // 16-byte chunk 4 hf + i of the row: 8 codes
+            const uint4 w = v[2 * c + (i >> 1)];
+            const uint2 lo = e4m3x4_to_bf16x4((i & 1) ? w.z : w.x), hi = e4m3x4_to_bf16x4((i & 1) ? w.w : w.y);
+            *reinterpret_cast<uint4*>(row + (((4 * hf + i) ^ (r & 7)) * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          }
+        }
+        {                                       // RoPE key: 64-byte rows, 64-byte swizzle
+          uint8_t* row = st + 4 * kChunkBytes + r * 64;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {         // 16-byte chunk 2 hf + i of the row: 8 codes
+            const uint32_t a = i ? v[8].z : v[8].x, c2 = i ? v[8].w : v[8].y;
+            const uint2 lo = e4m3x4_to_bf16x4(a), hi = e4m3x4_to_bf16x4(c2);
+            *reinterpret_cast<uint4*>(row + (((2 * hf + i) ^ ((r >> 1) & 3)) * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->conv[s]));
       }
+      if (!ok) fail_timeout(bars, check);
     }
-    if (lane == 0) bulk_wait_all();        // every copy landed before the CTA may exit
   } else {
-    // ------------------------------------------------------------ softmax + epilogue (thread = head)
-    const int h = tid;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    float m_used = -INFINITY, l_sum = 0.0f;
+    // ------------------------------------------------------------ tile groups: exchange, softmax, epilogue
+    // Group g = warp / 4 takes the tiles j = g (mod 2); warp w holds heads 32 (w % 4) .. + 31
+    // (thread = head = TMEM lane).  A tile's chain -- read S_r, send the fp16 copy, wait for the
+    // peer's, softmax, write P -- is longer than the QK^T that feeds it, so two groups run
+    // two tiles' chains at once.  The running max is handed from tile to tile through shared
+    // memory; each group keeps its own sum, and the two are reconciled in the epilogue.
+    const int g = warp >> 2, q4 = warp & 3;
+    const int h = q4 * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
+    const uint32_t recv_peer = map_to_rank(sbase + kOffRecv, peer);
+    float* m_pub = reinterpret_cast<float*>(smem + kOffXchg);    // [group][head]: running max after its last tile
+    float* fin_x = m_pub + 2 * kMaxHeads;                         // [group][2][head]: final (max, sum)
+    const float2 sc2 = make_float2(scale_log2, scale_log2), zero2 = make_float2(0.0f, 0.0f);
+    float m_g = -INFINITY, l_g = 0.0f;        // this group's sum, relative to 2^m_g
     bool ok = true;
     int armed = 0;
     // waits are made warp-uniform: tcgen05.ld / st below are .sync.aligned
@@ -460,51 +433,77 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     auto wait_cluster = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait<true>(smem_u32(bar), parity, abort_flag));
     };
-    for (int j = 0; j < n_tiles; ++j) {
-      const int bb = j & 1, slot = j & (kSlots - 1);
+    for (int j = g; j < n_tiles; j += 2) {
+      const int k = j >> 1, slot = j & (kSlots - 1);
       const int valid = min(kPage, t_end - (unit.page_begin + j) * kPage);
-      if (tid == 0) mbar_arrive_expect_tx(smem_u32(&bars->recvfull[slot]), (uint32_t)kSlotBytes);
+      // this group waited for slot j % 4's previous phase (tile j - 4) itself
+      if (lane == 0 && q4 == 0) mbar_arrive_expect_tx(smem_u32(&bars->recvfull[slot]), (uint32_t)kSlotBytes);
       armed = j + 1;
-      if (!wait_cta(&bars->sfull, j & 1)) { ok = false; break; }
+      if (!wait_cta(&bars->sfull[g], k & 1)) { ok = false; break; }
       tc_fence_after();
       // x2[i] = scores 2i, 2i + 1 in the log2 domain, as pairs for the packed fp32 ops
       float2 x2[32];
       {
         uint32_t r0[32], r1[32];
-        load_scores(lane_addr, r0, r1);   // own partial, kept in fp32 (the peer gets fp16)
+        tmem_ld32(lane_addr + kTmS, r0);      // own partial, kept in fp32 (the peer gets fp16)
+        tmem_ld32(lane_addr + kTmS + 32, r1);
+        tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->sfree));   // QK^T of tile j + 1 may overwrite S
-        if (!wait_cluster(&bars->recvfull[slot], (j >> 2) & 1)) { ok = false; break; }
-        // x = x_own * scale_log2 + x_peer
-        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        if (lane == 0) mbar_arrive(smem_u32(&bars->sfree[g]));   // QK^T of tile j + 1 may overwrite S
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          x2[i] = __ffma2_rn(make_float2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1])), sc2, zero2);
+          x2[16 + i] = __ffma2_rn(make_float2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])), sc2, zero2);
+        }
+      }
+      {
+        // fp16 copy for the peer, staged in this CTA's own receive slot (j + 2) % 4 and moved
+        // by one 4 KB bulk copy per warp into the peer's slot j % 4.  The staging rows last
+        // held tile j - 2 for this same warp, which has consumed them; the peer refills them
+        // with tile j + 2 only after its group g has finished tile j, which needed every copy
+        // of this tile, so after the copies have read them.  The peer's slot j % 4 needs no
+        // "free" handshake either: this CTA sends tile j after its group g finished tile
+        // j - 2, which needed the peer's tile j - 2 copies, sent after the peer's group g
+        // finished tile j - 4, the last user of the slot.
+        uint8_t* stg = smem + kOffRecv + ((j + 2) & (kSlots - 1)) * kSlotBytes;
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq)
+          *reinterpret_cast<uint4*>(stg + h * 128 + ((qq ^ (h & 7)) * 16)) =
+              make_uint4(f16x2_sat(x2[4 * qq].x, x2[4 * qq].y), f16x2_sat(x2[4 * qq + 1].x, x2[4 * qq + 1].y),
+                         f16x2_sat(x2[4 * qq + 2].x, x2[4 * qq + 2].y), f16x2_sat(x2[4 * qq + 3].x, x2[4 * qq + 3].y));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t peer_bar = map_to_rank(smem_u32(&bars->recvfull[slot]), peer);
+          asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                       ::"r"(recv_peer + slot * kSlotBytes + q4 * 32 * 128), "r"(smem_u32(stg + q4 * 32 * 128)),
+                       "r"(32 * 128), "r"(peer_bar) : "memory");
+          bulk_commit_group();
+        }
+      }
+      if (!wait_cluster(&bars->recvfull[slot], (j >> 2) & 1)) { ok = false; break; }
+      {
+        // x = x_own + x_peer
         const uint4* rp = reinterpret_cast<const uint4*>(smem + kOffRecv + slot * kSlotBytes + h * 128);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 v = rp[q ^ (h & 7)];
+        for (int qq = 0; qq < 8; ++qq) {
+          const uint4 v = rp[qq ^ (h & 7)];
           const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int i = 4 * q + k;
-            const uint32_t* r = i < 16 ? r0 + 2 * i : r1 + 2 * (i - 16);
-            x2[i] = __ffma2_rn(make_float2(__uint_as_float(r[0]), __uint_as_float(r[1])), sc2, f16x2_to_f32(ww[k]));
-          }
+          for (int kk = 0; kk < 4; ++kk) x2[4 * qq + kk] = __fadd2_rn(x2[4 * qq + kk], f16x2_to_f32(ww[kk]));
         }
       }
-
-      // a partial last page: rows past the context hold stale data; zero this CTA's latent
-      // rows there so P = 0 meets finite values in P . C
       if (valid < kPage) {
+        // a partial last page: rows past the context hold stale data; zero this CTA's latent
+        // rows there so P = 0 meets finite values in P . C
         uint8_t* st = smem + kOffStages + (j % kStages) * kStageBytes;
         const int rows = kPage - valid;
-        for (int i = tid; i < 4 * rows * 8; i += 128) {
-          const int c = i / (rows * 8), rr = valid + (i / 8) % rows, k = i % 8;
-          *reinterpret_cast<uint4*>(st + c * kChunkBytes + rr * 128 + k * 16) = make_uint4(0, 0, 0, 0);
+        for (int i = h; i < 4 * rows * 8; i += 128) {
+          const int cc = i / (rows * 8), rr = valid + (i / 8) % rows, kk = i % 8;
+          *reinterpret_cast<uint4*>(st + cc * kChunkBytes + rr * 128 + kk * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
-      }
-
-      if (valid < kPage) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           if (2 * i >= valid) x2[i].x = -INFINITY;
@@ -512,32 +511,53 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         }
       }
       const float mt = max64(x2);
-      const bool grow = mt > m_used + 8.0f;
+      // P slot g's previous user, P . C of tile j - 2, has finished.  Waited before the max
+      // is published: the other group then knows that this slot's phase for tile j - 2 is
+      // complete, so its own wait for P . C of tile j (one phase later) is unambiguous.
+      if (j >= 2 && !wait_cta(&bars->pdone[g], (k - 1) & 1)) { ok = false; break; }
+      // the running max after tile j - 1 (the other group's), then this tile's
+      float m_prev = -INFINITY;
+      if (j > 0) {
+        if (!wait_cta(&bars->mready[g ^ 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
+        m_prev = m_pub[(g ^ 1) * kMaxHeads + h];
+      }
+      const bool grow = mt > m_prev + 8.0f;
+      const float m_new = grow ? mt : m_prev;
+      m_pub[g * kMaxHeads + h] = m_new;       // read by the other group before it publishes again
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->mready[g]));
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // rescale this warp's rows of O once P . C of the previous tile has landed
-        if (!wait_cta(&bars->pdone[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
+        // rescale this warp's rows of O once P . C of tile j - 1 has landed (the other slot;
+        // its previous phase, tile j - 3, was seen complete by the other group before it
+        // published the max this group has just read)
+        if (!wait_cta(&bars->pdone[g ^ 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        const float alpha = grow ? ex2_approx(m_used - mt) : 1.0f;
+        const float alpha = grow ? ex2_approx(m_prev - m_new) : 1.0f;
+        const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll 1
         for (int c0 = 0; c0 < 256; c0 += 32) {
           uint32_t r[32];
           tmem_ld32(lane_addr + kTmO + c0, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          for (int i = 0; i < 16; ++i) {
+            const float2 v = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), al2, zero2);
+            r[2 * i] = __float_as_uint(v.x);
+            r[2 * i + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(lane_addr + kTmO + c0, r);
         }
         tmem_st_wait();
       }
-      if (grow) {
-        l_sum *= ex2_approx(m_used - mt);
-        m_used = mt;
+      if (m_g != m_new) {
+        l_g *= ex2_approx(m_g - m_new);       // 0 while this group has no sum yet
+        m_g = m_new;
       }
       uint32_t pk[32];
       float2 ps[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ps[i] = make_float2(0.0f, 0.0f);
-      const float2 negm2 = make_float2(-m_used, -m_used);
+      for (int i = 0; i < 4; ++i) ps[i] = zero2;
+      const float2 negm2 = make_float2(-m_new, -m_new);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float2 d = __fadd2_rn(x2[i], negm2);
@@ -547,25 +567,37 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       }
       {
         const float2 s2 = __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3]));
-        l_sum += s2.x + s2.y;
+        l_g += s2.x + s2.y;
       }
-      // P slot j % 2 once its previous user, P . C of tile j - 2, has finished reading it
-      if (j >= 2 && !wait_cta(&bars->pdone[bb], ((j - 2) >> 1) & 1)) { ok = false; break; }
-      tmem_st32(lane_addr + kTmP + 32 * bb, pk);
+      tmem_st32(lane_addr + kTmP + 32 * g, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->pfull[bb]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->pfull[g]));
     }
+    if (lane == 0) bulk_wait_all();           // this warp's copies have landed before the CTA may exit
     if (!ok) fail_timeout(bars, check);
-    // ---- epilogue: this CTA's 256 latent columns of every head
-    // (a single-phase barrier: a parity wait on pdone here could be two phases behind)
-    if (ok && n_tiles > 0 && wait_cta(&bars->ofinal, 0)) {
+    // ---- epilogue: reconcile the two groups' sums; group g writes latent columns
+    // [128 g, 128 g + 128) of this CTA's half of every head
+    // (ofinal is a single-phase barrier: a parity wait on pdone here could be two phases behind)
+    fin_x[(g * 2) * kMaxHeads + h] = m_g;
+    fin_x[(g * 2 + 1) * kMaxHeads + h] = l_g;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&bars->efin));
+    bool fin = ok && n_tiles > 0;
+    if (fin) {
+      fin = wait_cta(&bars->efin, 0) && wait_cta(&bars->ofinal, 0);
+      if (!fin) fail_timeout(bars, check);
+    }
+    if (fin) {
       tc_fence_after();
+      const float m_o = fin_x[((g ^ 1) * 2) * kMaxHeads + h], l_o = fin_x[((g ^ 1) * 2 + 1) * kMaxHeads + h];
+      const float m_fin = fmaxf(m_g, m_o);    // the running max after the last tile
+      const float l_sum = l_g * ex2_approx(m_g - m_fin) + l_o * ex2_approx(m_o - m_fin);
       const float inv = out_scale / l_sum;
       const bool live = h < n_h;
 #pragma unroll 1
-      for (int c0 = 0; c0 < 256; c0 += 32) {
+      for (int c0 = 128 * g; c0 < 128 * g + 128; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(lane_addr + kTmO + c0, r);
         tmem_ld_wait();
@@ -587,13 +619,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
           }
         }
       }
-      if (live && unit.part >= 0 && rank == 0)
-        ws.part_lse[(size_t)unit.part * n_h + h] = (m_used + log2f(l_sum)) * 0.69314718055994531f;
-    } else if (ok && n_tiles > 0) {
-      fail_timeout(bars, check);
+      if (live && unit.part >= 0 && rank == 0 && g == 0)
+        ws.part_lse[(size_t)unit.part * n_h + h] = (m_fin + log2f(l_sum)) * 0.69314718055994531f;
     }
-    // a timed-out CTA still lets in-flight partial-score stores from the peer land
-    if (!ok && tid == 0 && armed > 0) {
+    // a timed-out CTA still lets in-flight partial-score copies from the peer land
+    if (!ok && lane == 0 && q4 == 0 && armed > 0) {
       volatile int never = 0;
       mbar_wait<true>(smem_u32(&bars->recvfull[(armed - 1) & (kSlots - 1)]), ((armed - 1) >> 2) & 1, &never);
     }
@@ -663,7 +693,8 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, const int3
   // an FP8 cache holds codes of value / fp8_scale: the scale multiplies every score and the output
   const float cache_scale = kFp8 ? h.cfg.fp8_scale : 1.0f;
   const float scale_log2 = h.scale * cache_scale * 1.4426950408889634f;
-  return launch_pdl(decode_tc_kernel<kFp8>, dim3(2 * ws.max_units), dim3(kThreads), kSmemBytes, st, map, map_rope,
+  return launch_pdl(decode_tc_kernel<kFp8>, dim3(2 * ws.max_units), dim3(kFp8 ? kThreadsFp8 : kThreads), kSmemBytes,
+                    st, map, map_rope,
                     ctx_len,
                     h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, ws, h.check_word);
 }
