@@ -185,15 +185,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int unit_idx = blockIdx.x >> 1;
-  griddep_wait();                           // plan, absorbed queries and cache rows are inputs
-  griddep_launch_dependents();
-  if (unit_idx >= ws.counters[0]) return;   // both CTAs of the cluster leave together
-  const Unit unit = ws.units[unit_idx];
-  const int b = unit.b;
-  const int L = ctx_len[b];
-  const int t_end = min(unit.page_end * kPage, L);
-  const int n_tiles = unit.page_end - unit.page_begin;
+  const uint32_t stage0 = sbase + kOffStages;
 
+  // barriers and descriptor prefetch need nothing from the earlier kernels of the step
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
@@ -215,80 +209,108 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
-    tmem_alloc(smem_u32(&bars->tmem_base), 512);
-    tmem_relinquish();
-  }
   if (warp == kWarpProducer && lane == 0) {
     prefetch_tmap(&tmap);
     prefetch_tmap(&tmap_rope);
   }
+  __syncthreads();
+  griddep_wait();                           // plan, absorbed queries and cache rows are inputs
+  griddep_launch_dependents();
+  if (unit_idx >= ws.counters[0]) return;   // both CTAs of the cluster leave together
+  const Unit unit = ws.units[unit_idx];
+  const int b = unit.b;
+  const int n_tiles = unit.page_end - unit.page_begin;
+
+  // TMA of tile j into ring stage j % kStages (both CTAs: this CTA's 288 columns)
+  const int32_t* bt_row = block_table + (size_t)b * bt_stride + unit.page_begin;
+  auto issue_tile = [&](int j, int page) {
+    const int s = j % kStages;
+    if (page < 0 || page >= num_pages) {   // bad page id: read page 0 instead; the output is zeroed later
+      if (rank == 0) {
+        atomicOr(check, kCheckPageId);
+        ws.bad[b] = 1;
+      }
+      page = 0;
+    }
+    const uint32_t full = smem_u32(&bars->full[s]);
+    mbar_arrive_expect_tx(full, (uint32_t)(kFp8 ? kStageBytes / 2 : kStageBytes));
+    for (int c = 0; c < 4; ++c)            // FP8: each code box into the upper half of its chunk slot
+      tma_load_2d(stage0 + s * kStageBytes + c * kChunkBytes + (kFp8 ? kChunkBytes / 2 : 0), &tmap,
+                  (int)(rank * 256 + c * 64), page * kPage, full);
+    tma_load_2d(stage0 + s * kStageBytes + 4 * kChunkBytes + (kFp8 ? kRopeBytes / 2 : 0), &tmap_rope,
+                (int)(kDc + rank * 32), page * kPage, full);
+  };
+  // the ring starts empty: its first tiles are requested before anything else
+  const int n_pre = min(n_tiles, kStages);
+  if (warp == kWarpProducer && lane == 0) {
+    int pages[kStages];
+#pragma unroll
+    for (int j = 0; j < kStages; ++j) pages[j] = j < n_pre ? bt_row[j] : 0;
+    for (int j = 0; j < n_pre; ++j) issue_tile(j, pages[j]);
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(&bars->tmem_base), 512);
+    tmem_relinquish();
+  }
+  const int L = ctx_len[b];
+  const int t_end = min(unit.page_end * kPage, L);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  // ---- absorbed query of this CTA: latent half -> TMEM (A operand), RoPE part -> smem (CTA 1)
-  if (warp < 4) {
-    const int h = tid;
+  // ---- absorbed query of this CTA: latent half -> TMEM (A operand), RoPE part -> shared
+  // memory; warp w loads heads 32 (w % 4) .. + 31, latent columns 128 (w / 4) .. + 127 of
+  // this CTA's 256 (and warps 4-7 the 32 RoPE values), every load issued before any is used
+  if (warp < 8) {
+    const int q4 = warp & 3, half = warp >> 2;
+    const int h = q4 * 32 + lane;
     const bool live = h < n_h;
     const uint4* src = reinterpret_cast<const uint4*>(ws.q_abs + ((size_t)b * n_h + (live ? h : 0)) * kRow);
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
+    uint4 v[16], vr[4];
 #pragma unroll
-    for (int part = 0; part < 4; ++part) {        // 4 x 32 columns = 256 bf16
+    for (int i = 0; i < 16; ++i) v[i] = live ? src[rank * 32 + half * 16 + i] : make_uint4(0, 0, 0, 0);
+    if (half == 1) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) vr[k] = live ? src[64 + rank * 4 + k] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {        // 2 x 32 columns = 128 bf16
       uint32_t r[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint4 v = live ? src[rank * 32 + part * 8 + i] : make_uint4(0, 0, 0, 0);
-        r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+        const uint4 x = v[part * 8 + i];
+        r[4 * i] = x.x; r[4 * i + 1] = x.y; r[4 * i + 2] = x.z; r[4 * i + 3] = x.w;
       }
-      tmem_st32(lane_addr + kTmQ + 32 * part, r);
+      tmem_st32(lane_addr + kTmQ + 64 * half + 32 * part, r);
     }
-    {
+    if (half == 1) {
       // this CTA's 32 RoPE query values: 64-byte rows in the 64-byte swizzle
       uint8_t* qpe = smem + kOffQpe;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 v = live ? src[64 + rank * 4 + k] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qpe + h * 64 + ((k ^ ((h >> 1) & 3)) * 16)) = v;
-      }
+      for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(qpe + h * 64 + ((k ^ ((h >> 1) & 3)) * 16)) = vr[k];
       fence_proxy_async_smem();
     }
     tmem_st_wait();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();              // peer barriers initialised before any st.async into this CTA
+  cluster_sync();              // peer barriers initialised before any copy into this CTA
   tc_fence_after();
 
-  const uint32_t stage0 = sbase + kOffStages;
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int32_t* bt_row = block_table + (size_t)b * bt_stride + unit.page_begin;
-      const uint32_t bytes = (uint32_t)(kFp8 ? kStageBytes / 2 : kStageBytes);
-      int issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
+      int issued = n_pre;
+      for (int j = n_pre; j < n_tiles; ++j) {
         const int s = j % kStages;
-        if (j >= kStages && !mbar_wait(smem_u32(&bars->empty[s]), ((j / kStages) & 1) ^ 1, abort_flag)) {
+        const int page = bt_row[j];
+        if (!mbar_wait(smem_u32(&bars->empty[s]), ((j / kStages) & 1) ^ 1, abort_flag)) {
           fail_timeout(bars, check);
           break;
         }
-        int page = bt_row[j];
-        if (page < 0 || page >= num_pages) {   // bad page id: read page 0 instead; the output is zeroed later
-          if (rank == 0) {
-            atomicOr(check, kCheckPageId);
-            ws.bad[b] = 1;
-          }
-          page = 0;
-        }
-        const uint32_t full = smem_u32(&bars->full[s]);
-        mbar_arrive_expect_tx(full, bytes);
-        for (int c = 0; c < 4; ++c)          // FP8: each code box into the upper half of its chunk slot
-          tma_load_2d(stage0 + s * kStageBytes + c * kChunkBytes + (kFp8 ? kChunkBytes / 2 : 0), &tmap,
-                      (int)(rank * 256 + c * 64), page * kPage, full);
-        tma_load_2d(stage0 + s * kStageBytes + 4 * kChunkBytes + (kFp8 ? kRopeBytes / 2 : 0), &tmap_rope,
-                    (int)(kDc + rank * 32), page * kPage, full);
+        issue_tile(j, page);
         issued = j + 1;
       }
       // drain: every load issued has landed before the CTA may exit
