@@ -102,6 +102,7 @@ struct Bars {                               // mbarriers (8 bytes each) and flag
   uint64_t pfull[2];                        // P(j) written into P slot j % 2       (4 warps)
   uint64_t pdone[2];                        // P . C of a tile in P slot b done     (MMA commit)
   uint64_t ofinal;                          // single phase: the last P . C landed  (MMA commit)
+  uint64_t qfull;                           // single phase: the absorbed query landed (producer, tx)
   uint64_t recvfull[kSlots];                // peer's partial scores arrived        (1 + 16 KB tx)
   uint64_t drain[2];                        // every MMA of the QK^T / P . C issuer done
   uint32_t tmem_base;
@@ -170,6 +171,7 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_rope,
+                 const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_qpe,
                  const int32_t* __restrict__ ctx_len, int n_h,
                  const int32_t* __restrict__ block_table, int bt_stride, int num_pages, float scale_log2,
                  float out_scale, Workspace ws, unsigned* check) {
@@ -205,6 +207,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&bars->recvfull[i]), 1);
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->pdone[i]), 1);
     mbar_init(smem_u32(&bars->ofinal), 1);
+    mbar_init(smem_u32(&bars->qfull), 1);
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->drain[i]), 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -212,6 +215,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   if (warp == kWarpProducer && lane == 0) {
     prefetch_tmap(&tmap);
     prefetch_tmap(&tmap_rope);
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_qpe);
   }
   __syncthreads();
   griddep_wait();                           // plan, absorbed queries and cache rows are inputs
@@ -240,9 +245,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     tma_load_2d(stage0 + s * kStageBytes + 4 * kChunkBytes + (kFp8 ? kRopeBytes / 2 : 0), &tmap_rope,
                 (int)(kDc + rank * 32), page * kPage, full);
   };
-  // the ring starts empty: its first tiles are requested before anything else
+  // the absorbed query of this CTA (latent half: 4 boxes of 64 columns x 128 heads, 128-byte
+  // swizzle, staged in the still unused receive slots; RoPE half: straight into its 64-byte
+  // swizzled operand slot; heads past n_h read as zeros), then the first tiles of the empty ring
   const int n_pre = min(n_tiles, kStages);
   if (warp == kWarpProducer && lane == 0) {
+    const uint32_t qf = smem_u32(&bars->qfull);
+    mbar_arrive_expect_tx(qf, (uint32_t)(4 * kMaxHeads * 128 + kQpeBytes));
+    for (int c = 0; c < 4; ++c) tma_load_3d(sbase + kOffRecv + c * kMaxHeads * 128, &tmap_q, (int)(rank * 256 + c * 64), 0, b, qf);
+    tma_load_3d(sbase + kOffQpe, &tmap_qpe, (int)(kDc + rank * 32), 0, b, qf);
     int pages[kStages];
 #pragma unroll
     for (int j = 0; j < kStages; ++j) pages[j] = j < n_pre ? bt_row[j] : 0;
@@ -259,40 +270,29 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  // ---- absorbed query of this CTA: latent half -> TMEM (A operand), RoPE part -> shared
-  // memory; warp w loads heads 32 (w % 4) .. + 31, latent columns 128 (w / 4) .. + 127 of
-  // this CTA's 256 (and warps 4-7 the 32 RoPE values), every load issued before any is used
+  // ---- latent half of the query: shared memory -> TMEM (A operand of QK^T).  Warp w moves heads
+  // 32 (w % 4) .. + 31, latent columns 128 (w / 4) .. + 127 of this CTA's 256.
   if (warp < 8) {
     const int q4 = warp & 3, half = warp >> 2;
     const int h = q4 * 32 + lane;
-    const bool live = h < n_h;
-    const uint4* src = reinterpret_cast<const uint4*>(ws.q_abs + ((size_t)b * n_h + (live ? h : 0)) * kRow);
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
-    uint4 v[16], vr[4];
+    if (__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->qfull), 0, abort_flag))) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = live ? src[rank * 32 + half * 16 + i] : make_uint4(0, 0, 0, 0);
-    if (half == 1) {
+      for (int part = 0; part < 2; ++part) {      // box 2 half + part: 64 columns = 32 TMEM columns
+        const uint8_t* row = smem + kOffRecv + (2 * half + part) * kMaxHeads * 128 + h * 128;
+        uint32_t r[32];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) vr[k] = live ? src[64 + rank * 4 + k] : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {        // 2 x 32 columns = 128 bf16
-      uint32_t r[32];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 x = v[part * 8 + i];
-        r[4 * i] = x.x; r[4 * i + 1] = x.y; r[4 * i + 2] = x.z; r[4 * i + 3] = x.w;
+        for (int k = 0; k < 8; ++k) {
+          const uint4 x = *reinterpret_cast<const uint4*>(row + ((k ^ (h & 7)) * 16));
+          r[4 * k] = x.x; r[4 * k + 1] = x.y; r[4 * k + 2] = x.z; r[4 * k + 3] = x.w;
+        }
+        tmem_st32(lane_addr + kTmQ + 64 * half + 32 * part, r);
       }
-      tmem_st32(lane_addr + kTmQ + 64 * half + 32 * part, r);
+      tmem_st_wait();
+    } else {
+      fail_timeout(bars, check);
     }
-    if (half == 1) {
-      // this CTA's 32 RoPE query values: 64-byte rows in the 64-byte swizzle
-      uint8_t* qpe = smem + kOffQpe;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(qpe + h * 64 + ((k ^ ((h >> 1) & 3)) * 16)) = vr[k];
-      fence_proxy_async_smem();
-    }
-    tmem_st_wait();
+    fence_proxy_async_smem();    // these reads come before the copies that later reuse the slots
   }
   tc_fence_before();
   __syncthreads();
@@ -700,9 +700,25 @@ cudaError_t make_cache_tensor_map_fp8(const void* cache, int num_pages, int widt
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor map of the absorbed query [B][n_h][576] bf16 as (column, head, sequence): boxes of
+// `width` columns x 128 heads x 1 sequence (heads past n_h read as zeros), 128-byte swizzle for
+// 64 columns, 64-byte swizzle for 32.
+cudaError_t make_query_tensor_map(const void* q_abs, int batch, int n_h, int width, CUtensorMap* map) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)kRow, (cuuint64_t)n_h, (cuuint64_t)batch};
+  const cuuint64_t strides[2] = {(cuuint64_t)kRow * 2, (cuuint64_t)kRow * 2 * n_h};
+  const cuuint32_t box[3] = {(cuuint32_t)width, (cuuint32_t)kMaxHeads, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_abs), dims, strides, box, elem,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, width == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 namespace {
 template <bool kFp8>
-cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, const int32_t* block_table, int bt_stride,
+cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table, int bt_stride,
                              int num_pages, const CUtensorMap& map, const CUtensorMap& map_rope, const Workspace& ws,
                              cudaStream_t st) {
   static bool attr = false;
@@ -715,8 +731,13 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, const int3
   // an FP8 cache holds codes of value / fp8_scale: the scale multiplies every score and the output
   const float cache_scale = kFp8 ? h.cfg.fp8_scale : 1.0f;
   const float scale_log2 = h.scale * cache_scale * 1.4426950408889634f;
+  // the absorbed query [B][n_h][576] as (column, head, sequence): 64- and 32-column boxes of 128 heads
+  alignas(64) CUtensorMap map_q, map_qpe;
+  cudaError_t e = make_query_tensor_map(ws.q_abs, batch, h.cfg.n_h, 64, &map_q);
+  if (e == cudaSuccess) e = make_query_tensor_map(ws.q_abs, batch, h.cfg.n_h, 32, &map_qpe);
+  if (e != cudaSuccess) return e;
   return launch_pdl(decode_tc_kernel<kFp8>, dim3(2 * ws.max_units), dim3(kFp8 ? kThreadsFp8 : kThreads), kSmemBytes,
-                    st, map, map_rope,
+                    st, map, map_rope, map_q, map_qpe,
                     ctx_len,
                     h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, ws, h.check_word);
 }
@@ -740,8 +761,8 @@ cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, co
   }
   const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(hm.tmap);
   const CUtensorMap& map_rope = *reinterpret_cast<const CUtensorMap*>(hm.tmap_rope);
-  return fp8 ? launch_decode_tc<true>(h, ctx_len, block_table, bt_stride, num_pages, map, map_rope, ws, st)
-             : launch_decode_tc<false>(h, ctx_len, block_table, bt_stride, num_pages, map, map_rope, ws, st);
+  return fp8 ? launch_decode_tc<true>(h, ctx_len, batch, block_table, bt_stride, num_pages, map, map_rope, ws, st)
+             : launch_decode_tc<false>(h, ctx_len, batch, block_table, bt_stride, num_pages, map, map_rope, ws, st);
 }
 
 }  // namespace mla
