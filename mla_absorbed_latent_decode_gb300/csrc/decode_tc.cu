@@ -172,6 +172,7 @@ template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_rope,
                  const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_qpe,
+                 const __grid_constant__ CUtensorMap tmap_o,
                  const int32_t* __restrict__ ctx_len, int n_h,
                  const int32_t* __restrict__ block_table, int bt_stride, int num_pages, float scale_log2,
                  float out_scale, Workspace ws, unsigned* check) {
@@ -217,6 +218,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     prefetch_tmap(&tmap_rope);
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_qpe);
+    prefetch_tmap(&tmap_o);
   }
   __syncthreads();
   griddep_wait();                           // plan, absorbed queries and cache rows are inputs
@@ -618,27 +620,41 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       const float l_sum = l_g * ex2_approx(m_g - m_fin) + l_o * ex2_approx(m_o - m_fin);
       const float inv = out_scale / l_sum;
       const bool live = h < n_h;
+      // a whole sequence: bf16 rows staged in the (now idle) ring, this warp's 32 heads x 2 boxes
+      // of 64 columns, 128-byte swizzled, and written by TMA stores (heads past n_h are clipped)
+      uint8_t* ob = smem + kOffStages + (g * 4 + q4) * 2 * 4096;
 #pragma unroll 1
-      for (int c0 = 128 * g; c0 < 128 * g + 128; c0 += 32) {
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c0 = 128 * g + 32 * cc;
         uint32_t r[32];
         tmem_ld32(lane_addr + kTmO + c0, r);
         tmem_ld_wait();
-        if (!live) continue;
         if (unit.part < 0) {
-          uint4* dst = reinterpret_cast<uint4*>(ws.o_lat + ((size_t)b * n_h + h) * kDc + rank * 256 + c0);
+          uint8_t* row = ob + (cc >> 1) * 4096 + lane * 128;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float* f = reinterpret_cast<const float*>(r + 8 * i);
-            dst[i] = make_uint4(bf16x2_bits(f[0] * inv, f[1] * inv), bf16x2_bits(f[2] * inv, f[3] * inv),
-                                bf16x2_bits(f[4] * inv, f[5] * inv), bf16x2_bits(f[6] * inv, f[7] * inv));
+            *reinterpret_cast<uint4*>(row + (((((cc & 1) * 4) + i) ^ (lane & 7)) * 16)) =
+                make_uint4(bf16x2_bits(f[0] * inv, f[1] * inv), bf16x2_bits(f[2] * inv, f[3] * inv),
+                           bf16x2_bits(f[4] * inv, f[5] * inv), bf16x2_bits(f[6] * inv, f[7] * inv));
           }
-        } else {
+        } else if (live) {
           float4* dst = reinterpret_cast<float4*>(ws.part_o + ((size_t)unit.part * n_h + h) * kDc + rank * 256 + c0);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float* f = reinterpret_cast<const float*>(r + 4 * i);
             dst[i] = make_float4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
           }
+        }
+      }
+      if (unit.part < 0) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && 32 * q4 < n_h) {
+          for (int bx = 0; bx < 2; ++bx)
+            tma_store_3d(&tmap_o, smem_u32(ob + bx * 4096), (int)(rank * 256 + 128 * g + 64 * bx), 32 * q4, b);
+          bulk_commit_group();
+          bulk_wait_all();                    // written (and the staging read) before the CTA may exit
         }
       }
       if (live && unit.part >= 0 && rank == 0 && g == 0)
@@ -716,6 +732,21 @@ cudaError_t make_query_tensor_map(const void* q_abs, int batch, int n_h, int wid
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor map of the normalised latent sums o_lat [B][n_h][512] bf16 as (column, head, sequence):
+// store boxes of 64 columns x 32 heads x 1 sequence, 128-byte swizzle.
+cudaError_t make_latent_out_tensor_map(void* o_lat, int batch, int n_h, CUtensorMap* map) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)kDc, (cuuint64_t)n_h, (cuuint64_t)batch};
+  const cuuint64_t strides[2] = {(cuuint64_t)kDc * 2, (cuuint64_t)kDc * 2 * n_h};
+  const cuuint32_t box[3] = {64, 32, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o_lat, dims, strides, box, elem,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 namespace {
 template <bool kFp8>
 cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table, int bt_stride,
@@ -733,11 +764,13 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch,
   const float scale_log2 = h.scale * cache_scale * 1.4426950408889634f;
   // the absorbed query [B][n_h][576] as (column, head, sequence): 64- and 32-column boxes of 128 heads
   alignas(64) CUtensorMap map_q, map_qpe;
+  alignas(64) CUtensorMap map_o;
   cudaError_t e = make_query_tensor_map(ws.q_abs, batch, h.cfg.n_h, 64, &map_q);
   if (e == cudaSuccess) e = make_query_tensor_map(ws.q_abs, batch, h.cfg.n_h, 32, &map_qpe);
+  if (e == cudaSuccess) e = make_latent_out_tensor_map(ws.o_lat, batch, h.cfg.n_h, &map_o);
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_tc_kernel<kFp8>, dim3(2 * ws.max_units), dim3(kFp8 ? kThreadsFp8 : kThreads), kSmemBytes,
-                    st, map, map_rope, map_q, map_qpe,
+                    st, map, map_rope, map_q, map_qpe, map_o,
                     ctx_len,
                     h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, ws, h.check_word);
 }
