@@ -267,7 +267,7 @@ def run_ours(args):
         of that size, so that L2 ends up holding clean lines only and no write-back of the
         flush's own dirty lines lands inside the next timed step."""
         flush.zero_()
-        flush_rd.sum()
+        flush_rd.view(torch.int32).amax()
     sess.mla.set_option(B.MLA_OPT_PROFILE, 1)
 
     def step():
