@@ -260,6 +260,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
 #pragma unroll
     for (int j = 0; j < kStages; ++j) pages[j] = j < n_pre ? bt_row[j] : 0;
     for (int j = 0; j < n_pre; ++j) issue_tile(j, pages[j]);
+    for (int j = kStages; j < min(n_tiles, 2 * kStages); ++j) {    // the next user of each stage, into L2
+      const int pg = bt_row[j];
+      if (pg >= 0 && pg < num_pages) {
+        for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tmap, (int)(rank * 256 + c * 64), pg * kPage);
+        tma_prefetch_2d(&tmap_rope, (int)(kDc + rank * 32), pg * kPage);
+      }
+    }
   }
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
@@ -308,6 +315,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       for (int j = n_pre; j < n_tiles; ++j) {
         const int s = j % kStages;
         const int page = bt_row[j];
+        if (j + kStages < n_tiles) {         // the tile that will refill this stage next, into L2
+          const int pg = bt_row[j + kStages];
+          if (pg >= 0 && pg < num_pages) {
+            for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tmap, (int)(rank * 256 + c * 64), pg * kPage);
+            tma_prefetch_2d(&tmap_rope, (int)(kDc + rank * 32), pg * kPage);
+          }
+        }
         if (!mbar_wait(smem_u32(&bars->empty[s]), ((j / kStages) & 1) ^ 1, abort_flag)) {
           fail_timeout(bars, check);
           break;
