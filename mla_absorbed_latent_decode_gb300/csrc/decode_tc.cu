@@ -47,7 +47,7 @@
 //     than 8, so P <= 2^8.
 //   * Warp roles per CTA: warps 0-3 and 4-7 the two tile groups (score exchange,
 //     softmax, epilogue), warp 8 TMA producer, warp 9 issues QK^T, warp 10 issues
-//     P . C; with an FP8 cache, warps 11-14 convert each tile to bf16 in place.
+//     P . C; with an FP8 cache, warps 11-15 convert each tile to bf16 in place, one box each.
 //     Every wait is bounded; on a timeout the kernel sets MLA_CHECK_TIMEOUT,
 //     drains and returns.
 #include <cuda.h>
@@ -78,11 +78,11 @@ constexpr int kOffXchg = kOffBars + 1024;             // running maxima / final 
 constexpr int kXchgBytes = 3 * 2 * kMaxHeads * 4;
 constexpr int kSmemBytes = kOffXchg + kXchgBytes + 1024;   // + alignment slack
 constexpr int kThreads = 352;                          // 2 tile groups of 4 warps, producer, 2 MMA warps
-constexpr int kThreadsFp8 = 480;                       // + 4 FP8 conversion warps
+constexpr int kThreadsFp8 = 512;                       // + 5 FP8 conversion warps
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;                            // QK^T issuer (allocates TMEM)
 constexpr int kWarpPv = 10;                            // P . C issuer
-constexpr int kWarpConv = 11;                          // FP8 cache: warps 11-14 convert tiles
+constexpr int kWarpConv = 11;                          // FP8 cache: warps 11-15 convert tiles
 
 // TMEM column map
 constexpr uint32_t kTmO = 0;
@@ -92,8 +92,7 @@ constexpr uint32_t kTmP = 448;             // P slot b (64 bf16 per lane) at kTm
 
 struct Bars {                               // mbarriers (8 bytes each) and flags
   uint64_t full[kStages];                   // TMA tile landed                      (producer, tx)
-  uint64_t conv[kStages];                   // FP8 cache: tile converted to bf16    (4 conversion warps)
-  uint64_t cread[kStages];                  // FP8 cache: every code of the tile read (4 conversion warps)
+  uint64_t conv[kStages];                   // FP8 cache: tile converted to bf16    (5 conversion warps)
   uint64_t empty[kStages];                  // tile consumed by P . C               (MMA commit)
   uint64_t sfull[2];                        // S_r(j) in TMEM, tile group j % 2     (MMA commit)
   uint64_t sfree[2];                        // S_r(j) loaded by its tile group      (4 warps)
@@ -147,13 +146,16 @@ __device__ __forceinline__ void fail_timeout(Bars* bars, unsigned* check) {
   if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
 }
 
-// FP8 cache: e4m3 -> bf16, exact (every e4m3 value is a normal fp16 or zero, and a bf16).  Two
-// e4m3 codes -> fp16 pair by cvt; fp16 -> bf16 by moving the exponent bias from 15 to 127 and
-// dropping three mantissa bits that are zero for these values.
+// FP8 cache: e4m3 -> bf16, exact (every e4m3 value is a normal fp16 or zero, and a bf16 with
+// four significant bits at most).  Two e4m3 codes -> fp16 pair by cvt, then each fp16 -> bf16 by
+// cvt (exact here, so the rounding mode never acts).
 __device__ __forceinline__ uint32_t f16x2_to_bf16x2_exact(uint32_t w) {
-  const uint32_t t = (w >> 3) & 0x0FFF0FFFu;                  // magnitudes, realigned
-  const uint32_t add = ((t & 0x0000FFFFu) ? 0x00003800u : 0u) | ((t & 0xFFFF0000u) ? 0x38000000u : 0u);
-  return (w & 0x80008000u) | (t + add);
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
+      "cvt.rn.bf16.f16 l, l;\n\tcvt.rn.bf16.f16 h, h;\n\tmov.b32 %0, {l, h};\n\t}"
+      : "=r"(r)
+      : "r"(w));
+  return r;
 }
 __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
   uint32_t h0, h1;
@@ -165,8 +167,8 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
 }
 
 // kFp8: the cache holds e4m3 codes.  The producer TMA-loads each 64 x 64 code box into the
-// upper half of the 8 KB slot its bf16 chunk will occupy; the conversion warps convert the
-// tile in place (all reads, a barrier, then all writes) before QK^T may use it.  The tensor
+// upper half of the 8 KB slot its bf16 chunk will occupy; one conversion warp per box converts
+// it in place (all its reads, then all its writes) before QK^T may use the tile.  The tensor
 // scale is folded into the softmax scale and the output scale by the launcher.
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
@@ -195,8 +197,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
       mbar_init(smem_u32(&bars->empty[s]), 1);
-      mbar_init(smem_u32(&bars->conv[s]), 4);
-      mbar_init(smem_u32(&bars->cread[s]), 4);
+      mbar_init(smem_u32(&bars->conv[s]), 5);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->sfull[i]), 1);
@@ -394,12 +395,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     }
   } else if (warp >= kWarpConv) {
     // ------------------------------------------------------------ FP8 cache: e4m3 -> bf16 in place
-    // (launched only with an FP8 cache) thread = (row h / 2, 32-column half h % 2) of every
-    // chunk of a tile; every code of the tile is read, by all four warps, before any is
-    // overwritten.  Every wait is bounded: a warp that gives up aborts the kernel.
+    // (launched only with an FP8 cache) warp 11 + c converts latent chunk c of every tile,
+    // warp 15 the RoPE box.  A box's codes sit in the upper half of the slot its bf16 rows
+    // fill, so all of them are read (into the warp's registers) before any row is written;
+    // one warp per box makes that a warp-level order.  Every wait is bounded: a warp that
+    // gives up aborts the kernel.
     if constexpr (kFp8) {
-      const int h = tid - kWarpConv * 32;
-      const int r = h >> 1, hf = h & 1;
+      const int c = warp - kWarpConv;         // 0..3 latent chunk, 4 RoPE box
       bool ok = true;
       for (int t = 0; t < n_tiles; ++t) {
         const int s = t % kStages;
@@ -408,37 +410,39 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
           break;
         }
         uint8_t* st = smem + kOffStages + s * kStageBytes;
-        uint4 v[9];
+        if (c < 4) {
+          // lane = (row 8 k + lane / 4, 16 codes 16 (lane % 4) ..) for k = 0..7
+          const int p = lane & 3;
+          uint8_t* box = st + c * kChunkBytes;
+          uint4 v[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4* src = reinterpret_cast<const uint4*>(st + c * kChunkBytes + kChunkBytes / 2 + r * 64 + hf * 32);
-          v[2 * c] = src[0];
-          v[2 * c + 1] = src[1];
-        }
-        v[8] = *reinterpret_cast<const uint4*>(st + 4 * kChunkBytes + kRopeBytes / 2 + r * 32 + hf * 16);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->cread[s]));
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->cread[s]), (t / kStages) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
+          for (int k = 0; k < 8; ++k)
+            v[k] = *reinterpret_cast<const uint4*>(box + kChunkBytes / 2 + (8 * k + (lane >> 2)) * 64 + p * 16);
+          __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {           // latent: 128-byte rows, 128-byte swizzle
-          uint8_t* row = st + c * kChunkBytes + r * 128;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {         // 16-byte chunk 4 hf + i of the row: 8 codes
-            const uint4 w = v[2 * c + (i >> 1)];
-            const uint2 lo = e4m3x4_to_bf16x4((i & 1) ? w.z : w.x), hi = e4m3x4_to_bf16x4((i & 1) ? w.w : w.y);
-            *reinterpret_cast<uint4*>(row + (((4 * hf + i) ^ (r & 7)) * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          for (int k = 0; k < 8; ++k) {       // 128-byte rows, 128-byte swizzle
+            const int r = 8 * k + (lane >> 2);
+            const uint2 a = e4m3x4_to_bf16x4(v[k].x), b = e4m3x4_to_bf16x4(v[k].y);
+            const uint2 d = e4m3x4_to_bf16x4(v[k].z), e = e4m3x4_to_bf16x4(v[k].w);
+            *reinterpret_cast<uint4*>(box + r * 128 + (((2 * p) ^ (r & 7)) * 16)) = make_uint4(a.x, a.y, b.x, b.y);
+            *reinterpret_cast<uint4*>(box + r * 128 + (((2 * p + 1) ^ (r & 7)) * 16)) = make_uint4(d.x, d.y, e.x, e.y);
           }
-        }
-        {                                       // RoPE key: 64-byte rows, 64-byte swizzle
-          uint8_t* row = st + 4 * kChunkBytes + r * 64;
+        } else {
+          // lane = (row 16 k + lane / 2, 16 codes 16 (lane % 2) ..) for k = 0..3
+          const int p = lane & 1;
+          uint8_t* box = st + 4 * kChunkBytes;
+          uint4 v[4];
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {         // 16-byte chunk 2 hf + i of the row: 8 codes
-            const uint32_t a = i ? v[8].z : v[8].x, c2 = i ? v[8].w : v[8].y;
-            const uint2 lo = e4m3x4_to_bf16x4(a), hi = e4m3x4_to_bf16x4(c2);
-            *reinterpret_cast<uint4*>(row + (((2 * hf + i) ^ ((r >> 1) & 3)) * 16)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          for (int k = 0; k < 4; ++k)
+            v[k] = *reinterpret_cast<const uint4*>(box + kRopeBytes / 2 + (16 * k + (lane >> 1)) * 32 + p * 16);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {       // 64-byte rows, 64-byte swizzle
+            const int r = 16 * k + (lane >> 1);
+            const uint2 a = e4m3x4_to_bf16x4(v[k].x), b = e4m3x4_to_bf16x4(v[k].y);
+            const uint2 d = e4m3x4_to_bf16x4(v[k].z), e = e4m3x4_to_bf16x4(v[k].w);
+            *reinterpret_cast<uint4*>(box + r * 64 + (((2 * p) ^ ((r >> 1) & 3)) * 16)) = make_uint4(a.x, a.y, b.x, b.y);
+            *reinterpret_cast<uint4*>(box + r * 64 + (((2 * p + 1) ^ ((r >> 1) & 3)) * 16)) = make_uint4(d.x, d.y, e.x, e.y);
           }
         }
         fence_proxy_async_smem();
