@@ -146,24 +146,24 @@ __device__ __forceinline__ void fail_timeout(Bars* bars, unsigned* check) {
   if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
 }
 
-// FP8 cache: e4m3 -> bf16, exact (every e4m3 value is a normal fp16 or zero, and a bf16 with
-// four significant bits at most).  Two e4m3 codes -> fp16 pair by cvt, then each fp16 -> bf16 by
-// cvt (exact here, so the rounding mode never acts).
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2_exact(uint32_t w) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
-      "cvt.rn.bf16.f16 l, l;\n\tcvt.rn.bf16.f16 h, h;\n\tmov.b32 %0, {l, h};\n\t}"
-      : "=r"(r)
-      : "r"(w));
-  return r;
+// FP8 cache: e4m3 -> bf16, exact, in integer and fp32 arithmetic (no conversion instruction):
+// the code's 7 magnitude bits placed at bit 20 of a float32, its sign at bit 31, make that
+// value times 2^-120 (a normal e4m3 keeps its exponent and mantissa fields; a subnormal one
+// becomes a float32 subnormal), so one multiply by 2^120 (denormals kept) gives the value; it
+// has at most 4 significant bits, so the upper 16 bits of the float32 are its bf16.  Code k of
+// the word is moved to bits 24..31, shifted arithmetically by 4 (the sign lands on bits 28..31)
+// and masked.  Output: bf16 of codes (0, 1) and (2, 3), low half first.
+__device__ __forceinline__ float e4m3_at_top_to_f32(uint32_t t) {
+  const uint32_t bits = (uint32_t)((int32_t)t >> 4) & 0x87F00000u;
+  float f;
+  asm("mul.rn.f32 %0, %1, 0f7B800000;" : "=f"(f) : "f"(__uint_as_float(bits)));   // x 2^120
+  return f;
 }
 __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
-  uint32_t h0, h1;
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-      : "=r"(h0), "=r"(h1)
-      : "r"(w));
-  return make_uint2(f16x2_to_bf16x2_exact(h0), f16x2_to_bf16x2_exact(h1));
+  const float f0 = e4m3_at_top_to_f32(w << 24), f1 = e4m3_at_top_to_f32(w << 16);
+  const float f2 = e4m3_at_top_to_f32(w << 8), f3 = e4m3_at_top_to_f32(w);
+  return make_uint2(__byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632),
+                    __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632));
 }
 
 // kFp8: the cache holds e4m3 codes.  The producer TMA-loads each 64 x 64 code box into the
