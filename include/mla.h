@@ -156,6 +156,41 @@ mla_status_t mla_kv_append(mla_handle_t h, const void* rows, const int32_t* seq,
                            int32_t num_pages, mla_stream_t stream);
 
 /*
+ * mla_kv_project_append -- the down-projection of n hidden states into cache rows, written into
+ * the paged cache in the same call.
+ *
+ * Row i = x[i] . W_DKV^T ("DeepSeek-V2-Lite 真实权重执行审计" §3.1: kv_a_proj_with_mqa maps a
+ * hidden state to the [d_c | d_rope] row; the kv norm is the identity here), each value the
+ * bf16 rounding of an fp32 sum, is then stored exactly as mla_kv_append stores a row (same
+ * slot, rotation, encoding and device checks): the bytes equal those of mla_project into a
+ * rows buffer followed by mla_kv_append.
+ *
+ *   x            device [n][hidden] bf16, 16-byte aligned.
+ *   hidden       a positive multiple of 256.
+ *   w_dkv        device [d_c + d_rope][hidden] bf16, 16-byte aligned (caller-owned).
+ *   seq, pos, n, block_table, bt_rows, bt_stride, cache, num_pages: as in mla_kv_append.
+ */
+mla_status_t mla_kv_project_append(mla_handle_t h, const void* x, int32_t hidden, const void* w_dkv,
+                                   const int32_t* seq, const int32_t* pos, int32_t n,
+                                   const int32_t* block_table, int32_t bt_rows, int32_t bt_stride,
+                                   void* cache, int32_t num_pages, mla_stream_t stream);
+
+/*
+ * mla_project -- y = x . W^T for a few rows: the query projection (W_Q: [n_h (d_nope +
+ * d_rope)][hidden], giving q in the layout mla_decode takes, "80 行 PyTorch 从零写 DeepSeek 的
+ * MLA" §2) and the output projection over the heads' concatenated values (W_O).
+ *
+ *   x            device [m][k] bf16, 16-byte aligned; m >= 0 rows (0 is a no-op).
+ *   k            a positive multiple of 256.
+ *   w            device [n_out][k] bf16, 16-byte aligned (caller-owned).
+ *   n_out        a positive multiple of 16.
+ *   y            device [m][n_out] bf16, 4-byte aligned: each value the bf16 rounding of an
+ *                fp32 sum accumulated in a fixed order.
+ */
+mla_status_t mla_project(mla_handle_t h, const void* x, int32_t m, int32_t k, const void* w, int32_t n_out,
+                         void* y, mla_stream_t stream);
+
+/*
  * mla_decode_workspace_size -- bytes of device workspace mla_decode needs for
  * a batch of `batch` sequences of at most `max_ctx` tokens.  The workspace
  * holds the split plan, the absorbed queries and the split partials.

@@ -36,7 +36,8 @@ MLA_OPT_PROFILE = 2
 MLA_FIXED_SCRATCH_BYTES = 32 << 20     # include/mla.h: scratch of mla_decode_fixed_scratch
 
 EXPORTED = [
-    "mla_create", "mla_destroy", "mla_kv_append", "mla_decode_workspace_size", "mla_decode",
+    "mla_create", "mla_destroy", "mla_kv_append", "mla_kv_project_append", "mla_project",
+    "mla_decode_workspace_size", "mla_decode",
     "mla_decode_fixed_scratch",
     "mla_get_status", "mla_set_option", "mla_profile_read", "mla_profile_kernel_name",
     "mla_last_error", "mla_status_string",
@@ -76,6 +77,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_create.argtypes = [ctypes.POINTER(MlaConfig), vp, vp, vp, ctypes.POINTER(vp)]
     lib.mla_destroy.argtypes = [vp]
     lib.mla_kv_append.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, vp, i32, vp]
+    lib.mla_kv_project_append.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp, i32, i32, vp, i32, vp]
+    lib.mla_project.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp]
     lib.mla_decode_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
     lib.mla_decode.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, sz, vp, vp]
     lib.mla_decode_fixed_scratch.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, vp]
@@ -154,6 +157,17 @@ class Mla:
         bt_rows, bt_stride = int(block_table.shape[0]), int(block_table.shape[1])
         _check(self._lib.mla_kv_append(self._h, _ptr(rows), _ptr(seq), _ptr(pos), n, _ptr(block_table), bt_rows,
                                        bt_stride, _ptr(cache), int(num_pages), _stream(stream)))
+
+    def kv_project_append(self, x, w_dkv, seq, pos, block_table, cache, num_pages: int, stream=None) -> None:
+        n, hidden = int(x.shape[0]), int(x.shape[1])
+        bt_rows, bt_stride = int(block_table.shape[0]), int(block_table.shape[1])
+        _check(self._lib.mla_kv_project_append(self._h, _ptr(x), hidden, _ptr(w_dkv), _ptr(seq), _ptr(pos), n,
+                                               _ptr(block_table), bt_rows, bt_stride, _ptr(cache), int(num_pages),
+                                               _stream(stream)))
+
+    def project(self, x, w, y, stream=None) -> None:
+        m, k, n_out = int(x.shape[0]), int(x.shape[1]), int(w.shape[0])
+        _check(self._lib.mla_project(self._h, _ptr(x), m, k, _ptr(w), n_out, _ptr(y), _stream(stream)))
 
     def decode_workspace_size(self, batch: int, max_ctx: int) -> int:
         out = ctypes.c_size_t()

@@ -248,6 +248,52 @@ mla_status_t mla_kv_append(mla_handle_t hh, const void* rows, const int32_t* seq
   return MLA_OK;
 }
 
+mla_status_t mla_kv_project_append(mla_handle_t hh, const void* x, int32_t hidden, const void* w_dkv,
+                                   const int32_t* seq, const int32_t* pos, int32_t n, const int32_t* block_table,
+                                   int32_t bt_rows, int32_t bt_stride, void* cache, int32_t num_pages,
+                                   mla_stream_t stream) {
+  g_last_error.clear();
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  if (!h) return fail(MLA_ERR_INVALID_ARG, "mla_kv_project_append: handle is NULL");
+  if (n < 0) return fail(MLA_ERR_INVALID_ARG, "mla_kv_project_append: n = %d is negative", n);
+  if (hidden <= 0 || hidden % 256 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "mla_kv_project_append: hidden = %d must be a positive multiple of 256", hidden);
+  if (n == 0) return MLA_OK;
+  if (!x || !w_dkv || !seq || !pos || !block_table || !cache)
+    return fail(MLA_ERR_INVALID_ARG,
+                "mla_kv_project_append: a device pointer (x, w_dkv, seq, pos, block_table, cache) is NULL");
+  if (bt_rows <= 0 || bt_stride <= 0 || num_pages <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "mla_kv_project_append: bt_rows=%d bt_stride=%d num_pages=%d must be positive",
+                bt_rows, bt_stride, num_pages);
+  if (!aligned(x, 16) || !aligned(w_dkv, 16) || !aligned(cache, 16))
+    return fail(MLA_ERR_INVALID_ARG, "mla_kv_project_append: x, w_dkv and cache must be 16-byte aligned");
+  cudaError_t e = mla::launch_kv_project_append(*h, static_cast<const __nv_bfloat16*>(x), n, hidden,
+                                                static_cast<const __nv_bfloat16*>(w_dkv), seq, pos, block_table,
+                                                bt_rows, bt_stride, cache, num_pages,
+                                                reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_project_append launch");
+  return MLA_OK;
+}
+
+mla_status_t mla_project(mla_handle_t hh, const void* x, int32_t m, int32_t k, const void* w, int32_t n_out,
+                         void* y, mla_stream_t stream) {
+  g_last_error.clear();
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  if (!h) return fail(MLA_ERR_INVALID_ARG, "mla_project: handle is NULL");
+  if (m < 0) return fail(MLA_ERR_INVALID_ARG, "mla_project: m = %d is negative", m);
+  if (k <= 0 || k % 256 != 0) return fail(MLA_ERR_INVALID_ARG, "mla_project: k = %d must be a positive multiple of 256", k);
+  if (n_out <= 0 || n_out % 16 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "mla_project: n_out = %d must be a positive multiple of 16", n_out);
+  if (m == 0) return MLA_OK;
+  if (!x || !w || !y) return fail(MLA_ERR_INVALID_ARG, "mla_project: a device pointer (x, w, y) is NULL");
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 4))
+    return fail(MLA_ERR_INVALID_ARG, "mla_project: x and w must be 16-byte aligned, y 4-byte aligned");
+  cudaError_t e = mla::launch_project(static_cast<const __nv_bfloat16*>(x), m, k, static_cast<const __nv_bfloat16*>(w),
+                                      n_out, static_cast<__nv_bfloat16*>(y), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "project launch");
+  return MLA_OK;
+}
+
 mla_status_t mla_decode_workspace_size(mla_handle_t hh, int32_t batch, int32_t max_ctx, size_t* bytes) {
   g_last_error.clear();
   Handle* h = reinterpret_cast<Handle*>(hh);

@@ -10,33 +10,12 @@
 // 32 bytes (bf16) or 16 bytes (e4m3) out); lanes 0..3 also own RoPE values
 // [16 l, 16 l + 16) of the key.  HBM-bound: 1152 bytes read and 1152 (bf16) or
 // 576 (e4m3) bytes written per row.
-#include <cuda_fp8.h>
-
+#include "append_ops.cuh"
 #include "internal.cuh"
 #include "sm100_ptx.cuh"
 
 namespace mla {
 namespace {
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return (lo & 0xFFFFu) | (hi << 16);
-}
-
-// Rotate one interleaved pair by (cos, sin) with every product and sum rounded to fp32.
-__device__ __forceinline__ void rope_pair(float x0, float x1, float2 cs, float* o0, float* o1) {
-  *o0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
-  *o1 = __fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y));
-}
 
 template <bool kFp8>
 __global__ void __launch_bounds__(256) kv_append_kernel(

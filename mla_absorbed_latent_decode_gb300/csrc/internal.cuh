@@ -85,6 +85,14 @@ void clear_last_error();
 mla_status_t set_last_error(mla_status_t s, const char* msg);
 
 // Kernel launchers (each returns the launch error).
+// y[m][n_out] = bf16(x[m][k] . w[n_out][k]^T); k a multiple of 256, n_out of 16.
+cudaError_t launch_project(const __nv_bfloat16* x, int m, int k, const __nv_bfloat16* w, int n_out,
+                           __nv_bfloat16* y, cudaStream_t st);
+// rows = x[n][k] . w_dkv[576][k]^T written into the paged cache as mla_kv_append writes rows.
+cudaError_t launch_kv_project_append(const Handle& h, const __nv_bfloat16* x, int n, int k,
+                                     const __nv_bfloat16* w, const int32_t* seq, const int32_t* pos,
+                                     const int32_t* block_table, int bt_rows, int bt_stride, void* cache,
+                                     int num_pages, cudaStream_t st);
 cudaError_t launch_kv_append(const Handle& h, const __nv_bfloat16* rows, const int32_t* seq,
                              const int32_t* pos, int n, const int32_t* block_table, int bt_rows,
                              int bt_stride, void* cache, int num_pages, cudaStream_t st);
