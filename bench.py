@@ -64,10 +64,23 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+LAYER = "v2lite_layer"      # the V2-Lite layer step with its projections on the GPU
+
+
 def workload(name):
     from mla_absorbed_latent_decode_gb300 import workloads as W
+    if name == LAYER:
+        # x -> W_Q, W_DKV on the device (mla_project, mla_kv_project_append), then the decode;
+        # the workload's rows and query are placeholders until the CPU leg projects them
+        inp = W.v2lite_single_step_inputs(seed=0)
+        rows = np.zeros((inp["tokens"], W.D_C + W.D_ROPE), np.uint16)
+        q = np.zeros((inp["n_h"], W.D_NOPE + W.D_ROPE), np.uint16)
+        wl = W.v2lite_single_step(rows, q, inp["w_uk"], inp["w_uv"], n_h=inp["n_h"])
+        wl.name = LAYER
+        wl.extra["layer"] = inp
+        return wl
     if name not in W.NAMED:
-        raise SystemExit(f"unknown workload {name}; choose from {sorted(W.NAMED)}")
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(W.NAMED) + [LAYER]}")
     return W.NAMED[name]()
 
 
@@ -78,6 +91,10 @@ def algorithmic(wl):
     cache = tokens * (wl.d_c + wl.d_rope) * e
     weights = 2 * wl.n_h * 128 * 512 * 2
     flops = 2 * wl.n_h * tokens * (576 + 512) + 4 * wl.B * wl.n_h * 128 * 512
+    if "layer" in wl.extra:                            # + W_Q and W_DKV for the step's token
+        proj = (wl.n_h * (wl.d_nope + wl.d_rope) + wl.d_c + wl.d_rope) * wl.extra["layer"]["x"].shape[1]
+        weights += 2 * proj
+        flops += 2 * wl.B * proj
     return cache, weights, flops
 
 
@@ -92,6 +109,13 @@ def oracle_sample(wl, seconds):
     about `seconds` of CPU work; return (GB/s of latent cache processed, description)."""
     from oracle import mla_ref
     from oracle import e4m3
+    if "layer" in wl.extra and "projected" not in wl.extra:
+        inp = wl.extra["layer"]
+        c, kr, qq = mla_ref.project_inputs(mla_ref.bf16_to_f64(inp["x"]), mla_ref.bf16_to_f64(inp["w_dkv"]),
+                                           mla_ref.bf16_to_f64(inp["w_q"]), inp["n_h"], wl.d_c)
+        wl.rows = mla_ref.bf16_round(np.concatenate([c, kr], axis=1).astype(np.float32))
+        wl.q = mla_ref.bf16_round(qq[-1].astype(np.float32)).reshape(1, inp["n_h"], -1)
+        wl.extra["projected"] = True
     starts = np.concatenate([[0], np.cumsum(wl.ctx_len.astype(np.int64))])
     q = mla_ref.bf16_to_f64(wl.q)
     w_uk = mla_ref.bf16_to_f64(wl.w_uk)
@@ -255,8 +279,21 @@ def run_ours(args):
 
     wl = workload(args.workload)
     sess = DecodeSession(wl, device=str(dev))
-    sess.prefill()
-    rows, seq, pos = sess.step_inputs()
+    layer = "layer" in wl.extra
+    if layer:
+        inp = wl.extra["layer"]
+        T, qw = inp["tokens"], wl.n_h * (wl.d_nope + wl.d_rope)
+        x_all = bf16_tensor(inp["x"], dev)
+        w_q, w_dkv = bf16_tensor(inp["w_q"], dev), bf16_tensor(inp["w_dkv"], dev)
+        lseq = torch.zeros(T, dtype=torch.int32, device=dev)
+        lpos = torch.arange(T, dtype=torch.int32, device=dev)
+        sess.mla.kv_project_append(x_all[:T - 1], w_dkv, lseq[:T - 1], lpos[:T - 1], sess.block_table, sess.cache,
+                                   wl.num_pages)                              # the 25-token prefill
+        x_new = x_all[T - 1:]
+        q_new = torch.empty((1, qw), dtype=torch.bfloat16, device=dev)
+    else:
+        sess.prefill()
+        rows, seq, pos = sess.step_inputs()
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -271,8 +308,14 @@ def run_ours(args):
     sess.mla.set_option(B.MLA_OPT_PROFILE, 1)
 
     def step():
-        sess.append_step(rows, seq, pos)
-        sess.decode()
+        if layer:                     # the new token's q and cache row projected on the device
+            sess.mla.project(x_new, w_q, q_new)
+            sess.mla.kv_project_append(x_new, w_dkv, lseq[T - 1:], lpos[T - 1:], sess.block_table, sess.cache,
+                                       wl.num_pages)
+            sess.decode(q=q_new.view(1, wl.n_h, -1))
+        else:
+            sess.append_step(rows, seq, pos)
+            sess.decode()
 
     for _ in range(args.warmup):
         flush_l2()
@@ -327,9 +370,13 @@ def run_ours(args):
     # of several microseconds; five small ones cost more than the 3 MB of queries); each input
     # is a 256-byte aligned segment of the packed buffer
     last = wl.last_row_index()
-    parts = [("rows", wl.rows[last].view(np.int16)), ("seq", wl.row_seq[last].astype(np.int32)),
-             ("pos", wl.row_pos[last].astype(np.int32)), ("q", wl.q.view(np.int16)),
-             ("ctx", wl.ctx_len.astype(np.int32))]
+    if layer:                         # the step's input is the new token's hidden state
+        parts = [("x", inp["x"][T - 1:].view(np.int16)), ("seq", np.zeros(1, np.int32)),
+                 ("pos", np.array([T - 1], np.int32)), ("ctx", wl.ctx_len.astype(np.int32))]
+    else:
+        parts = [("rows", wl.rows[last].view(np.int16)), ("seq", wl.row_seq[last].astype(np.int32)),
+                 ("pos", wl.row_pos[last].astype(np.int32)), ("q", wl.q.view(np.int16)),
+                 ("ctx", wl.ctx_len.astype(np.int32))]
     offs, total = {}, 0
     for name, a in parts:
         offs[name] = total
@@ -349,10 +396,18 @@ def run_ours(args):
 
     def e2e_step():
         d_pack.copy_(h_pack, non_blocking=True)
-        sess.mla.kv_append(views["rows"].view(torch.bfloat16), views["seq"], views["pos"], sess.block_table,
-                           sess.cache, wl.num_pages)
-        sess.mla.decode(views["q"].view(torch.bfloat16), views["ctx"], wl.max_ctx, sess.block_table, sess.cache,
-                        wl.num_pages, sess.workspace, sess.out)
+        if layer:
+            xv = views["x"].view(torch.bfloat16)
+            sess.mla.project(xv, w_q, q_new)
+            sess.mla.kv_project_append(xv, w_dkv, views["seq"], views["pos"], sess.block_table, sess.cache,
+                                       wl.num_pages)
+            sess.mla.decode(q_new.view(1, wl.n_h, -1), views["ctx"], wl.max_ctx, sess.block_table, sess.cache,
+                            wl.num_pages, sess.workspace, sess.out)
+        else:
+            sess.mla.kv_append(views["rows"].view(torch.bfloat16), views["seq"], views["pos"], sess.block_table,
+                               sess.cache, wl.num_pages)
+            sess.mla.decode(views["q"].view(torch.bfloat16), views["ctx"], wl.max_ctx, sess.block_table,
+                            sess.cache, wl.num_pages, sess.workspace, sess.out)
         h_out.copy_(sess.out.view(torch.int16), non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -418,9 +473,12 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": cache_b},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s (latent KV)", "ms_per_step": round(e2e, 5),
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-            "gpu_launches": args.steps * (1 + len(kernel_ms[0])),
+            "gpu_launches": args.steps * ((2 if layer else 1) + len(kernel_ms[0])),
             "clocks": clock_info,
         }
+        if layer:
+            line["config"]["projections"] = ("the new token's q = x . W_Q and cache row = x . W_DKV computed on "
+                                             "the device (mla_project, mla_kv_project_append) inside the step")
         if world == 1 and not args.no_cpu_baseline:
             g, el, desc = oracle_sample(wl, args.cpu_seconds)
             line["cpu_baseline"] = {"value": round(g, 4), "unit": "GB/s (latent KV)", "cores": blas_threads(),
