@@ -199,7 +199,8 @@ class ClockSampler:
 
     def __init__(self, gpu_index):
         self.proc, self.gpu = None, gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        out_dir = os.environ.get("MLA_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"mla_bench_clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
