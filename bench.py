@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--workload", default="v3_b64_s4096_bf16")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--naive-ab", action="store_true",
+                    help="also time the standard-mode decode over the expanded per-head cache (bf16 cache only)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU seconds of the oracle baseline sample")
     return ap.parse_args()
 
@@ -426,6 +428,7 @@ def run_ours(args):
         s1.synchronize()
         e2e_ms.append(s0.elapsed_time(s1))
     e2e = statistics.mean(e2e_ms)
+    naive = naive_ab(args, wl, sess, flush_l2, stream) if args.naive_ab and not layer else None
 
     # max over ranks
     t = torch.tensor([ms, e2e, warm], dtype=torch.float64, device=dev)
@@ -481,6 +484,11 @@ def run_ours(args):
         if layer:
             line["config"]["projections"] = ("the new token's q = x . W_Q and cache row = x . W_DKV computed on "
                                              "the device (mla_project, mla_kv_project_append) inside the step")
+        if naive is not None:
+            naive["absorbed_step_us"] = round(ms * 1000.0, 2)
+            naive["naive_over_absorbed"] = round(naive["decode_us"] / (ms * 1000.0), 2)
+            naive["frac_of_hbm"] = round(naive["gbs"] / hbm, 4)
+            line["naive_ab"] = naive
         if world == 1 and not args.no_cpu_baseline:
             g, el, desc = oracle_sample(wl, args.cpu_seconds)
             line["cpu_baseline"] = {"value": round(g, 4), "unit": "GB/s (latent KV)", "cores": blas_threads(),
@@ -490,6 +498,52 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def naive_ab(args, wl, sess, flush_l2, stream):
+    """Standard-mode decode of the same batch: the latent cache expanded once into per-head keys
+    [W_UK c ; k_r] and values W_UV c (mla_expand_kv, untimed), then K decode calls over it
+    (mla_decode_naive), L2 flushed between calls.  The bytes it must read per call are
+    B * s_ctx * n_h * (d_nope + d_rope + d_v) * 2 -- the per-token cache of a standard MHA."""
+    import torch
+    if wl.cache_dtype != 1:
+        return None
+    mla = sess.mla
+    kvx = torch.empty((wl.num_pages, wl.page_size, wl.n_h, wl.d_nope + wl.d_rope + wl.d_v), dtype=torch.bfloat16,
+                      device=sess.cache.device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    mla.expand_kv(sess.cache, wl.num_pages, kvx)
+    e1.record(stream)
+    ws = torch.empty(mla.decode_naive_workspace_size(wl.B, wl.max_ctx), dtype=torch.uint8, device=kvx.device)
+    out = torch.empty_like(sess.out)
+
+    def call():
+        mla.decode_naive(sess.q, sess.ctx_len, wl.max_ctx, sess.block_table, kvx, wl.num_pages, ws, out)
+    for _ in range(max(3, args.warmup)):
+        flush_l2()
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush_l2()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        call()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        times.append(s0.elapsed_time(s1))
+    if sess.status() != 0:
+        raise SystemExit("device check word set during the standard-mode decode")
+    us = statistics.mean(times) * 1000.0
+    xbytes = wl.total_tokens * wl.n_h * (wl.d_nope + wl.d_rope + wl.d_v) * 2
+    res = {"decode_us": round(us, 2), "expanded_bytes_per_step": int(xbytes), "gbs": round(xbytes / (us * 1e3), 1),
+           "expand_ms_once": round(e0.elapsed_time(e1), 2),
+           "note": "standard-mode decode (expanded per-head K/V, no absorption) over the same batch; "
+                   "decode call only, L2 flushed between calls"}
+    del kvx
+    torch.cuda.empty_cache()
+    return res
 
 
 def main():

@@ -191,6 +191,41 @@ mla_status_t mla_project(mla_handle_t h, const void* x, int32_t m, int32_t k, co
                          void* y, mla_stream_t stream);
 
 /*
+ * mla_expand_kv -- the standard-mode (naive) cache of an MLA layer, for comparison with the
+ * absorbed path ("80 行 PyTorch 从零写 DeepSeek 的 MLA" §3/§5: the naive mode caches each
+ * head's key and value; "DeepSeek-V2-Lite 真实权重执行审计" §3.2: 10,240 bytes per token at
+ * 16 heads against 1,152 for the latent row).
+ *
+ * For every slot of every page: key_h = [W_UK[h] c ; k_r] (d_nope + d_rope) and value_h =
+ * W_UV[h] c (d_v), each product an fp32 sum rounded to bf16, k_r copied as cached (already
+ * rotated).  Slots that hold no token produce values nobody reads.
+ *
+ *   cache        device, a bf16 cache as written by mla_kv_append (an FP8 cache is
+ *                MLA_ERR_UNSUPPORTED), 16-byte aligned.
+ *   num_pages    pages of cache (and of kvx).
+ *   kvx          device [num_pages][page_size][n_h][d_nope + d_rope + d_v] bf16, 16-byte aligned.
+ */
+mla_status_t mla_expand_kv(mla_handle_t h, const void* cache, int32_t num_pages, void* kvx, mla_stream_t stream);
+
+/* mla_decode_naive_workspace_size -- device workspace bytes of mla_decode_naive. */
+mla_status_t mla_decode_naive_workspace_size(mla_handle_t h, int32_t batch, int32_t max_ctx, size_t* bytes);
+
+/*
+ * mla_decode_naive -- standard-mode decode over the expanded cache: per sequence and head,
+ * o_h = sum_t softmax_t(q_h . key_h,t * scale) value_h,t with q_h = [q_nope ; RoPE(q_pe,
+ * ctx_len - 1)] -- the same function as mla_decode (the pages' naive = absorbed identity),
+ * computed without absorption, reading n_h (d_nope + d_rope + d_v) values per token.
+ *
+ * Arguments as in mla_decode, with kvx (from mla_expand_kv, same block table and page ids) in
+ * place of the latent cache; out is [batch][n_h][d_v] bf16.  Split-KV over 256-token pieces
+ * merged by log-sum-exp.  Device checks as in mla_decode (bad lengths and page ids zero that
+ * sequence's output and set the check word).
+ */
+mla_status_t mla_decode_naive(mla_handle_t h, const void* q, const int32_t* ctx_len, int32_t batch, int32_t max_ctx,
+                              const int32_t* block_table, int32_t bt_stride, const void* kvx, int32_t num_pages,
+                              void* workspace, size_t workspace_bytes, void* out, mla_stream_t stream);
+
+/*
  * mla_decode_workspace_size -- bytes of device workspace mla_decode needs for
  * a batch of `batch` sequences of at most `max_ctx` tokens.  The workspace
  * holds the split plan, the absorbed queries and the split partials.

@@ -37,6 +37,7 @@ MLA_FIXED_SCRATCH_BYTES = 32 << 20     # include/mla.h: scratch of mla_decode_fi
 
 EXPORTED = [
     "mla_create", "mla_destroy", "mla_kv_append", "mla_kv_project_append", "mla_project",
+    "mla_expand_kv", "mla_decode_naive_workspace_size", "mla_decode_naive",
     "mla_decode_workspace_size", "mla_decode",
     "mla_decode_fixed_scratch",
     "mla_get_status", "mla_set_option", "mla_profile_read", "mla_profile_kernel_name",
@@ -79,6 +80,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_kv_append.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, vp, i32, vp]
     lib.mla_kv_project_append.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp, i32, i32, vp, i32, vp]
     lib.mla_project.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp]
+    lib.mla_expand_kv.argtypes = [vp, vp, i32, vp, vp]
+    lib.mla_decode_naive_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
+    lib.mla_decode_naive.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, sz, vp, vp]
     lib.mla_decode_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
     lib.mla_decode.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, sz, vp, vp]
     lib.mla_decode_fixed_scratch.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, vp]
@@ -168,6 +172,22 @@ class Mla:
     def project(self, x, w, y, stream=None) -> None:
         m, k, n_out = int(x.shape[0]), int(x.shape[1]), int(w.shape[0])
         _check(self._lib.mla_project(self._h, _ptr(x), m, k, _ptr(w), n_out, _ptr(y), _stream(stream)))
+
+    def expand_kv(self, cache, num_pages: int, kvx, stream=None) -> None:
+        _check(self._lib.mla_expand_kv(self._h, _ptr(cache), int(num_pages), _ptr(kvx), _stream(stream)))
+
+    def decode_naive_workspace_size(self, batch: int, max_ctx: int) -> int:
+        out = ctypes.c_size_t()
+        _check(self._lib.mla_decode_naive_workspace_size(self._h, int(batch), int(max_ctx), ctypes.byref(out)))
+        return int(out.value)
+
+    def decode_naive(self, q, ctx_len, max_ctx: int, block_table, kvx, num_pages: int, workspace, out,
+                     stream=None) -> None:
+        batch = int(ctx_len.shape[0])
+        ws_bytes = int(workspace.numel() * workspace.element_size())
+        _check(self._lib.mla_decode_naive(self._h, _ptr(q), _ptr(ctx_len), batch, int(max_ctx), _ptr(block_table),
+                                          int(block_table.shape[1]), _ptr(kvx), int(num_pages), _ptr(workspace),
+                                          ws_bytes, _ptr(out), _stream(stream)))
 
     def decode_workspace_size(self, batch: int, max_ctx: int) -> int:
         out = ctypes.c_size_t()

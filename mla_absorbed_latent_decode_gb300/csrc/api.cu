@@ -294,6 +294,63 @@ mla_status_t mla_project(mla_handle_t hh, const void* x, int32_t m, int32_t k, c
   return MLA_OK;
 }
 
+mla_status_t mla_expand_kv(mla_handle_t hh, const void* cache, int32_t num_pages, void* kvx, mla_stream_t stream) {
+  g_last_error.clear();
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  if (!h) return fail(MLA_ERR_INVALID_ARG, "mla_expand_kv: handle is NULL");
+  if (h->cfg.cache_dtype != MLA_CACHE_BF16)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_expand_kv: only a bf16 cache can be expanded");
+  if (num_pages <= 0) return fail(MLA_ERR_INVALID_ARG, "mla_expand_kv: num_pages = %d must be positive", num_pages);
+  if (!cache || !kvx) return fail(MLA_ERR_INVALID_ARG, "mla_expand_kv: cache or kvx is NULL");
+  if (!aligned(cache, 16) || !aligned(kvx, 16))
+    return fail(MLA_ERR_INVALID_ARG, "mla_expand_kv: cache and kvx must be 16-byte aligned");
+  cudaError_t e = mla::launch_expand_kv(*h, cache, num_pages, kvx, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "expand_kv launch");
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_naive_workspace_size(mla_handle_t hh, int32_t batch, int32_t max_ctx, size_t* bytes) {
+  g_last_error.clear();
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  if (!h) return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive_workspace_size: handle is NULL");
+  if (!bytes) return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive_workspace_size: bytes is NULL");
+  if (batch <= 0) return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive_workspace_size: batch = %d must be positive", batch);
+  if (max_ctx <= 0 || max_ctx > h->cfg.max_position)
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive_workspace_size: max_ctx = %d must be in [1, max_position=%d]",
+                max_ctx, h->cfg.max_position);
+  *bytes = mla::naive_workspace_bytes(h->cfg.n_h, batch, max_ctx);
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_naive(mla_handle_t hh, const void* q, const int32_t* ctx_len, int32_t batch, int32_t max_ctx,
+                              const int32_t* block_table, int32_t bt_stride, const void* kvx, int32_t num_pages,
+                              void* workspace, size_t workspace_bytes, void* out, mla_stream_t stream) {
+  g_last_error.clear();
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  if (!h) return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive: handle is NULL");
+  if (batch <= 0) return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive: batch = %d must be positive", batch);
+  if (max_ctx <= 0 || max_ctx > h->cfg.max_position)
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive: max_ctx = %d must be in [1, max_position=%d]", max_ctx,
+                h->cfg.max_position);
+  if (!q || !ctx_len || !block_table || !kvx || !workspace || !out)
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive: a device pointer is NULL");
+  const int need_pages = (max_ctx + mla::kPage - 1) / mla::kPage;
+  if (bt_stride < need_pages)
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive: bt_stride = %d holds fewer than the %d pages of max_ctx = %d",
+                bt_stride, need_pages, max_ctx);
+  if (num_pages <= 0) return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive: num_pages = %d must be positive", num_pages);
+  if (!aligned(q, 16) || !aligned(kvx, 16) || !aligned(out, 16))
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode_naive: q, kvx and out must be 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(MLA_ERR_WORKSPACE, "mla_decode_naive: workspace must be 256-byte aligned");
+  const size_t need = mla::naive_workspace_bytes(h->cfg.n_h, batch, max_ctx);
+  if (workspace_bytes < need)
+    return fail(MLA_ERR_WORKSPACE, "mla_decode_naive: workspace has %zu bytes, %zu needed", workspace_bytes, need);
+  cudaError_t e = mla::launch_decode_naive(*h, q, ctx_len, batch, max_ctx, block_table, bt_stride, kvx, num_pages,
+                                           workspace, out, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode_naive launch");
+  return MLA_OK;
+}
+
 mla_status_t mla_decode_workspace_size(mla_handle_t hh, int32_t batch, int32_t max_ctx, size_t* bytes) {
   g_last_error.clear();
   Handle* h = reinterpret_cast<Handle*>(hh);

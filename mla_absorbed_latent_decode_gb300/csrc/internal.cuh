@@ -85,6 +85,12 @@ void clear_last_error();
 mla_status_t set_last_error(mla_status_t s, const char* msg);
 
 // Kernel launchers (each returns the launch error).
+// Standard-mode (expanded) decode: the per-head key/value cache and its decode.
+size_t naive_workspace_bytes(int n_h, int batch, int max_ctx);
+cudaError_t launch_expand_kv(const Handle& h, const void* cache, int num_pages, void* kvx, cudaStream_t st);
+cudaError_t launch_decode_naive(const Handle& h, const void* q, const int32_t* ctx_len, int batch, int max_ctx,
+                                const int32_t* block_table, int bt_stride, const void* kvx, int num_pages,
+                                void* workspace, void* out, cudaStream_t st);
 // y[m][n_out] = bf16(x[m][k] . w[n_out][k]^T); k a multiple of 256, n_out of 16.
 cudaError_t launch_project(const __nv_bfloat16* x, int m, int k, const __nv_bfloat16* w, int n_out,
                            __nv_bfloat16* y, cudaStream_t st);
