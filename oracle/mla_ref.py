@@ -239,6 +239,47 @@ def causal_forward_naive(x, w_dkv, w_q, w_uk, w_uv, scale, base):
 
 
 # ---------------------------------------------------------------------------
+# prefill of a chunk of queries over the cached rows
+# ---------------------------------------------------------------------------
+
+def prefill_naive(q, c_kv, k_r_rot, w_uk, w_uv, pos0, scale, base):
+    """Causal prefill of ``n_q`` query tokens in standard (MHA) mode over a sequence's rows.
+
+    "G5 MLA KV 访存建模设计规格", 名词定义 and 用例 2: prefill handles every prompt
+    token in one pass (query length = prompt length) and is compute-bound;
+    "DeepSeek MLA 吸收式缓存：真实权重执行与 FlashMLA 架构边界" §6.1: dense prefill
+    runs in MHA mode, i.e. with the latent expanded per head (§2.1):
+
+        k_{h,t} = [ W_UK[h] c_t ; k_r,t ],   v_{h,t} = W_UV[h] c_t
+        q_{h,i} = [ q_nope,h,i ; RoPE(q_pe,h,i, pos0 + i) ]
+        o_{h,i} = sum_{t <= pos0 + i} softmax_t(scale * q_{h,i} . k_{h,t}) v_{h,t}
+
+    Query i sits at position ``pos0 + i`` and sees the rows ``0 .. pos0 + i`` (a
+    chunk after a cached prefix of ``pos0`` rows; ``pos0 = 0`` is a whole prompt).
+    The full masked score matrix is formed per head.  Shapes: q [n_q, n_h, d_q],
+    c_kv [T, d_c], k_r_rot [T, d_rope] (rotated at their positions) with
+    T >= pos0 + n_q.  Returns [n_q, n_h, d_v].
+    """
+    q = np.asarray(q, np.float64)
+    n_q = q.shape[0]
+    T = pos0 + n_q
+    c_kv = np.asarray(c_kv, np.float64)[:T]
+    k_r_rot = np.asarray(k_r_rot, np.float64)[:T]
+    n_h, d_nope, _ = w_uk.shape
+    qpos = pos0 + np.arange(n_q)
+    q_pe = rope(q[:, :, d_nope:], qpos[:, None], base)          # [n_q, n_h, d_rope]
+    visible = np.arange(T)[None, :] <= qpos[:, None]             # [n_q, T]
+    out = np.empty((n_q, n_h, w_uv.shape[1]))
+    for h in range(n_h):
+        k = np.concatenate([c_kv @ np.asarray(w_uk[h], np.float64).T, k_r_rot], axis=1)   # [T, d_q]
+        v = c_kv @ np.asarray(w_uv[h], np.float64).T                                     # [T, d_v]
+        qh = np.concatenate([q[:, h, :d_nope], q_pe[:, h]], axis=1)                      # [n_q, d_q]
+        s = np.where(visible, scale * (qh @ k.T), -np.inf)
+        out[:, h] = softmax(s, axis=1) @ v
+    return out
+
+
+# ---------------------------------------------------------------------------
 # the paged latent cache (stored values of a row)
 # ---------------------------------------------------------------------------
 

@@ -182,6 +182,39 @@ def pin_one_shot_equals_incremental(ref):
     assert np.max(np.abs(nv - full[L - 1])) <= 1e-12
 
 
+def pin_prefill_rows_are_decodes(ref):
+    """A causal prefill chunk is the per-position decode of each of its queries: row i of a
+    chunk after a prefix of pos0 rows is the decode (naive and absorbed) of query i over the
+    rows 0 .. pos0 + i; a whole prompt (pos0 = 0) is the one-shot causal forward; and a prompt
+    prefilled in two chunks gives the rows of the single pass."""
+    n_h, T, pos0 = 3, 11, 6
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((T, n_h, 8))
+    _, c, kr, w_uk, w_uv = _tiny_problem(22, T=T)
+    kr_rot = ref.rope(kr, np.arange(T), BASE)
+    s = ref.default_scale(4, 4)
+    chunk = ref.prefill_naive(q[pos0:], c, kr_rot, w_uk, w_uv, pos0, s, BASE)
+    assert chunk.shape == (T - pos0, n_h, 5)
+    for i in range(T - pos0):
+        p = pos0 + i
+        nv = ref.naive_decode(q[p], c[:p + 1], kr_rot[:p + 1], w_uk, w_uv, p, s, BASE)
+        ab = ref.absorbed_decode(q[p], c[:p + 1], kr_rot[:p + 1], w_uk, w_uv, p, s, BASE)
+        assert np.max(np.abs(chunk[i] - nv)) <= 1e-13 and np.max(np.abs(chunk[i] - ab)) <= 1e-12
+    whole = ref.prefill_naive(q, c, kr_rot, w_uk, w_uv, 0, s, BASE)
+    assert np.max(np.abs(whole[pos0:] - chunk)) <= 1e-13
+    head = ref.prefill_naive(q[:pos0], c, kr_rot, w_uk, w_uv, 0, s, BASE)
+    assert np.max(np.abs(whole[:pos0] - head)) <= 1e-13
+    # from hidden states: the one-shot causal forward of the projected prompt
+    L, hidden = 9, 32
+    x = rng.standard_normal((L, hidden))
+    w_dkv = rng.standard_normal((10, hidden)) * 0.3
+    w_q = rng.standard_normal((n_h * 8, hidden)) * 0.3
+    cx, krx, qx = ref.project_inputs(x, w_dkv, w_q, n_h, 6)
+    pre = ref.prefill_naive(qx, cx, ref.rope(krx, np.arange(L), BASE), w_uk, w_uv, 0, s, BASE)
+    one = ref.causal_forward_naive(x, w_dkv, w_q, w_uk, w_uv, s, BASE)
+    assert np.max(np.abs(pre - one)) <= 1e-12
+
+
 # --------------------------------------------------------------------------- bytes
 
 def pin_cache_bytes(ref):
@@ -234,6 +267,6 @@ def pin_mha_ratio_and_read_bytes(ref):
 ALL_PINS = [
     pin_rope_closed_forms, pin_rope_relative_position, pin_scale_worked_example,
     pin_naive_equals_absorbed, pin_rope_on_content_breaks_absorption, pin_closed_forms,
-    pin_split_lse_identity, pin_one_shot_equals_incremental, pin_cache_bytes,
+    pin_split_lse_identity, pin_one_shot_equals_incremental, pin_prefill_rows_are_decodes, pin_cache_bytes,
     pin_mha_ratio_and_read_bytes,
 ]

@@ -84,6 +84,25 @@ def _split_linear_merge(q_abs, c_kv, k_r_rot, scale, bounds):
     return sum(w[j][:, None] * parts[j][0] for j in range(len(parts))), np.log(np.exp(np.stack([p[1] for p in parts])).sum(0))
 
 
+def _prefill_with(strict_mask=False, chunk_position=False):
+    def prefill(q, c_kv, k_r_rot, w_uk, w_uv, pos0, scale, base):
+        q = np.asarray(q, np.float64)
+        n_q, T = q.shape[0], pos0 + q.shape[0]
+        n_h, d_nope, _ = w_uk.shape
+        qpos = pos0 + np.arange(n_q)
+        q_pe = mla_ref.rope(q[:, :, d_nope:], (np.full(n_q, pos0) if chunk_position else qpos)[:, None], base)
+        visible = (np.arange(T)[None, :] < qpos[:, None]) if strict_mask else (np.arange(T)[None, :] <= qpos[:, None])
+        visible[:, 0] = True                     # keep every row defined
+        out = np.empty((n_q, n_h, w_uv.shape[1]))
+        for h in range(n_h):
+            k = np.concatenate([c_kv[:T] @ w_uk[h].T, k_r_rot[:T]], axis=1)
+            qh = np.concatenate([q[:, h, :d_nope], q_pe[:, h]], axis=1)
+            s = np.where(visible, scale * (qh @ k.T), -np.inf)
+            out[:, h] = _orig["softmax"](s, axis=1) @ (c_kv[:T] @ w_uv[h].T)
+        return out
+    return prefill
+
+
 MUTATIONS = {
     "rope_rotates_backwards": ("rope", _rope_with(sign=-1.0)),
     "rope_frequency_step_1": ("rope", _rope_with(freq_step=1)),
@@ -94,6 +113,8 @@ MUTATIONS = {
     "naive_drops_rope_key": ("naive_decode", _naive_without_rope_key),
     "softmax_unnormalised": ("softmax", _softmax_unnormalised),
     "causal_mask_missing": ("causal_forward_naive", _causal_unmasked),
+    "prefill_mask_excludes_diagonal": ("prefill_naive", _prefill_with(strict_mask=True)),
+    "prefill_queries_rotated_at_chunk_start": ("prefill_naive", _prefill_with(chunk_position=True)),
     "cache_bytes_without_rope": ("absorb_cache_bytes", lambda t, d_c, d_r, e: int(t) * int(d_c) * int(e)),
     "naive_bytes_without_values": ("naive_cache_bytes", lambda t, n, dn, dr, dv, e: int(t) * int(n) * (int(dn) + int(dr)) * int(e)),
     "read_bytes_times_heads": ("decode_kv_read_bytes", lambda B, s, d_c, d_r, e: _orig["decode_kv_read_bytes"](B, s, d_c, d_r, e) * 2),
