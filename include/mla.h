@@ -225,6 +225,46 @@ mla_status_t mla_decode_naive(mla_handle_t h, const void* q, const int32_t* ctx_
                               const int32_t* block_table, int32_t bt_stride, const void* kvx, int32_t num_pages,
                               void* workspace, size_t workspace_bytes, void* out, mla_stream_t stream);
 
+/* mla_prefill_workspace_size -- device workspace bytes of mla_prefill:
+ * batch * round_up(max_ctx, 128) * (2 n_h d_nope + d_rope) * 2 (the expanded keys and values). */
+mla_status_t mla_prefill_workspace_size(mla_handle_t h, int32_t batch, int32_t max_ctx, size_t* bytes);
+
+/*
+ * mla_prefill -- causal prefill of a chunk of query tokens per sequence over the sequence's
+ * cached rows, in MHA mode ("G5 MLA KV 访存建模设计规格", 名词定义 and 用例 2: prefill takes
+ * every prompt token at once and is compute-bound; "DeepSeek MLA 吸收式缓存：真实权重执行与
+ * FlashMLA 架构边界" §6.1: FlashMLA's dense prefill runs in MHA mode).
+ *
+ * The chunk's rows must already be in the cache (mla_kv_append / mla_kv_project_append).  Query
+ * i of sequence b is at position ctx_len[b] - q_len[b] + i and attends the cached rows 0 .. that
+ * position:  o_h = sum_t softmax_t(scale q_h . [W_UK[h] c_t ; k_r,t]) W_UV[h] c_t,  q_h =
+ * [q_nope ; RoPE(q_pe, position)].  A whole prompt is q_len = ctx_len; a chunk after a cached
+ * prefix is q_len < ctx_len.  Keys and values are expanded per head into the workspace (bf16
+ * values of fp32 sums), then attention runs on the tensor cores: fp32 scores and sums, bf16 P.
+ *
+ *   q            device [total_q][n_h][d_nope + d_rope] bf16, 16-byte aligned, unrotated (as in
+ *                mla_decode); the rows of sequence b are q_start[b] .. q_start[b] + q_len[b] - 1.
+ *   q_start      device [batch] int32: first query row of each sequence.
+ *   q_len        device [batch] int32: query tokens of each sequence, 0 <= q_len <= ctx_len and
+ *                q_len <= max_q.
+ *   total_q      rows of q and out (>= 1).
+ *   max_q        host bound on q_len, 1 <= max_q <= max_ctx (sets the grid).
+ *   ctx_len, batch, max_ctx, block_table, bt_stride, num_pages: as in mla_decode.
+ *   cache        device, a bf16 cache (an FP8 cache is MLA_ERR_UNSUPPORTED), 128-byte aligned.
+ *   workspace    device, >= mla_prefill_workspace_size bytes, 256-byte aligned; overwritten.
+ *   out          device [total_q][n_h][d_v] bf16, 16-byte aligned: row q_start[b] + i is the
+ *                output of query i of sequence b; other rows are not written.
+ *
+ * Device checks (mla_get_status): a sequence whose q_start / q_len do not fit [0, total_q)
+ * or exceed max_q sets MLA_CHECK_CTX_LEN and writes nothing; one whose ctx_len is outside
+ * [1, max_ctx] or below q_len sets MLA_CHECK_CTX_LEN and gets zero rows; a page id outside
+ * [0, num_pages) in the pages its queries see sets MLA_CHECK_PAGE_ID and zeroes those rows.
+ */
+mla_status_t mla_prefill(mla_handle_t h, const void* q, const int32_t* q_start, const int32_t* q_len,
+                         int32_t total_q, int32_t max_q, const int32_t* ctx_len, int32_t batch, int32_t max_ctx,
+                         const int32_t* block_table, int32_t bt_stride, const void* cache, int32_t num_pages,
+                         void* workspace, size_t workspace_bytes, void* out, mla_stream_t stream);
+
 /*
  * mla_decode_workspace_size -- bytes of device workspace mla_decode needs for
  * a batch of `batch` sequences of at most `max_ctx` tokens.  The workspace

@@ -38,6 +38,7 @@ MLA_FIXED_SCRATCH_BYTES = 32 << 20     # include/mla.h: scratch of mla_decode_fi
 EXPORTED = [
     "mla_create", "mla_destroy", "mla_kv_append", "mla_kv_project_append", "mla_project",
     "mla_expand_kv", "mla_decode_naive_workspace_size", "mla_decode_naive",
+    "mla_prefill_workspace_size", "mla_prefill",
     "mla_decode_workspace_size", "mla_decode",
     "mla_decode_fixed_scratch",
     "mla_get_status", "mla_set_option", "mla_profile_read", "mla_profile_kernel_name",
@@ -83,6 +84,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_expand_kv.argtypes = [vp, vp, i32, vp, vp]
     lib.mla_decode_naive_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
     lib.mla_decode_naive.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, sz, vp, vp]
+    lib.mla_prefill_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
+    lib.mla_prefill.argtypes = [vp, vp, vp, vp, i32, i32, vp, i32, i32, vp, i32, vp, i32, vp, sz, vp, vp]
     lib.mla_decode_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
     lib.mla_decode.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, sz, vp, vp]
     lib.mla_decode_fixed_scratch.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, vp]
@@ -188,6 +191,19 @@ class Mla:
         _check(self._lib.mla_decode_naive(self._h, _ptr(q), _ptr(ctx_len), batch, int(max_ctx), _ptr(block_table),
                                           int(block_table.shape[1]), _ptr(kvx), int(num_pages), _ptr(workspace),
                                           ws_bytes, _ptr(out), _stream(stream)))
+
+    def prefill_workspace_size(self, batch: int, max_ctx: int) -> int:
+        out = ctypes.c_size_t()
+        _check(self._lib.mla_prefill_workspace_size(self._h, int(batch), int(max_ctx), ctypes.byref(out)))
+        return int(out.value)
+
+    def prefill(self, q, q_start, q_len, max_q: int, ctx_len, max_ctx: int, block_table, cache, num_pages: int,
+                workspace, out, stream=None) -> None:
+        batch, total_q = int(ctx_len.shape[0]), int(q.shape[0])
+        ws_bytes = int(workspace.numel() * workspace.element_size())
+        _check(self._lib.mla_prefill(self._h, _ptr(q), _ptr(q_start), _ptr(q_len), total_q, int(max_q), _ptr(ctx_len),
+                                     batch, int(max_ctx), _ptr(block_table), int(block_table.shape[1]), _ptr(cache),
+                                     int(num_pages), _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
 
     def decode_workspace_size(self, batch: int, max_ctx: int) -> int:
         out = ctypes.c_size_t()

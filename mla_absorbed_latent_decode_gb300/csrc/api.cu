@@ -351,6 +351,57 @@ mla_status_t mla_decode_naive(mla_handle_t hh, const void* q, const int32_t* ctx
   return MLA_OK;
 }
 
+mla_status_t mla_prefill_workspace_size(mla_handle_t hh, int32_t batch, int32_t max_ctx, size_t* bytes) {
+  g_last_error.clear();
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  if (!h) return fail(MLA_ERR_INVALID_ARG, "mla_prefill_workspace_size: handle is NULL");
+  if (!bytes) return fail(MLA_ERR_INVALID_ARG, "mla_prefill_workspace_size: bytes is NULL");
+  if (batch <= 0) return fail(MLA_ERR_INVALID_ARG, "mla_prefill_workspace_size: batch = %d must be positive", batch);
+  if (max_ctx <= 0 || max_ctx > h->cfg.max_position)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill_workspace_size: max_ctx = %d must be in [1, max_position=%d]",
+                max_ctx, h->cfg.max_position);
+  *bytes = mla::prefill_workspace_bytes(h->cfg.n_h, batch, max_ctx);
+  return MLA_OK;
+}
+
+mla_status_t mla_prefill(mla_handle_t hh, const void* q, const int32_t* q_start, const int32_t* q_len, int32_t total_q,
+                         int32_t max_q, const int32_t* ctx_len, int32_t batch, int32_t max_ctx,
+                         const int32_t* block_table, int32_t bt_stride, const void* cache, int32_t num_pages,
+                         void* workspace, size_t workspace_bytes, void* out, mla_stream_t stream) {
+  g_last_error.clear();
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  if (!h) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: handle is NULL");
+  if (h->cfg.cache_dtype != MLA_CACHE_BF16)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: only a bf16 cache is supported");
+  if (batch <= 0) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: batch = %d must be positive", batch);
+  if (max_ctx <= 0 || max_ctx > h->cfg.max_position)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: max_ctx = %d must be in [1, max_position=%d]", max_ctx,
+                h->cfg.max_position);
+  if (max_q <= 0 || max_q > max_ctx)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: max_q = %d must be in [1, max_ctx=%d]", max_q, max_ctx);
+  if (total_q <= 0) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: total_q = %d must be positive", total_q);
+  if (!q || !q_start || !q_len || !ctx_len || !block_table || !cache || !workspace || !out)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: a device pointer is NULL");
+  const int need_pages = (max_ctx + mla::kPage - 1) / mla::kPage;
+  if (bt_stride < need_pages)
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: bt_stride = %d holds fewer than the %d pages of max_ctx = %d",
+                bt_stride, need_pages, max_ctx);
+  if (num_pages <= 0) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: num_pages = %d must be positive", num_pages);
+  const long long rows = (long long)batch * h->cfg.n_h * ((max_ctx + 127) / 128 * 128);
+  if (rows >= (1LL << 31))
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: batch x n_h x max_ctx = %lld expanded rows exceed 2^31", rows);
+  if (!aligned(q, 16) || !aligned(cache, 128) || !aligned(out, 16))
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: q and out must be 16-byte aligned, cache 128-byte aligned");
+  if (!aligned(workspace, 256)) return fail(MLA_ERR_WORKSPACE, "mla_prefill: workspace must be 256-byte aligned");
+  const size_t need = mla::prefill_workspace_bytes(h->cfg.n_h, batch, max_ctx);
+  if (workspace_bytes < need)
+    return fail(MLA_ERR_WORKSPACE, "mla_prefill: workspace has %zu bytes, %zu needed", workspace_bytes, need);
+  cudaError_t e = mla::launch_prefill(*h, q, q_start, q_len, total_q, max_q, ctx_len, batch, max_ctx, block_table,
+                                      bt_stride, cache, num_pages, workspace, out, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return MLA_OK;
+}
+
 mla_status_t mla_decode_workspace_size(mla_handle_t hh, int32_t batch, int32_t max_ctx, size_t* bytes) {
   g_last_error.clear();
   Handle* h = reinterpret_cast<Handle*>(hh);

@@ -794,10 +794,9 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch,
 }
 }  // namespace
 
-// Decode-kernel dispatch: the tensor-core kernel, with in-shared-memory e4m3 -> bf16
-// conversion for an FP8 cache.
-cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table,
-                          int bt_stride, const void* cache, int num_pages, const Workspace& ws, cudaStream_t st) {
+// TMA descriptors of a cache (64- and 32-column boxes of one page), rebuilt only when the
+// cache pointer or its page count changes.
+cudaError_t cache_maps(const Handle& h, const void* cache, int num_pages) {
   const bool fp8 = h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3;
   Handle& hm = const_cast<Handle&>(h);
   if (hm.tmap_cache != cache || hm.tmap_pages != num_pages) {
@@ -810,8 +809,18 @@ cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, co
     hm.tmap_cache = cache;
     hm.tmap_pages = num_pages;
   }
-  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(hm.tmap);
-  const CUtensorMap& map_rope = *reinterpret_cast<const CUtensorMap*>(hm.tmap_rope);
+  return cudaSuccess;
+}
+
+// Decode-kernel dispatch: the tensor-core kernel, with in-shared-memory e4m3 -> bf16
+// conversion for an FP8 cache.
+cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table,
+                          int bt_stride, const void* cache, int num_pages, const Workspace& ws, cudaStream_t st) {
+  const bool fp8 = h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3;
+  cudaError_t e = cache_maps(h, cache, num_pages);
+  if (e != cudaSuccess) return e;
+  const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(h.tmap);
+  const CUtensorMap& map_rope = *reinterpret_cast<const CUtensorMap*>(h.tmap_rope);
   return fp8 ? launch_decode_tc<true>(h, ctx_len, batch, block_table, bt_stride, num_pages, map, map_rope, ws, st)
              : launch_decode_tc<false>(h, ctx_len, batch, block_table, bt_stride, num_pages, map, map_rope, ws, st);
 }

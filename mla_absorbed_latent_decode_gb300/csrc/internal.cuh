@@ -76,6 +76,8 @@ struct Handle {
 
 // TMA descriptors of the weights (built once in mla_create).
 cudaError_t prepare_weight_maps(Handle& h);
+// TMA descriptors of a cache in h.tmap / h.tmap_rope (64- and 32-column boxes of one page).
+cudaError_t cache_maps(const Handle& h, const void* cache, int num_pages);
 
 // Workspace sizing and carving (host).
 size_t workspace_bytes(const Handle& h, int batch, Workspace* carve, char* base);
@@ -91,6 +93,12 @@ cudaError_t launch_expand_kv(const Handle& h, const void* cache, int num_pages, 
 cudaError_t launch_decode_naive(const Handle& h, const void* q, const int32_t* ctx_len, int batch, int max_ctx,
                                 const int32_t* block_table, int bt_stride, const void* kvx, int num_pages,
                                 void* workspace, void* out, cudaStream_t st);
+// Causal prefill in MHA mode: per-head expansion of the cached rows, then attention.
+size_t prefill_workspace_bytes(int n_h, int batch, int max_ctx);
+cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_start, const int32_t* q_len, int total_q,
+                           int max_q, const int32_t* ctx_len, int batch, int max_ctx, const int32_t* block_table,
+                           int bt_stride, const void* cache, int num_pages, void* workspace, void* out,
+                           cudaStream_t st);
 // y[m][n_out] = bf16(x[m][k] . w[n_out][k]^T); k a multiple of 256, n_out of 16.
 cudaError_t launch_project(const __nv_bfloat16* x, int m, int k, const __nv_bfloat16* w, int n_out,
                            __nv_bfloat16* y, cudaStream_t st);

@@ -1,0 +1,592 @@
+// prefill.cu -- causal prefill over the latent cache in MHA mode, on tcgen05 tensor cores.
+//
+// Prefill handles every query token of a prompt (or of a chunk after a cached prefix) in one
+// pass; with query length = context length it is compute-bound ("G5 MLA KV 访存建模设计规格",
+// 名词定义 and 用例 2).  FlashMLA runs dense prefill in MHA mode, i.e. with the latent expanded
+// per head ("DeepSeek MLA 吸收式缓存：真实权重执行与 FlashMLA 架构边界" §6.1 support matrix,
+// §2.1 for the expansion), which costs 2 (d_nope + d_rope + d_v) = 640 flops per query, key
+// and head against 2 (d_c + d_rope + d_c) = 2176 in the absorbed form.
+//
+//   1. expand_tc_kernel: for every cached row t of a sequence and head h,
+//        K_nope[b][h][t] = W_UK[h] c_t,   V[b][h][t] = W_UV[h] c_t     (bf16),
+//      and the (already rotated) RoPE key K_r[b][t] copied once per token;
+//      CTA = (head, 128 tokens): D[128 tokens][256] = C[128][512] . [W_UK[h] ; W_UV[h]]^T,
+//      A = two cache pages by TMA, B = the head's weight rows, K-major, 4-stage ring.
+//   2. prefill_attn_kernel: CTA = (128 queries, head, sequence); query i of sequence b sits at
+//      position ctx_len - q_len + i and sees keys 0 .. that position.  Per 128-key tile j:
+//        S = Q K^T (M = 128 queries, N = 128 keys, K = 128 + 64) into one of two TMEM score
+//        buffers; online softmax (base 2, lazy rescale of O when the running maximum grows by
+//        more than 2^8) by warps 0-3, one query row per thread; P (bf16) into TMEM; O += P V
+//        (A = P from TMEM, B = V MN-major).  One thread issues every MMA, QK^T(j + 1) ahead of
+//        P V(j); K and V tiles arrive by TMA from two producer warps through 2-stage rings.
+//
+// TMEM of the attention CTA (512 columns): O [0, 128), S0 [128, 256), S1 [256, 384),
+// P0 [384, 448), P1 [448, 512).  Shared memory: Q 48 KB, K ring 2 x 48 KB, V ring 2 x 32 KB.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "append_ops.cuh"
+#include "internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBox = 128 * 128;        // 64 bf16 columns x 128 rows, 128-byte swizzled: 16 KB
+constexpr int kPageBox = 128 * 64;     // 64 bf16 columns x 64 rows (one cache page): 8 KB
+constexpr int kTile = 128;             // tokens of an expansion tile = keys of an attention tile
+constexpr int kQBlk = 128;             // queries of an attention CTA
+
+// ------------------------------------------------------------------ expansion
+constexpr int kExStages = 4;
+constexpr int kExStageBytes = 2 * kPageBox + 2 * kBox;      // two pages x 64 columns, W_UK and W_UV boxes
+constexpr int kExThreads = 192;                              // warps 0-3 epilogue, 4 producer, 5 MMA
+constexpr int kExSmem = kExStages * kExStageBytes + 1024 + 1024;
+
+struct ExBars {
+  uint64_t full[kExStages];
+  uint64_t empty[kExStages];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ bool page_ok(int p, int num_pages) { return p >= 0 && p < num_pages; }
+
+__global__ void __launch_bounds__(kExThreads, 1)
+expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_wuk,
+                 const __grid_constant__ CUtensorMap tm_wuv, const __nv_bfloat16* __restrict__ cache,
+                 const int32_t* __restrict__ ctx_len, int n_h, int max_ctx, const int32_t* __restrict__ block_table,
+                 int bt_stride, int num_pages, int lpad, __nv_bfloat16* __restrict__ kn,
+                 __nv_bfloat16* __restrict__ vv, __nv_bfloat16* __restrict__ kr, unsigned* check) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(smem);
+  ExBars* bars = reinterpret_cast<ExBars*>(smem + kExStages * kExStageBytes);
+  volatile int* abort_flag = &bars->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x, tb = blockIdx.y, b = blockIdx.z;
+  griddep_wait();                          // the rows may have been appended by the previous kernel
+  griddep_launch_dependents();
+  const int L = ctx_len[b];
+  const int t0 = tb * kTile;
+  if (L < 1 || L > max_ctx || t0 >= L) return;   // the attention kernel flags invalid lengths
+  const bool need1 = t0 + kPage < L;
+  const int p0 = block_table[(size_t)b * bt_stride + 2 * tb];
+  const int p1 = need1 ? block_table[(size_t)b * bt_stride + 2 * tb + 1] : -1;
+  const bool ok0 = page_ok(p0, num_pages), ok1 = need1 && page_ok(p1, num_pages);
+  if (tid == 0 && (!ok0 || (need1 && !ok1))) atomicOr(check, kCheckPageId);
+
+  if (tid == 0) {
+    for (int i = 0; i < kExStages; ++i) {
+      mbar_init(smem_u32(&bars->full[i]), 1);
+      mbar_init(smem_u32(&bars->empty[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->done), 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) { tmem_alloc(smem_u32(&bars->tmem_base), 256); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_cache);
+      const uint32_t bytes = (ok0 ? kPageBox : 0) + (ok1 ? kPageBox : 0) + 2 * kBox;
+      int issued = 0;
+      bool ok = true;
+      for (int kc = 0; kc < kDc / 64; ++kc) {
+        const int s = kc % kExStages;
+        if (kc >= kExStages && !mbar_wait(smem_u32(&bars->empty[s]), ((kc / kExStages) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = sbase + s * kExStageBytes, fb = smem_u32(&bars->full[s]);
+        mbar_arrive_expect_tx(fb, bytes);
+        if (ok0) tma_load_2d(st, &tm_cache, 64 * kc, p0 * kPage, fb);
+        if (ok1) tma_load_2d(st + kPageBox, &tm_cache, 64 * kc, p1 * kPage, fb);
+        tma_load_2d(st + 2 * kPageBox, &tm_wuk, 64 * kc, kDn * h, fb);
+        tma_load_2d(st + 2 * kPageBox + kBox, &tm_wuv, 64 * kc, kDv * h, fb);
+        issued = kc + 1;
+      }
+      if (!ok && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+      for (int kc = max(0, issued - kExStages); kc < issued; ++kc) {   // every copy lands before exit
+        volatile int never = 0;
+        mbar_wait(smem_u32(&bars->full[kc % kExStages]), (kc / kExStages) & 1, &never);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      // M = 128 tokens, N = 256 (the head's 128 W_UK rows, then its 128 W_UV rows), both K-major
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 256, false, false);
+      bool ok = true;
+      for (int kc = 0; kc < kDc / 64; ++kc) {
+        const int s = kc % kExStages;
+        if (!mbar_wait(smem_u32(&bars->full[s]), (kc / kExStages) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t st = sbase + s * kExStageBytes;
+        const uint64_t a = sdesc_sw128(st, 16, 1024), w = sdesc_sw128(st + 2 * kPageBox, 16, 1024);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)          // 16 latent columns per MMA: 32-byte steps in the 128-byte row
+          mma_ss(tmem, a + (uint64_t)(2 * k), w + (uint64_t)(2 * k), idesc, (kc > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bars->empty[s]));
+      }
+      if (!ok && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+      mma_commit(smem_u32(&bars->done));     // also after a failure: every issued MMA has finished
+      volatile int never = 0;
+      mbar_wait(smem_u32(&bars->done), 0, &never);     // ... before the CTA frees its TMEM
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue: thread = token
+    const int r = 32 * warp + lane, t = t0 + r;
+    const bool row_ok = t < L && (r < kPage ? ok0 : ok1);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort_flag) && !*abort_flag);
+    tc_fence_after();
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    uint4* dk = reinterpret_cast<uint4*>(kn + (((size_t)b * n_h + h) * lpad + t) * kDn);
+    uint4* dv = reinterpret_cast<uint4*>(vv + (((size_t)b * n_h + h) * lpad + t) * kDv);
+    if (ok) {
+#pragma unroll 1
+      for (int g = 0; g < 8; ++g) {          // columns 32 g .. 32 g + 31: K_nope for g < 4, V after
+        uint32_t v[32];
+        tmem_ld32(lane_addr + 32 * g, v);
+        tmem_ld_wait();
+        uint4* d = (g < 4 ? dk : dv) + 4 * (g & 3);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          d[i] = row_ok ? make_uint4(bf16x2(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
+                                     bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                                     bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                                     bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])))
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (h == 0) {                          // the RoPE key, shared by the heads, once per token
+        uint4* d = reinterpret_cast<uint4*>(kr + ((size_t)b * lpad + t) * kDr);
+        if (row_ok) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              cache + ((size_t)(r < kPage ? p0 : p1) * kPage + (r & (kPage - 1))) * kRow + kDc);
+#pragma unroll
+          for (int i = 0; i < kDr / 8; ++i) d[i] = src[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < kDr / 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------------ attention
+constexpr int kAtThreads = 224;        // warps 0-3 softmax + epilogue, 4 K producer, 5 V producer, 6 MMA
+constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6;
+constexpr int kOffQ = 0;                               // q_nope 0..63, q_nope 64..127, q_pe: 3 boxes
+constexpr int kOffK = 3 * kBox;                        // 2 stages x (k_nope 0..63, 64..127, k_r)
+constexpr int kOffV = kOffK + 2 * 3 * kBox;            // 2 stages x (v 0..63, 64..127)
+constexpr int kOffBars = kOffV + 2 * 2 * kBox;
+constexpr int kAtSmem = kOffBars + 1024 + 1024;
+constexpr uint32_t kTmO = 0, kTmS = 128, kTmP = 384;   // TMEM columns
+constexpr float kRescaleLog2 = 8.0f;                   // rescale O when the row maximum grows by > 2^8
+
+struct AtBars {
+  uint64_t qfull, qready;
+  uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
+  uint64_t sfull[2], sfree[2], pfull[2], pdone[2];
+  uint64_t ofinal;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void at_fail(AtBars* bars, unsigned* check) {
+  if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+}
+
+__global__ void __launch_bounds__(kAtThreads, 1)
+prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kn,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kr,
+                    const int32_t* __restrict__ q_start, const int32_t* __restrict__ q_len, int total_q, int max_q,
+                    const int32_t* __restrict__ ctx_len, int n_h, int max_ctx, const int32_t* __restrict__ block_table,
+                    int bt_stride, int num_pages, const float2* __restrict__ rope_cs, int max_position,
+                    float scale_log2, int lpad, __nv_bfloat16* __restrict__ out, unsigned* check) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(smem);
+  AtBars* bars = reinterpret_cast<AtBars*>(smem + kOffBars);
+  volatile int* abort_flag = &bars->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qb = gridDim.x - 1 - blockIdx.x;           // the longest query blocks start first
+  const int h = blockIdx.y, b = blockIdx.z;
+  griddep_wait();                                      // the expanded keys and values
+  griddep_launch_dependents();
+  const int L = ctx_len[b], nq = q_len[b], qs = q_start[b];
+  const bool rows_ok = nq >= 0 && nq <= max_q && qs >= 0 && (long long)qs + nq <= total_q;
+  const bool seq_ok = rows_ok && L >= 1 && L <= max_ctx && nq <= L;
+  const int r0 = qb * kQBlk;
+  if (!rows_ok) {                                      // nowhere to write: flag only
+    if (tid == 0 && qb == 0 && h == 0) atomicOr(check, kCheckCtxLen);
+    return;
+  }
+  if (r0 >= nq) return;
+  const int nrows = min(kQBlk, nq - r0);
+  const int p_first = L - nq + r0, p_last = p_first + nrows - 1;   // positions of the block's queries
+  // every page the block's keys come from must be a valid page id
+  bool bad = !seq_ok;
+  if (seq_ok) {
+    const int npages = (p_last + kPage) / kPage;
+    for (int i = tid; i < npages; i += kAtThreads) bad |= !page_ok(block_table[(size_t)b * bt_stride + i], num_pages);
+  }
+  bad = __syncthreads_or(bad);
+  if (bad) {                                           // zero output rows, flag
+    if (tid == 0) atomicOr(check, seq_ok ? kCheckPageId : kCheckCtxLen);
+    for (int i = tid; i < nrows * (kDv / 8); i += kAtThreads) {
+      const int r = i / (kDv / 8), c = i % (kDv / 8);
+      reinterpret_cast<uint4*>(out + ((size_t)(qs + r0 + r) * n_h + h) * kDv)[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
+  const int n_kt = (p_last + kTile) / kTile;            // key tiles 0 .. n_kt - 1
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars->qfull), 1);
+    mbar_init(smem_u32(&bars->qready), 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->kfull[i]), 1);
+      mbar_init(smem_u32(&bars->kempty[i]), 1);
+      mbar_init(smem_u32(&bars->vfull[i]), 1);
+      mbar_init(smem_u32(&bars->vempty[i]), 1);
+      mbar_init(smem_u32(&bars->sfull[i]), 1);
+      mbar_init(smem_u32(&bars->sfree[i]), 4);
+      mbar_init(smem_u32(&bars->pfull[i]), 4);
+      mbar_init(smem_u32(&bars->pdone[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->ofinal), 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) { tmem_alloc(smem_u32(&bars->tmem_base), 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int kv_row0 = (b * n_h + h) * lpad;            // this head's first expanded row
+
+  if (warp == kWarpK) {
+    // ---------------------------------------------------------------- Q, then the key tiles
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_kn);
+      prefetch_tmap(&tm_kr);
+      const uint32_t qf = smem_u32(&bars->qfull);
+      mbar_arrive_expect_tx(qf, 3 * kBox);
+      for (int c = 0; c < 3; ++c) tma_load_3d(sbase + kOffQ + c * kBox, &tm_q, 64 * c, h, qs + r0, qf);
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(smem_u32(&bars->kempty[s]), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+        const uint32_t st = sbase + kOffK + s * 3 * kBox, fb = smem_u32(&bars->kfull[s]);
+        mbar_arrive_expect_tx(fb, 3 * kBox);
+        tma_load_2d(st, &tm_kn, 0, kv_row0 + kTile * j, fb);
+        tma_load_2d(st + kBox, &tm_kn, 64, kv_row0 + kTile * j, fb);
+        tma_load_2d(st + 2 * kBox, &tm_kr, 0, b * lpad + kTile * j, fb);
+        issued = j + 1;
+      }
+      if (!ok) at_fail(bars, check);
+      volatile int never = 0;
+      mbar_wait(qf, 0, &never);
+      for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(smem_u32(&bars->kfull[j & 1]), (j >> 1) & 1, &never);
+    }
+  } else if (warp == kWarpV) {
+    // ---------------------------------------------------------------- value tiles
+    if (lane == 0) {
+      prefetch_tmap(&tm_v);
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(smem_u32(&bars->vempty[s]), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+        const uint32_t st = sbase + kOffV + s * 2 * kBox, fb = smem_u32(&bars->vfull[s]);
+        mbar_arrive_expect_tx(fb, 2 * kBox);
+        tma_load_2d(st, &tm_v, 0, kv_row0 + kTile * j, fb);
+        tma_load_2d(st + kBox, &tm_v, 64, kv_row0 + kTile * j, fb);
+        issued = j + 1;
+      }
+      if (!ok) at_fail(bars, check);
+      volatile int never = 0;
+      for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(smem_u32(&bars->vfull[j & 1]), (j >> 1) & 1, &never);
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
+      const uint64_t qd = sdesc_sw128(sbase + kOffQ, 16, 1024);
+      bool ok = mbar_wait(smem_u32(&bars->qready), 0, abort_flag);
+      auto pv = [&](int jj) -> bool {       // O += P(jj) V(jj)
+        const int s = jj & 1;
+        if (!mbar_wait(smem_u32(&bars->pfull[s]), (jj >> 1) & 1, abort_flag) ||
+            !mbar_wait(smem_u32(&bars->vfull[s]), (jj >> 1) & 1, abort_flag))
+          return false;
+        tc_fence_after();
+        // V tile: 128 key rows (K) x 128 value columns (N) in two 64-column boxes, MN-major
+        const uint64_t vd = sdesc_sw128(sbase + kOffV + s * 2 * kBox, kBox, 1024);
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          mma_ts(tmem + kTmO, tmem + kTmP + 64 * s + 8 * k, vd + (uint64_t)(128 * k), idesc_pv,
+                 (jj > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bars->vempty[s]));
+        mma_commit(smem_u32(&bars->pdone[s]));
+        return true;
+      };
+      for (int j = 0; ok && j < n_kt; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(smem_u32(&bars->kfull[s]), (j >> 1) & 1, abort_flag) ||
+            (j >= 2 && !mbar_wait(smem_u32(&bars->sfree[s]), ((j - 2) >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t kd = sdesc_sw128(sbase + kOffK + s * 3 * kBox, 16, 1024);
+#pragma unroll
+        for (int k = 0; k < kDq / 16; ++k) {  // box k / 4 (k_nope, k_nope, k_r), 32-byte step k % 4
+          const uint64_t off = (uint64_t)(((k >> 2) * kBox + (k & 3) * 32) >> 4);
+          mma_ss(tmem + kTmS + 128 * s, qd + off, kd + off, idesc_qk, k > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->sfull[s]));
+        mma_commit(smem_u32(&bars->kempty[s]));
+        if (j >= 1) ok = pv(j - 1);
+      }
+      if (ok) ok = pv(n_kt - 1);
+      if (!ok) at_fail(bars, check);
+      mma_commit(smem_u32(&bars->ofinal));   // after a failure too: every issued MMA has finished
+      volatile int never = 0;
+      mbar_wait(smem_u32(&bars->ofinal), 0, &never);   // ... before the CTA frees its TMEM
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax: thread = query row
+    const int r = 32 * warp + lane;
+    const int qpos = p_first + r;
+    const int lim = min(qpos, L - 1);                  // last visible key (rows past the block clamp)
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    bool ok = mbar_wait(smem_u32(&bars->qfull), 0, abort_flag);
+    if (ok) {
+      // rotate this row's q_pe in place at its position (swizzled box: chunk c at c ^ (r & 7))
+      uint8_t* row = smem + kOffQ + 2 * kBox + r * 128;
+      const float2* cs = rope_cs + (size_t)min(lim, max_position - 1) * (kDr / 2);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4* p = reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4));
+        uint4 v = *p;
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float y0, y1;
+          rope_pair(bf16_lo(w[i]), bf16_hi(w[i]), cs[4 * c + i], &y0, &y1);
+          w[i] = pack_bf16(y0, y1);
+        }
+        *p = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&bars->qready));
+    float m_ref = -INFINITY, l = 0.0f;
+    for (int j = 0; ok && j < n_kt; ++j) {
+      const int s = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sfull[s]), (j >> 1) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t x[kTile];                               // scores, then scaled base-2 logits (float bits)
+#pragma unroll
+      for (int g = 0; g < 4; ++g) tmem_ld32(tmem + lane_off + kTmS + 128 * s + 32 * g, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * g]));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->sfree[s]));
+      float mx = -INFINITY;
+      const bool masked = kTile * j + kTile - 1 > p_first;
+#pragma unroll
+      for (int c = 0; c < kTile; ++c) {
+        const float v = (masked && kTile * j + c > lim) ? -INFINITY : __uint_as_float(x[c]) * scale_log2;
+        x[c] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      const float m_new = fmaxf(m_ref, mx);
+      if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleLog2)) {
+        const float alpha = ex2_approx(m_ref - m_new);
+        l *= alpha;
+        m_ref = m_new;
+        if (j > 0) {                                   // O holds P V of tiles < j: rescale it
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pdone[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int g = 0; g < 4; ++g) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + kTmO + 32 * g, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tmem + lane_off + kTmO + 32 * g, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      if (j >= 2) {                                    // P V(j - 2) has read this P buffer
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pdone[s]), ((j - 2) >> 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      float sum = 0.0f;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float a = ex2_approx(__uint_as_float(x[64 * hf + 2 * c]) - m_ref);
+          const float bb = ex2_approx(__uint_as_float(x[64 * hf + 2 * c + 1]) - m_ref);
+          sum += a + bb;
+          pk[c] = bf16x2(a, bb);
+        }
+        tmem_st32(tmem + lane_off + kTmP + 64 * s + 32 * hf, pk);
+      }
+      l += sum;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->pfull[s]));
+    }
+    // ---------------------------------------------------------------- epilogue
+    ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->ofinal), 0, abort_flag)) && !*abort_flag;
+    tc_fence_after();
+    if (ok) {
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(qs + r0 + r) * n_h + h) * kDv);
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + kTmO + 32 * g, o);
+        tmem_ld_wait();
+        if (r < nrows) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[4 * g + i] = make_uint4(bf16x2(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv),
+                                        bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv),
+                                        bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv),
+                                        bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult qr;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 matrix [rows][width] with boxes of 64 columns x 128 rows, 128-byte swizzle.
+cudaError_t rows_map_2d(const void* base, long long rows, int width, CUtensorMap* m) {
+  auto enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)width * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t elem[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? cudaSuccess
+             : cudaErrorInvalidValue;
+}
+
+// Queries [total_q][n_h][192] bf16 as (column, head, row): boxes of 64 columns x 1 head x 128 rows
+// (rows past total_q read as zeros).
+cudaError_t query_map(const void* q, int total_q, int n_h, CUtensorMap* m) {
+  auto enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)kDq, (cuuint64_t)n_h, (cuuint64_t)total_q};
+  const cuuint64_t strides[2] = {(cuuint64_t)kDq * 2, (cuuint64_t)kDq * 2 * n_h};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kQBlk};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? cudaSuccess
+             : cudaErrorInvalidValue;
+}
+
+int padded_ctx(int max_ctx) { return (max_ctx + kTile - 1) / kTile * kTile; }
+
+}  // namespace
+
+// Workspace of a prefill: K_nope and V [B][n_h][lpad][128] and K_r [B][lpad][64], bf16,
+// lpad = max_ctx rounded up to 128 tokens.
+size_t prefill_workspace_bytes(int n_h, int batch, int max_ctx) {
+  return (size_t)batch * padded_ctx(max_ctx) * (2 * (size_t)n_h * kDn + kDr) * 2;
+}
+
+cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_start, const int32_t* q_len, int total_q,
+                           int max_q, const int32_t* ctx_len, int batch, int max_ctx, const int32_t* block_table,
+                           int bt_stride, const void* cache, int num_pages, void* workspace, void* out,
+                           cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(expand_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kExSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaError_t e = cache_maps(h, cache, num_pages);
+  if (e != cudaSuccess) return e;
+  const int n_h = h.cfg.n_h, lpad = padded_ctx(max_ctx);
+  __nv_bfloat16* kn = static_cast<__nv_bfloat16*>(workspace);
+  __nv_bfloat16* vv = kn + (size_t)batch * n_h * lpad * kDn;
+  __nv_bfloat16* kr = vv + (size_t)batch * n_h * lpad * kDv;
+  alignas(64) CUtensorMap tm_q, tm_kn, tm_v, tm_kr;
+  if ((e = query_map(q, total_q, n_h, &tm_q)) != cudaSuccess) return e;
+  if ((e = rows_map_2d(kn, (long long)batch * n_h * lpad, kDn, &tm_kn)) != cudaSuccess) return e;
+  if ((e = rows_map_2d(vv, (long long)batch * n_h * lpad, kDv, &tm_v)) != cudaSuccess) return e;
+  if ((e = rows_map_2d(kr, (long long)batch * lpad, kDr, &tm_kr)) != cudaSuccess) return e;
+  e = launch_pdl(expand_tc_kernel, dim3(n_h, lpad / kTile, batch), dim3(kExThreads), kExSmem, st,
+                 *reinterpret_cast<const CUtensorMap*>(h.tmap), *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk),
+                 *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv), static_cast<const __nv_bfloat16*>(cache), ctx_len,
+                 n_h, max_ctx, block_table, bt_stride, num_pages, lpad, kn, vv, kr, h.check_word);
+  if (e != cudaSuccess) return e;
+  const float scale_log2 = h.scale * 1.4426950408889634f;
+  return launch_pdl(prefill_attn_kernel, dim3((max_q + kQBlk - 1) / kQBlk, n_h, batch), dim3(kAtThreads), kAtSmem, st,
+                    tm_q, tm_kn, tm_v, tm_kr, q_start, q_len, total_q, max_q, ctx_len, n_h, max_ctx, block_table,
+                    bt_stride, num_pages, (const float2*)h.rope_cs, h.cfg.max_position, scale_log2, lpad,
+                    static_cast<__nv_bfloat16*>(out), h.check_word);
+}
+
+}  // namespace mla

@@ -169,6 +169,26 @@ def _finish_decode(rng, name, seed, n_h, ctx_len, cache_dtype, shuffle, spare_pa
 # the five named workloads
 # ---------------------------------------------------------------------------
 
+def make_prefill(name, seed, n_h, ctx_len, q_len=None, *, q_std=1.0) -> Workload:
+    """Prefill inputs: a decode workload's cache rows, weights and paged layout (same draws as
+    ``make_decode``), plus query rows for the last ``q_len[b]`` positions of every sequence
+    (every position when ``q_len`` is None), packed [total_q][n_h][d_nope + d_rope] in
+    sequence order and drawn from a second stream of the same seed."""
+    wl = make_decode(name, seed, n_h, ctx_len)
+    ql = wl.ctx_len.copy() if q_len is None else np.asarray(q_len, np.int32)
+    rng = np.random.default_rng([seed, 1])
+    q = _normal_bf16(rng, (int(np.sum(ql.astype(np.int64))), n_h, D_NOPE + D_ROPE), q_std)
+    starts = np.concatenate([[0], np.cumsum(ql.astype(np.int64))[:-1]]).astype(np.int32)
+    wl.extra["prefill"] = {"q": q, "q_len": ql, "q_start": starts}
+    return wl
+
+
+def v3_prefill(seed=5, B=2, s_ctx=4096, n_h=128) -> Workload:
+    """DeepSeek-V3 shapes, B=2 whole prompts of 4096 tokens (query length = context length)."""
+    wl = make_prefill("v3_prefill_b2_s4096", seed, n_h, np.full(B, s_ctx, np.int32))
+    return wl
+
+
 def v2lite_single_step_inputs(seed=0, tokens=26, hidden=2048, n_h=16):
     """V2-Lite layer inputs for a 25-token prefill plus one decode token.
 
