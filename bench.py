@@ -70,8 +70,13 @@ def peaks():
 LAYER = "v2lite_layer"      # the V2-Lite layer step with its projections on the GPU
 
 
+PREFILL = "v3_prefill_b2_s4096"   # whole-prompt prefill, MHA mode (a compute-bound second workload)
+
+
 def workload(name):
     from mla_absorbed_latent_decode_gb300 import workloads as W
+    if name == PREFILL:
+        return W.v3_prefill()
     if name == LAYER:
         # x -> W_Q, W_DKV on the device (mla_project, mla_kv_project_append), then the decode;
         # the workload's rows and query are placeholders until the CPU leg projects them
@@ -83,7 +88,7 @@ def workload(name):
         wl.extra["layer"] = inp
         return wl
     if name not in W.NAMED:
-        raise SystemExit(f"unknown workload {name}; choose from {sorted(W.NAMED) + [LAYER]}")
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(W.NAMED) + [LAYER, PREFILL]}")
     return W.NAMED[name]()
 
 
@@ -99,6 +104,20 @@ def algorithmic(wl):
         weights += 2 * proj
         flops += 2 * wl.B * proj
     return cache, weights, flops
+
+
+def prefill_flops(wl):
+    """FLOPs of one prefill step: the per-head expansion of every cached row (W_UK and W_UV,
+    2 n_h (d_nope + d_v) d_c per row) and the causal attention (2 n_h (d_nope + d_rope + d_v)
+    per visible query-key pair); returns (expansion, attention)."""
+    p = wl.extra["prefill"]
+    rows = int(np.sum(wl.ctx_len.astype(np.int64)))
+    expand = 2 * wl.n_h * (wl.d_nope + wl.d_v) * wl.d_c * rows
+    pairs = 0
+    for L, n in zip(wl.ctx_len.astype(np.int64), p["q_len"].astype(np.int64)):
+        pairs += n * (L - n) + n * (n + 1) // 2          # query i sees L - n + i + 1 keys
+    attn = 2 * wl.n_h * (wl.d_nope + wl.d_rope + wl.d_v) * pairs
+    return expand, attn
 
 
 def cache_bytes_per_token(wl):
@@ -546,8 +565,237 @@ def naive_ab(args, wl, sess, flush_l2, stream):
     return res
 
 
+# ------------------------------------------------------------------ prefill workload
+
+def prefill_oracle_sample(wl, seconds):
+    """Time the oracle's MHA-mode prefill of sequence 0, one head at a time, until about
+    `seconds` of CPU work; return (algorithmic TFLOP/s, seconds, description)."""
+    from oracle import mla_ref
+    p = wl.extra["prefill"]
+    L, n = int(wl.ctx_len[0]), int(p["q_len"][0])
+    vals = wl.extra.get("oracle_vals0")
+    if vals is None:                                  # the oracle's own cache contents (untimed)
+        vals = mla_ref.bf16_to_f64(mla_ref.stored_row_bf16(wl.rows[:L], wl.row_pos[:L], wl.d_c, wl.rope_base))
+        wl.extra["oracle_vals0"] = vals
+    q = mla_ref.bf16_to_f64(p["q"][:n])
+    w_uk, w_uv = mla_ref.bf16_to_f64(wl.w_uk), mla_ref.bf16_to_f64(wl.w_uv)
+    scale = mla_ref.default_scale(wl.d_nope, wl.d_rope)
+    elapsed, heads = 0.0, 0
+    for h in range(wl.n_h):
+        t0 = time.perf_counter()
+        mla_ref.prefill_naive(q[:, h:h + 1], vals[:, :wl.d_c], vals[:, wl.d_c:], w_uk[h:h + 1], w_uv[h:h + 1], L - n,
+                              scale, wl.rope_base)
+        elapsed += time.perf_counter() - t0
+        heads += 1
+        if elapsed >= seconds:
+            break
+    pairs = n * (L - n) + n * (n + 1) // 2
+    flops = heads * (2 * (wl.d_nope + wl.d_v) * wl.d_c * L + 2 * (wl.d_nope + wl.d_rope + wl.d_v) * pairs)
+    return flops / elapsed / 1e12, elapsed, (f"{heads} of {wl.n_h} heads of sequence 0 ({L} tokens, {n} queries), "
+                                             f"fp64 MHA-mode prefill, {elapsed:.1f} s")
+
+
+def run_prefill_reference(args, wl):
+    per_step = max(0.5, min(3.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        prefill_oracle_sample(wl, per_step)
+    vals, desc = [], ""
+    for _ in range(args.steps):
+        v, _, desc = prefill_oracle_sample(wl, per_step)
+        vals.append(v)
+    v = statistics.mean(vals)
+    fe, fa = prefill_flops(wl)
+    line = {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(v, 6), "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round((fe + fa) / (v * 1e12) * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "s_ctx": wl.max_ctx, "n_h": wl.n_h, "cache": "bf16",
+                   "note": "ms_per_step extrapolated from the sampled throughput to the whole batch"},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+PREFILL_METRIC = "MLA prefill (MHA mode, causal) TFLOP/s and % of the bf16 tensor peak"
+
+
+def run_prefill(args, wl):
+    """One step = mla_kv_append of every prompt row + mla_prefill (expansion + attention)."""
+    import torch
+    import torch.distributed as dist
+
+    from mla_absorbed_latent_decode_gb300 import binding as B
+    from mla_absorbed_latent_decode_gb300.runner import DecodeSession, bf16_tensor
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    p = wl.extra["prefill"]
+    sess = DecodeSession(wl, device=str(dev))
+    rows = bf16_tensor(wl.rows, dev)
+    seq = torch.from_numpy(wl.row_seq.astype(np.int32)).to(dev)
+    pos = torch.from_numpy(wl.row_pos.astype(np.int32)).to(dev)
+    q = bf16_tensor(p["q"], dev)
+    q_start = torch.from_numpy(p["q_start"].astype(np.int32)).to(dev)
+    q_len = torch.from_numpy(p["q_len"].astype(np.int32)).to(dev)
+    max_q = int(p["q_len"].max())
+    ws = torch.empty(sess.mla.prefill_workspace_size(wl.B, wl.max_ctx), dtype=torch.uint8, device=dev)
+    out = torch.empty((q.shape[0], wl.n_h, wl.d_v), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones_like(flush)
+
+    def flush_l2():
+        flush.zero_()
+        flush_rd.view(torch.int32).amax()
+
+    def step(rows=rows, seq=seq, pos=pos, q=q, q_start=q_start, q_len=q_len, ctx=sess.ctx_len):
+        sess.mla.kv_append(rows, seq, pos, sess.block_table, sess.cache, wl.num_pages)
+        sess.mla.prefill(q, q_start, q_len, max_q, ctx, wl.max_ctx, sess.block_table, sess.cache, wl.num_pages,
+                         ws, out)
+
+    for _ in range(max(3, args.warmup)):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    if sess.status() != 0:
+        raise SystemExit("device check word set during warm-up")
+
+    def timed_pass(profile):
+        sess.mla.set_option(B.MLA_OPT_PROFILE, 1 if profile else 0)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        kms = []
+        for a, z in ev:
+            flush_l2()
+            a.record(stream)
+            step()
+            z.record(stream)
+            if profile:
+                kms.append(sess.mla.profile_read())
+        torch.cuda.synchronize()
+        return [a.elapsed_time(z) for a, z in ev], kms
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms, _ = timed_pass(False)
+    torch.cuda.synchronize()
+    _, kernel_ms = timed_pass(True)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    sess.mla.set_option(B.MLA_OPT_PROFILE, 0)
+    if sess.status() != 0:
+        raise SystemExit("device check word set during the timed steps")
+    ms = statistics.mean(step_ms)
+
+    # end to end with host buffers: the prompt rows, indices and queries in, the outputs back
+    parts = [("rows", wl.rows.view(np.int16)), ("seq", wl.row_seq.astype(np.int32)),
+             ("pos", wl.row_pos.astype(np.int32)), ("q", p["q"].view(np.int16)),
+             ("q_start", p["q_start"].astype(np.int32)), ("q_len", p["q_len"].astype(np.int32)),
+             ("ctx", wl.ctx_len.astype(np.int32))]
+    offs, total = {}, 0
+    for name, a in parts:
+        offs[name] = total
+        total += (a.nbytes + 255) // 256 * 256
+    h_pack = torch.empty(total, dtype=torch.uint8).pin_memory()
+    d_pack = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = {}
+    for name, a in parts:
+        flat = np.ascontiguousarray(a).reshape(-1)
+        h_pack[offs[name]:offs[name] + flat.nbytes].copy_(torch.from_numpy(flat.view(np.uint8)))
+        dt = torch.int16 if flat.dtype == np.int16 else torch.int32
+        views[name] = d_pack[offs[name]:offs[name] + flat.nbytes].view(dt).view(a.shape)
+    h_out = torch.empty(tuple(out.shape), dtype=torch.int16).pin_memory()
+    h2d = sum(a.nbytes for _, a in parts)
+    d2h = h_out.numel() * 2
+
+    def e2e_step():
+        d_pack.copy_(h_pack, non_blocking=True)
+        step(views["rows"].view(torch.bfloat16), views["seq"], views["pos"], views["q"].view(torch.bfloat16),
+             views["q_start"], views["q_len"], views["ctx"])
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush_l2()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush_l2()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        z.record(stream)
+        z.synchronize()
+        e2e_ms.append(a.elapsed_time(z))
+    e2e = statistics.mean(e2e_ms)
+
+    t = torch.tensor([ms, e2e], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms, e2e = float(t[0]), float(t[1])
+    fe, fa = prefill_flops(wl)
+    hbm, tc_burst, tc_sust, peak_kind = peaks()
+    per_kernel = {k: round(statistics.mean(km[k] for km in kernel_ms) * 1000.0, 2) for k in kernel_ms[0]}
+    attn_ms = per_kernel["mla_prefill_attention"] / 1000.0
+    exp_ms = per_kernel["mla_prefill_expand"] / 1000.0
+    achieved = fa / (attn_ms * 1e-3) / 1e12
+    if rank == 0:
+        line = {
+            "metric": PREFILL_METRIC, "value": round(world * (fe + fa) / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "us_per_step": round(ms * 1000.0, 2), "us_per_step_median": round(statistics.median(step_ms) * 1000.0, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "s_ctx": wl.max_ctx, "n_h": wl.n_h, "q_len": max_q,
+                       "mode": "MHA (latent expanded per head), causal, whole prompts",
+                       "flops_per_step": {"expansion": int(fe), "attention": int(fa)},
+                       "l2": f"flushed between steps outside the timed events ({flush.numel() >> 20} MiB write + "
+                             f"read); the step's queries ({q.numel() * 2 >> 20} MiB) also exceed L2",
+                       "timing": "value from K steps without per-kernel events; per_kernel_us and roofline from "
+                                 "a second K-step pass with per-kernel events",
+                       "arithmetic": "bf16 MMA operands (expanded K/V, P), fp32 accumulation and softmax",
+                       "parallelism": f"replicas x{world}"},
+            "per_kernel_us": per_kernel,
+            "roofline": {"bound": "tensor", "kernel": "mla_prefill_attention", "achieved": round(achieved, 1),
+                         "peak": tc_burst, "unit": "TFLOP/s", "frac": round(achieved / tc_burst, 4), "traffic": None,
+                         "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                         "algorithmic_flops_per_launch": int(fa),
+                         "expansion": {"achieved": round(fe / (exp_ms * 1e-3) / 1e12, 1),
+                                       "frac": round(fe / (exp_ms * 1e-3) / 1e12 / tc_burst, 4)}},
+            "e2e": {"value": round(world * (fe + fa) / (e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "ms_per_step": round(e2e, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": args.steps * 3,
+            "clocks": clock_info,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            v, _, desc = prefill_oracle_sample(wl, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s", "cores": blas_threads(),
+                                    "kind": "oracle", "sample": desc}
+        print(json.dumps(line), flush=True)
+    sess.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
+    if args.workload == PREFILL:
+        wl = workload(args.workload)
+        if args.impl == "reference":
+            return 0 if int(os.environ.get("RANK", "0")) != 0 else run_prefill_reference(args, wl)
+        return run_prefill(args, wl)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -337,20 +337,24 @@ mla_status_t mla_get_status(mla_handle_t h, mla_stream_t stream, uint32_t* devic
 #define MLA_OPT_SPLITS  1   /* value 0: the planner chooses; k > 0: split every sequence into
                                k chunks (capped at its page count).  Used to test that the
                                result does not depend on the split. */
-#define MLA_OPT_PROFILE 2   /* value 1: record CUDA events around each kernel mla_decode
-                               launches; mla_profile_read returns the durations. 0: off. */
+#define MLA_OPT_PROFILE 2   /* value 1: record CUDA events around each kernel mla_decode and
+                               mla_prefill launch (which serialises them); mla_profile_read
+                               returns the durations. 0: off. */
 
 mla_status_t mla_set_option(mla_handle_t h, int32_t option, int64_t value);
 
 /*
  * mla_profile_read -- with MLA_OPT_PROFILE on, synchronize and return the
- * device time in milliseconds of each kernel of the last mla_decode call, in
- * launch order (q-absorb, plan, decode, combine + W_UV).  *count receives the
- * number of kernels; at most `capacity` values are written.  Names of the
- * kernels come from mla_profile_kernel_name.
+ * device time in milliseconds of each kernel of the last profiled mla_decode
+ * (q-absorb + plan, decode, combine + W_UV) or mla_prefill (expansion,
+ * attention) call, in launch order.  *count receives the number of kernels; at
+ * most `capacity` values are written.  mla_profile_last_name(h, i) names kernel
+ * i of that call ("" past the end); mla_profile_kernel_name(i) names the
+ * kernels of mla_decode.
  */
 mla_status_t mla_profile_read(mla_handle_t h, float* kernel_ms, int32_t capacity, int32_t* count);
 const char* mla_profile_kernel_name(int32_t index);
+const char* mla_profile_last_name(mla_handle_t h, int32_t index);
 
 /* Thread-local message of this thread's last failed call ("" if none). */
 const char* mla_last_error(void);

@@ -41,7 +41,7 @@ EXPORTED = [
     "mla_prefill_workspace_size", "mla_prefill",
     "mla_decode_workspace_size", "mla_decode",
     "mla_decode_fixed_scratch",
-    "mla_get_status", "mla_set_option", "mla_profile_read", "mla_profile_kernel_name",
+    "mla_get_status", "mla_set_option", "mla_profile_read", "mla_profile_kernel_name", "mla_profile_last_name",
     "mla_last_error", "mla_status_string",
 ]
 
@@ -94,6 +94,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]
     lib.mla_profile_kernel_name.argtypes = [i32]
     lib.mla_profile_kernel_name.restype = ctypes.c_char_p
+    lib.mla_profile_last_name.argtypes = [vp, i32]
+    lib.mla_profile_last_name.restype = ctypes.c_char_p
     lib.mla_last_error.argtypes = []
     lib.mla_last_error.restype = ctypes.c_char_p
     lib.mla_status_string.argtypes = [ctypes.c_int]
@@ -239,4 +241,4 @@ class Mla:
         buf = (ctypes.c_float * 16)()
         n = ctypes.c_int32(0)
         _check(self._lib.mla_profile_read(self._h, buf, 16, ctypes.byref(n)))
-        return {self._lib.mla_profile_kernel_name(i).decode(): float(buf[i]) for i in range(n.value)}
+        return {self._lib.mla_profile_last_name(self._h, i).decode(): float(buf[i]) for i in range(n.value)}

@@ -39,6 +39,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 const char* kKernelNames[] = {"mla_q_absorb_plan", "mla_decode_splitkv", "mla_combine_uv"};
 constexpr int kNumKernels = 3;
+const char* kPrefillKernelNames[] = {"mla_prefill_expand", "mla_prefill_attention"};
 
 mla_status_t check_config(const mla_config_t* c) {
   // Mandatory fields: a zero means "not given" and is reported by name.
@@ -146,6 +147,12 @@ const char* mla_status_string(mla_status_t s) {
 
 const char* mla_profile_kernel_name(int32_t index) {
   return (index >= 0 && index < kNumKernels) ? kKernelNames[index] : "";
+}
+
+const char* mla_profile_last_name(mla_handle_t hh, int32_t index) {
+  const Handle* h = reinterpret_cast<const Handle*>(hh);
+  if (!h || index < 0 || index >= h->n_ev_recorded - 1) return "";
+  return h->prof_prefill ? kPrefillKernelNames[index] : kKernelNames[index];
 }
 
 mla_status_t mla_create(const mla_config_t* cfg, const void* w_uk, const void* w_uv,
@@ -396,9 +403,17 @@ mla_status_t mla_prefill(mla_handle_t hh, const void* q, const int32_t* q_start,
   const size_t need = mla::prefill_workspace_bytes(h->cfg.n_h, batch, max_ctx);
   if (workspace_bytes < need)
     return fail(MLA_ERR_WORKSPACE, "mla_prefill: workspace has %zu bytes, %zu needed", workspace_bytes, need);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool prof = h->profile != 0;
+  if (prof) cudaEventRecord(h->ev[0], st);
   cudaError_t e = mla::launch_prefill(*h, q, q_start, q_len, total_q, max_q, ctx_len, batch, max_ctx, block_table,
-                                      bt_stride, cache, num_pages, workspace, out, reinterpret_cast<cudaStream_t>(stream));
+                                      bt_stride, cache, num_pages, workspace, out, st, prof ? h->ev[1] : nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  if (prof) {
+    cudaEventRecord(h->ev[2], st);
+    h->n_ev_recorded = 3;
+    h->prof_prefill = 1;
+  }
   return MLA_OK;
 }
 
@@ -461,6 +476,7 @@ mla_status_t mla_decode(mla_handle_t hh, const void* q, const int32_t* ctx_len, 
     return cuda_fail(e, "combine_uv launch");
   mark();
   h->n_ev_recorded = ev;
+  h->prof_prefill = 0;
   return MLA_OK;
 }
 

@@ -66,6 +66,7 @@ struct Handle {
   int profile;              // MLA_OPT_PROFILE
   cudaEvent_t ev[8];
   int n_ev_recorded;
+  int prof_prefill;         // the last profiled call was mla_prefill (else mla_decode)
   alignas(64) unsigned char tmap[128];   // TMA descriptor (CUtensorMap) of the last cache seen
   alignas(64) unsigned char tmap_rope[128];  // same cache, RoPE-key columns (32-column boxes)
   alignas(64) unsigned char tmap_wuk[128];  // TMA descriptors of the handle's weight copies
@@ -98,7 +99,7 @@ size_t prefill_workspace_bytes(int n_h, int batch, int max_ctx);
 cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_start, const int32_t* q_len, int total_q,
                            int max_q, const int32_t* ctx_len, int batch, int max_ctx, const int32_t* block_table,
                            int bt_stride, const void* cache, int num_pages, void* workspace, void* out,
-                           cudaStream_t st);
+                           cudaStream_t st, cudaEvent_t between = nullptr);
 // y[m][n_out] = bf16(x[m][k] . w[n_out][k]^T); k a multiple of 256, n_out of 16.
 cudaError_t launch_project(const __nv_bfloat16* x, int m, int k, const __nv_bfloat16* w, int n_out,
                            __nv_bfloat16* y, cudaStream_t st);

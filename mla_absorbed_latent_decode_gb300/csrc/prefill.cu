@@ -17,8 +17,8 @@
 //        S = Q K^T (M = 128 queries, N = 128 keys, K = 128 + 64) into one of two TMEM score
 //        buffers; online softmax (base 2, lazy rescale of O when the running maximum grows by
 //        more than 2^8) by warps 0-3, one query row per thread; P (bf16) into TMEM; O += P V
-//        (A = P from TMEM, B = V MN-major).  One thread issues every MMA, QK^T(j + 1) ahead of
-//        P V(j); K and V tiles arrive by TMA from two producer warps through 2-stage rings.
+//        (A = P from TMEM, B = V MN-major).  One thread issues the QK^T MMAs and another the
+//        P V ones; K and V tiles arrive by TMA from two producer warps through 2-stage rings.
 //
 // TMEM of the attention CTA (512 columns): O [0, 128), S0 [128, 256), S1 [256, 384),
 // P0 [384, 448), P1 [448, 512).  Shared memory: Q 48 KB, K ring 2 x 48 KB, V ring 2 x 32 KB.
@@ -194,8 +194,8 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
 }
 
 // ------------------------------------------------------------------ attention
-constexpr int kAtThreads = 224;        // warps 0-3 softmax + epilogue, 4 K producer, 5 V producer, 6 MMA
-constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6;
+constexpr int kAtThreads = 256;        // warps 0-3 softmax + epilogue, 4 K / 5 V producers, 6 QK^T / 7 P V issuers
+constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6, kWarpPv = 7;
 constexpr int kOffQ = 0;                               // q_nope 0..63, q_nope 64..127, q_pe: 3 boxes
 constexpr int kOffK = 3 * kBox;                        // 2 stages x (k_nope 0..63, 64..127, k_r)
 constexpr int kOffV = kOffK + 2 * 3 * kBox;            // 2 stages x (v 0..63, 64..127)
@@ -208,10 +208,32 @@ struct AtBars {
   uint64_t qfull, qready;
   uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
   uint64_t sfull[2], sfree[2], pfull[2], pdone[2];
-  uint64_t ofinal;
+  uint64_t ofinal, qkdrain;
   uint32_t tmem_base;
   int abort;
 };
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum of 128 values (float bits) as a tree of three-input maxima, depth 5.
+__device__ __forceinline__ float max128(const uint32_t (&x)[kTile]) {
+  float a[44], b[15], c[5];
+#pragma unroll
+  for (int i = 0; i < 42; ++i)
+    a[i] = max3(__uint_as_float(x[3 * i]), __uint_as_float(x[3 * i + 1]), __uint_as_float(x[3 * i + 2]));
+  a[42] = __uint_as_float(x[126]);
+  a[43] = __uint_as_float(x[127]);
+#pragma unroll
+  for (int i = 0; i < 14; ++i) b[i] = max3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  b[14] = fmaxf(a[42], a[43]);
+#pragma unroll
+  for (int i = 0; i < 5; ++i) c[i] = max3(b[3 * i], b[3 * i + 1], b[3 * i + 2]);
+  return max3(max3(c[0], c[1], c[2]), c[3], c[4]);
+}
 
 __device__ __forceinline__ void at_fail(AtBars* bars, unsigned* check) {
   if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
@@ -277,6 +299,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_init(smem_u32(&bars->pdone[i]), 1);
     }
     mbar_init(smem_u32(&bars->ofinal), 1);
+    mbar_init(smem_u32(&bars->qkdrain), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -333,30 +356,14 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(smem_u32(&bars->vfull[j & 1]), (j >> 1) & 1, &never);
     }
   } else if (warp == kWarpMma) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- QK^T issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
       const uint64_t qd = sdesc_sw128(sbase + kOffQ, 16, 1024);
       bool ok = mbar_wait(smem_u32(&bars->qready), 0, abort_flag);
-      auto pv = [&](int jj) -> bool {       // O += P(jj) V(jj)
-        const int s = jj & 1;
-        if (!mbar_wait(smem_u32(&bars->pfull[s]), (jj >> 1) & 1, abort_flag) ||
-            !mbar_wait(smem_u32(&bars->vfull[s]), (jj >> 1) & 1, abort_flag))
-          return false;
-        tc_fence_after();
-        // V tile: 128 key rows (K) x 128 value columns (N) in two 64-column boxes, MN-major
-        const uint64_t vd = sdesc_sw128(sbase + kOffV + s * 2 * kBox, kBox, 1024);
-#pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)
-          mma_ts(tmem + kTmO, tmem + kTmP + 64 * s + 8 * k, vd + (uint64_t)(128 * k), idesc_pv,
-                 (jj > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bars->vempty[s]));
-        mma_commit(smem_u32(&bars->pdone[s]));
-        return true;
-      };
       for (int j = 0; ok && j < n_kt; ++j) {
         const int s = j & 1;
+        // K(j) has landed and the score buffer's previous tile, j - 2, has been read
         if (!mbar_wait(smem_u32(&bars->kfull[s]), (j >> 1) & 1, abort_flag) ||
             (j >= 2 && !mbar_wait(smem_u32(&bars->sfree[s]), ((j - 2) >> 1) & 1, abort_flag))) {
           ok = false;
@@ -371,13 +378,39 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         mma_commit(smem_u32(&bars->sfull[s]));
         mma_commit(smem_u32(&bars->kempty[s]));
-        if (j >= 1) ok = pv(j - 1);
       }
-      if (ok) ok = pv(n_kt - 1);
       if (!ok) at_fail(bars, check);
-      mma_commit(smem_u32(&bars->ofinal));   // after a failure too: every issued MMA has finished
+      mma_commit(smem_u32(&bars->qkdrain));   // every QK^T issued above has finished ...
       volatile int never = 0;
-      mbar_wait(smem_u32(&bars->ofinal), 0, &never);   // ... before the CTA frees its TMEM
+      mbar_wait(smem_u32(&bars->qkdrain), 0, &never);   // ... before the CTA frees its TMEM
+    }
+  } else if (warp == kWarpPv) {
+    // ---------------------------------------------------------------- P V issuer (its own thread:
+    // a P V never waits behind a QK^T issue; the two write disjoint TMEM, O and P against S)
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
+      bool ok = true;
+      for (int jj = 0; ok && jj < n_kt; ++jj) {
+        const int s = jj & 1;
+        if (!mbar_wait(smem_u32(&bars->pfull[s]), (jj >> 1) & 1, abort_flag) ||
+            !mbar_wait(smem_u32(&bars->vfull[s]), (jj >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // V tile: 128 key rows (K) x 128 value columns (N) in two 64-column boxes, MN-major
+        const uint64_t vd = sdesc_sw128(sbase + kOffV + s * 2 * kBox, kBox, 1024);
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          mma_ts(tmem + kTmO, tmem + kTmP + 64 * s + 8 * k, vd + (uint64_t)(128 * k), idesc_pv,
+                 (jj > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bars->vempty[s]));
+        mma_commit(smem_u32(&bars->pdone[s]));
+      }
+      if (!ok) at_fail(bars, check);
+      mma_commit(smem_u32(&bars->ofinal));   // after a failure too: every issued P V has finished
+      volatile int never = 0;
+      mbar_wait(smem_u32(&bars->ofinal), 0, &never);
     }
   } else {
     // ---------------------------------------------------------------- softmax: thread = query row
@@ -420,15 +453,13 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->sfree[s]));
-      float mx = -INFINITY;
-      const bool masked = kTile * j + kTile - 1 > p_first;
+      if (kTile * j + kTile - 1 > p_first) {           // a tile on the diagonal: hide keys past the row
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) {
-        const float v = (masked && kTile * j + c > lim) ? -INFINITY : __uint_as_float(x[c]) * scale_log2;
-        x[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < kTile; ++c)
+          if (kTile * j + c > lim) x[c] = __float_as_uint(-INFINITY);
       }
-      const float m_new = fmaxf(m_ref, mx);
+      // the scale is positive, so the maximum of the raw scores gives the scaled one
+      const float m_new = fmaxf(m_ref, max128(x) * scale_log2);
       if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleLog2)) {
         const float alpha = ex2_approx(m_ref - m_new);
         l *= alpha;
@@ -437,13 +468,18 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pdone[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
+          const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll 1
           for (int g = 0; g < 4; ++g) {
             uint32_t o[32];
             tmem_ld32(tmem + lane_off + kTmO + 32 * g, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            for (int i = 0; i < 16; ++i) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), al2);
+              o[2 * i] = __float_as_uint(v.x);
+              o[2 * i + 1] = __float_as_uint(v.y);
+            }
             tmem_st32(tmem + lane_off + kTmO + 32 * g, o);
           }
           tmem_st_wait();
@@ -454,19 +490,26 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (!ok) break;
         tc_fence_after();
       }
-      float sum = 0.0f;
+      // p = 2^(score * scale_log2 - m): one packed FMA per pair, four independent partial sums
+      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m_ref, -m_ref);
+      float2 ps[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ps[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float a = ex2_approx(__uint_as_float(x[64 * hf + 2 * c]) - m_ref);
-          const float bb = ex2_approx(__uint_as_float(x[64 * hf + 2 * c + 1]) - m_ref);
-          sum += a + bb;
-          pk[c] = bf16x2(a, bb);
+          const float2 d = __ffma2_rn(make_float2(__uint_as_float(x[64 * hf + 2 * c]),
+                                                  __uint_as_float(x[64 * hf + 2 * c + 1])), sc2, nm2);
+          const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
+          ps[c & 3] = __fadd2_rn(ps[c & 3], pp);
+          pk[c] = bf16x2(pp.x, pp.y);
         }
         tmem_st32(tmem + lane_off + kTmP + 64 * s + 32 * hf, pk);
       }
+      const float2 sum2 = __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3]));
+      const float sum = sum2.x + sum2.y;
       l += sum;
       tmem_st_wait();
       tc_fence_before();
@@ -557,7 +600,7 @@ size_t prefill_workspace_bytes(int n_h, int batch, int max_ctx) {
 cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_start, const int32_t* q_len, int total_q,
                            int max_q, const int32_t* ctx_len, int batch, int max_ctx, const int32_t* block_table,
                            int bt_stride, const void* cache, int num_pages, void* workspace, void* out,
-                           cudaStream_t st) {
+                           cudaStream_t st, cudaEvent_t between) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(expand_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kExSmem);
@@ -582,6 +625,7 @@ cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_star
                  *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv), static_cast<const __nv_bfloat16*>(cache), ctx_len,
                  n_h, max_ctx, block_table, bt_stride, num_pages, lpad, kn, vv, kr, h.check_word);
   if (e != cudaSuccess) return e;
+  if (between && (e = cudaEventRecord(between, st)) != cudaSuccess) return e;   // profiling: splits the two kernels
   const float scale_log2 = h.scale * 1.4426950408889634f;
   return launch_pdl(prefill_attn_kernel, dim3((max_q + kQBlk - 1) / kQBlk, n_h, batch), dim3(kAtThreads), kAtSmem, st,
                     tm_q, tm_kn, tm_v, tm_kr, q_start, q_len, total_q, max_q, ctx_len, n_h, max_ctx, block_table,
