@@ -10,8 +10,9 @@
 //   1. expand_tc_kernel: for every cached row t of a sequence and head h,
 //        K_nope[b][h][t] = W_UK[h] c_t,   V[b][h][t] = W_UV[h] c_t     (bf16),
 //      and the (already rotated) RoPE key K_r[b][t] copied once per token;
-//      CTA = (head, 128 tokens): D[128 tokens][256] = C[128][512] . [W_UK[h] ; W_UV[h]]^T,
-//      A = two cache pages by TMA, B = the head's weight rows, K-major, 4-stage ring.
+//      item = (head, 128 tokens): D[128 tokens][256] = C[128][512] . [W_UK[h] ; W_UV[h]]^T,
+//      A = two cache pages by TMA, B = the head's weight rows, K-major, 4-stage ring;
+//      persistent CTAs, two TMEM accumulators (the epilogue of an item under the next's MMAs).
 //   2. prefill_attn_kernel: CTA = (128 queries, head, sequence); query i of sequence b sits at
 //      position ctx_len - q_len + i and sees keys 0 .. that position.  Per 128-key tile j:
 //        S = Q K^T (M = 128 queries, N = 128 keys, K = 128 + 64) into one of two TMEM score
@@ -48,7 +49,9 @@ constexpr int kExSmem = kExStages * kExStageBytes + 1024 + 1024;
 struct ExBars {
   uint64_t full[kExStages];
   uint64_t empty[kExStages];
-  uint64_t done;
+  uint64_t acc_full[2];      // the MMAs of an item are done: its accumulator may be read
+  uint64_t acc_empty[2];     // the epilogue has read the accumulator (4 warps arrive)
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -60,11 +63,38 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ bool page_ok(int p, int num_pages) { return p >= 0 && p < num_pages; }
 
+// One expansion item: 128 tokens of a sequence for one head.  Items are numbered with the head
+// fastest, so the CTAs working at the same time share the token tile (its cache rows stay in L2).
+struct ExItem {
+  int h, t0, b, L, p0, p1;
+  bool valid, ok0, ok1;
+};
+
+__device__ __forceinline__ ExItem ex_item(int idx, int n_h, int ntb, const int32_t* ctx_len, int max_ctx,
+                                          const int32_t* block_table, int bt_stride, int num_pages) {
+  ExItem it;
+  it.h = idx % n_h;
+  const int tb = (idx / n_h) % ntb;
+  it.b = idx / (n_h * ntb);
+  it.t0 = tb * kTile;
+  it.L = ctx_len[it.b];
+  it.valid = it.L >= 1 && it.L <= max_ctx && it.t0 < it.L;   // the attention kernel flags bad lengths
+  const bool need1 = it.t0 + kPage < it.L;
+  it.p0 = it.valid ? block_table[(size_t)it.b * bt_stride + 2 * tb] : -1;
+  it.p1 = it.valid && need1 ? block_table[(size_t)it.b * bt_stride + 2 * tb + 1] : -1;
+  it.ok0 = it.valid && page_ok(it.p0, num_pages);
+  it.ok1 = it.valid && need1 && page_ok(it.p1, num_pages);
+  return it;
+}
+
+// Persistent: CTA c takes items c, c + gridDim.x, ...; the K-chunk ring runs on across items and
+// the accumulator alternates between two 256-column TMEM halves, so the epilogue of one item
+// overlaps the loads and MMAs of the next.
 __global__ void __launch_bounds__(kExThreads, 1)
 expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_wuk,
                  const __grid_constant__ CUtensorMap tm_wuv, const __nv_bfloat16* __restrict__ cache,
                  const int32_t* __restrict__ ctx_len, int n_h, int max_ctx, const int32_t* __restrict__ block_table,
-                 int bt_stride, int num_pages, int lpad, __nv_bfloat16* __restrict__ kn,
+                 int bt_stride, int num_pages, int lpad, int n_items, __nv_bfloat16* __restrict__ kn,
                  __nv_bfloat16* __restrict__ vv, __nv_bfloat16* __restrict__ kr, unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -73,58 +103,57 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
   ExBars* bars = reinterpret_cast<ExBars*>(smem + kExStages * kExStageBytes);
   volatile int* abort_flag = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x, tb = blockIdx.y, b = blockIdx.z;
-  griddep_wait();                          // the rows may have been appended by the previous kernel
-  griddep_launch_dependents();
-  const int L = ctx_len[b];
-  const int t0 = tb * kTile;
-  if (L < 1 || L > max_ctx || t0 >= L) return;   // the attention kernel flags invalid lengths
-  const bool need1 = t0 + kPage < L;
-  const int p0 = block_table[(size_t)b * bt_stride + 2 * tb];
-  const int p1 = need1 ? block_table[(size_t)b * bt_stride + 2 * tb + 1] : -1;
-  const bool ok0 = page_ok(p0, num_pages), ok1 = need1 && page_ok(p1, num_pages);
-  if (tid == 0 && (!ok0 || (need1 && !ok1))) atomicOr(check, kCheckPageId);
-
+  const int ntb = lpad / kTile;
   if (tid == 0) {
     for (int i = 0; i < kExStages; ++i) {
       mbar_init(smem_u32(&bars->full[i]), 1);
       mbar_init(smem_u32(&bars->empty[i]), 1);
     }
-    mbar_init(smem_u32(&bars->done), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->acc_full[i]), 1);
+      mbar_init(smem_u32(&bars->acc_empty[i]), 4);
+    }
+    mbar_init(smem_u32(&bars->drain), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) { tmem_alloc(smem_u32(&bars->tmem_base), 256); tmem_relinquish(); }
+  if (warp == 5) { tmem_alloc(smem_u32(&bars->tmem_base), 512); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  griddep_wait();                          // the rows may have been appended by the previous kernel
+  griddep_launch_dependents();
 
   if (warp == 4) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       prefetch_tmap(&tm_cache);
-      const uint32_t bytes = (ok0 ? kPageBox : 0) + (ok1 ? kPageBox : 0) + 2 * kBox;
-      int issued = 0;
+      int c = 0;                           // K chunks issued so far (ring position)
       bool ok = true;
-      for (int kc = 0; kc < kDc / 64; ++kc) {
-        const int s = kc % kExStages;
-        if (kc >= kExStages && !mbar_wait(smem_u32(&bars->empty[s]), ((kc / kExStages) - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+        const ExItem it = ex_item(idx, n_h, ntb, ctx_len, max_ctx, block_table, bt_stride, num_pages);
+        if (!it.valid) continue;
+        if (it.h == 0 && (!it.ok0 || (it.t0 + kPage < it.L && !it.ok1))) atomicOr(check, kCheckPageId);
+        const uint32_t bytes = (it.ok0 ? kPageBox : 0) + (it.ok1 ? kPageBox : 0) + 2 * kBox;
+        for (int kc = 0; kc < kDc / 64; ++kc, ++c) {
+          const int s = c % kExStages;
+          if (c >= kExStages && !mbar_wait(smem_u32(&bars->empty[s]), ((c / kExStages) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = sbase + s * kExStageBytes, fb = smem_u32(&bars->full[s]);
+          mbar_arrive_expect_tx(fb, bytes);
+          if (it.ok0) tma_load_2d(st, &tm_cache, 64 * kc, it.p0 * kPage, fb);
+          if (it.ok1) tma_load_2d(st + kPageBox, &tm_cache, 64 * kc, it.p1 * kPage, fb);
+          tma_load_2d(st + 2 * kPageBox, &tm_wuk, 64 * kc, kDn * it.h, fb);
+          tma_load_2d(st + 2 * kPageBox + kBox, &tm_wuv, 64 * kc, kDv * it.h, fb);
         }
-        const uint32_t st = sbase + s * kExStageBytes, fb = smem_u32(&bars->full[s]);
-        mbar_arrive_expect_tx(fb, bytes);
-        if (ok0) tma_load_2d(st, &tm_cache, 64 * kc, p0 * kPage, fb);
-        if (ok1) tma_load_2d(st + kPageBox, &tm_cache, 64 * kc, p1 * kPage, fb);
-        tma_load_2d(st + 2 * kPageBox, &tm_wuk, 64 * kc, kDn * h, fb);
-        tma_load_2d(st + 2 * kPageBox + kBox, &tm_wuv, 64 * kc, kDv * h, fb);
-        issued = kc + 1;
       }
       if (!ok && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
-      for (int kc = max(0, issued - kExStages); kc < issued; ++kc) {   // every copy lands before exit
+      for (int k = max(0, c - kExStages); k < c; ++k) {   // every copy lands before exit
         volatile int never = 0;
-        mbar_wait(smem_u32(&bars->full[kc % kExStages]), (kc / kExStages) & 1, &never);
+        mbar_wait(smem_u32(&bars->full[k % kExStages]), (k / kExStages) & 1, &never);
       }
     }
   } else if (warp == 5) {
@@ -132,52 +161,73 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
     if (lane == 0) {
       // M = 128 tokens, N = 256 (the head's 128 W_UK rows, then its 128 W_UV rows), both K-major
       constexpr uint32_t idesc = idesc_bf16_f32(128, 256, false, false);
+      int c = 0, v = 0;                    // K chunks consumed, items accumulated
       bool ok = true;
-      for (int kc = 0; kc < kDc / 64; ++kc) {
-        const int s = kc % kExStages;
-        if (!mbar_wait(smem_u32(&bars->full[s]), (kc / kExStages) & 1, abort_flag)) { ok = false; break; }
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+        const ExItem it = ex_item(idx, n_h, ntb, ctx_len, max_ctx, block_table, bt_stride, num_pages);
+        if (!it.valid) continue;
+        const int a = v & 1;
+        // the accumulator's previous item (v - 2) has been read by the epilogue
+        if (v >= 2 && !mbar_wait(smem_u32(&bars->acc_empty[a]), ((v >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t st = sbase + s * kExStageBytes;
-        const uint64_t a = sdesc_sw128(st, 16, 1024), w = sdesc_sw128(st + 2 * kPageBox, 16, 1024);
+        for (int kc = 0; kc < kDc / 64; ++kc, ++c) {
+          const int s = c % kExStages;
+          if (!mbar_wait(smem_u32(&bars->full[s]), (c / kExStages) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = sbase + s * kExStageBytes;
+          const uint64_t ad = sdesc_sw128(st, 16, 1024), wd = sdesc_sw128(st + 2 * kPageBox, 16, 1024);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)          // 16 latent columns per MMA: 32-byte steps in the 128-byte row
-          mma_ss(tmem, a + (uint64_t)(2 * k), w + (uint64_t)(2 * k), idesc, (kc > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bars->empty[s]));
+          for (int k = 0; k < 4; ++k)        // 16 latent columns per MMA: 32-byte steps in the 128-byte row
+            mma_ss(tmem + 256 * a, ad + (uint64_t)(2 * k), wd + (uint64_t)(2 * k), idesc, (kc > 0 || k > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bars->empty[s]));
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&bars->acc_full[a]));
+        ++v;
       }
       if (!ok && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
-      mma_commit(smem_u32(&bars->done));     // also after a failure: every issued MMA has finished
+      mma_commit(smem_u32(&bars->drain));    // every issued MMA has finished ...
       volatile int never = 0;
-      mbar_wait(smem_u32(&bars->done), 0, &never);     // ... before the CTA frees its TMEM
+      mbar_wait(smem_u32(&bars->drain), 0, &never);   // ... before the CTA frees its TMEM
     }
   } else {
     // ---------------------------------------------------------------- epilogue: thread = token
-    const int r = 32 * warp + lane, t = t0 + r;
-    const bool row_ok = t < L && (r < kPage ? ok0 : ok1);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort_flag) && !*abort_flag);
-    tc_fence_after();
     const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    uint4* dk = reinterpret_cast<uint4*>(kn + (((size_t)b * n_h + h) * lpad + t) * kDn);
-    uint4* dv = reinterpret_cast<uint4*>(vv + (((size_t)b * n_h + h) * lpad + t) * kDv);
-    if (ok) {
+    const int r = 32 * warp + lane;
+    int v = 0;
+    for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
+      const ExItem it = ex_item(idx, n_h, ntb, ctx_len, max_ctx, block_table, bt_stride, num_pages);
+      if (!it.valid) continue;
+      const int a = v & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->acc_full[a]), (v >> 1) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const int t = it.t0 + r;
+      const bool row_ok = t < it.L && (r < kPage ? it.ok0 : it.ok1);
+      uint4* dk = reinterpret_cast<uint4*>(kn + (((size_t)it.b * n_h + it.h) * lpad + t) * kDn);
+      uint4* dv = reinterpret_cast<uint4*>(vv + (((size_t)it.b * n_h + it.h) * lpad + t) * kDv);
 #pragma unroll 1
       for (int g = 0; g < 8; ++g) {          // columns 32 g .. 32 g + 31: K_nope for g < 4, V after
-        uint32_t v[32];
-        tmem_ld32(lane_addr + 32 * g, v);
+        uint32_t x[32];
+        tmem_ld32(lane_addr + 256 * a + 32 * g, x);
         tmem_ld_wait();
         uint4* d = (g < 4 ? dk : dv) + 4 * (g & 3);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          d[i] = row_ok ? make_uint4(bf16x2(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
-                                     bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
-                                     bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
-                                     bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])))
+          d[i] = row_ok ? make_uint4(bf16x2(__uint_as_float(x[8 * i]), __uint_as_float(x[8 * i + 1])),
+                                     bf16x2(__uint_as_float(x[8 * i + 2]), __uint_as_float(x[8 * i + 3])),
+                                     bf16x2(__uint_as_float(x[8 * i + 4]), __uint_as_float(x[8 * i + 5])),
+                                     bf16x2(__uint_as_float(x[8 * i + 6]), __uint_as_float(x[8 * i + 7])))
                         : make_uint4(0u, 0u, 0u, 0u);
       }
-      if (h == 0) {                          // the RoPE key, shared by the heads, once per token
-        uint4* d = reinterpret_cast<uint4*>(kr + ((size_t)b * lpad + t) * kDr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[a]));
+      if (it.h == 0) {                       // the RoPE key, shared by the heads, once per token
+        uint4* d = reinterpret_cast<uint4*>(kr + ((size_t)it.b * lpad + t) * kDr);
         if (row_ok) {
           const uint4* src = reinterpret_cast<const uint4*>(
-              cache + ((size_t)(r < kPage ? p0 : p1) * kPage + (r & (kPage - 1))) * kRow + kDc);
+              cache + ((size_t)(r < kPage ? it.p0 : it.p1) * kPage + (r & (kPage - 1))) * kRow + kDc);
 #pragma unroll
           for (int i = 0; i < kDr / 8; ++i) d[i] = src[i];
         } else {
@@ -185,12 +235,13 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
           for (int i = 0; i < kDr / 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
+      ++v;
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 256);
+  if (warp == 5) tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------ attention
@@ -620,10 +671,11 @@ cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_star
   if ((e = rows_map_2d(kn, (long long)batch * n_h * lpad, kDn, &tm_kn)) != cudaSuccess) return e;
   if ((e = rows_map_2d(vv, (long long)batch * n_h * lpad, kDv, &tm_v)) != cudaSuccess) return e;
   if ((e = rows_map_2d(kr, (long long)batch * lpad, kDr, &tm_kr)) != cudaSuccess) return e;
-  e = launch_pdl(expand_tc_kernel, dim3(n_h, lpad / kTile, batch), dim3(kExThreads), kExSmem, st,
+  const int n_items = n_h * (lpad / kTile) * batch;
+  e = launch_pdl(expand_tc_kernel, dim3(min(n_items, h.num_sms)), dim3(kExThreads), kExSmem, st,
                  *reinterpret_cast<const CUtensorMap*>(h.tmap), *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk),
                  *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv), static_cast<const __nv_bfloat16*>(cache), ctx_len,
-                 n_h, max_ctx, block_table, bt_stride, num_pages, lpad, kn, vv, kr, h.check_word);
+                 n_h, max_ctx, block_table, bt_stride, num_pages, lpad, n_items, kn, vv, kr, h.check_word);
   if (e != cudaSuccess) return e;
   if (between && (e = cudaEventRecord(between, st)) != cudaSuccess) return e;   // profiling: splits the two kernels
   const float scale_log2 = h.scale * 1.4426950408889634f;
