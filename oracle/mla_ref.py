@@ -357,6 +357,53 @@ def stored_row_e4m3(row_bf16_bits, pos, d_c, base, scale):
     return encode(vals / np.float32(scale))
 
 
+FP8_BLOCK = 128          # latent values per scale in the per-block FP8 format
+
+
+def stored_row_fp8_block(row_bf16_bits, pos, d_c, base):
+    """The 656 bytes a per-block-scaled FP8 cache holds for one appended row.
+
+    "G5 MLA KV 访存建模设计规格" 附录 A (FlashMLA row): the deployed FP8 cache
+    holds 656 bytes per token with per-block scales, against 576 for the pure
+    latent; the page does not break the 656 down.  Reading taken (it sums to
+    656 exactly): ``[512 e4m3 latent codes | 4 fp32 scales, one per 128 latent
+    values | 64 bf16 RoPE-key values]``.  A block's scale is its largest
+    magnitude divided by 448 (the largest e4m3 magnitude) in float32, 0 for an
+    all-zero block; each latent value is divided by its block's scale in float32
+    and encoded e4m3 nearest-even, saturating; the RoPE key is rotated and
+    rounded to bf16 exactly as in :func:`stored_row_bf16` (not quantised).
+    Input [..., 576] bf16 bits; returns uint8 [..., 656].
+    """
+    from .e4m3 import encode
+    bits = np.asarray(row_bf16_bits, np.uint16)
+    lead = bits.shape[:-1]
+    x = bf16_to_f64(bits).astype(np.float32).reshape(-1, bits.shape[-1])
+    n, nb = x.shape[0], d_c // FP8_BLOCK
+    lat = x[:, :d_c].reshape(n, nb, FP8_BLOCK)
+    scale = (np.max(np.abs(lat), axis=2) / np.float32(448.0)).astype(np.float32)          # [n, nb]
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    codes = np.where(scale[:, :, None] > 0, encode(lat / safe[:, :, None]), np.uint8(0)).astype(np.uint8)
+    rope = bf16_round(rope_row_fp32(x[:, d_c:], np.asarray(pos).reshape(-1) if np.ndim(pos) else pos, base))
+    out = np.concatenate([codes.reshape(n, d_c), scale.astype("<f4").view(np.uint8).reshape(n, 4 * nb),
+                          rope.astype("<u2").view(np.uint8).reshape(n, -1)], axis=1)
+    return out.reshape(lead + (out.shape[-1],))
+
+
+def fp8_block_values(stored, d_c):
+    """float64 values of per-block FP8 rows (see :func:`stored_row_fp8_block`): each latent
+    code's value times its block's scale, then the bf16 RoPE key.  Returns [..., d_c + d_rope]."""
+    from .e4m3 import decode
+    st = np.asarray(stored, np.uint8)
+    lead = st.shape[:-1]
+    st = st.reshape(-1, st.shape[-1])
+    nb = d_c // FP8_BLOCK
+    scale = np.ascontiguousarray(st[:, d_c:d_c + 4 * nb]).view("<f4").astype(np.float64)       # [n, nb]
+    lat = decode(st[:, :d_c]).reshape(-1, nb, FP8_BLOCK) * scale[:, :, None]
+    rope = bf16_to_f64(np.ascontiguousarray(st[:, d_c + 4 * nb:]).view("<u2"))
+    out = np.concatenate([lat.reshape(-1, d_c), rope], axis=1)
+    return out.reshape(lead + (out.shape[-1],))
+
+
 # ---------------------------------------------------------------------------
 # byte accounting
 # ---------------------------------------------------------------------------

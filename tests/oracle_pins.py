@@ -264,9 +264,52 @@ def pin_mha_ratio_and_read_bytes(ref):
     assert ref.decode_kv_read_bytes(3, [5, 6, 7], 512, 64, 1) == 18 * 576
 
 
+def pin_fp8_block_format(ref):
+    """The per-block FP8 row: 656 bytes per token, the pages' figure against 576 for the pure
+    latent; in every non-zero block the largest magnitude lands exactly on the largest e4m3
+    code and every value within e4m3's half-step of its block; a block's scale belongs to that
+    block alone (a power-of-two change of one block's values moves only its scale); the RoPE
+    key is the bf16 cache's, not quantised; an all-zero block is zeros."""
+    g = load_golden("fp8_block_format.json")
+    rng = np.random.default_rng(31)
+    n = 6
+    x = rng.standard_normal((n, 576)) * np.array([1.0, 30.0, 1e-3, 7.0] * 128 + [1.0] * 64)[None, :]
+    x[3, 128:256] = 0.0                                              # an all-zero block
+    bits = ref.bf16_round(x.astype(np.float32))
+    pos = np.arange(n) * 37
+    st = ref.stored_row_fp8_block(bits, pos, 512, BASE)
+    assert st.shape == (n, g["bytes_per_token"]) and 512 + 64 == g["pure_latent_bytes_per_token"]
+    codes = st[:, :512].reshape(n, 4, 128)
+    vals = ref.fp8_block_values(st, 512)
+    xv = ref.bf16_to_f64(bits)
+    for r in range(n):
+        for k in range(4):
+            blk = xv[r, 128 * k:128 * (k + 1)]
+            if not np.any(blk):
+                assert not np.any(codes[r, k]) and not np.any(vals[r, 128 * k:128 * (k + 1)])
+                continue
+            mag = codes[r, k] & 0x7F
+            assert mag.max() == 0x7E and mag[np.argmax(np.abs(blk))] == 0x7E
+            sc = np.max(np.abs(blk)) / 448.0
+            err = np.abs(vals[r, 128 * k:128 * (k + 1)] - blk)
+            assert np.all(err <= 2.0 ** -4 * np.abs(blk) * (1 + 2.0 ** -20) + sc * 2.0 ** -10)
+    # one block scaled by 4: only that block's scale moves (times 4); every code stays
+    y = xv.copy()
+    y[:, 256:384] *= 4.0
+    st4 = ref.stored_row_fp8_block(ref.bf16_round(y.astype(np.float32)), pos, 512, BASE)
+    assert np.array_equal(st4[:, :512], st[:, :512])
+    s1 = np.ascontiguousarray(st[:, 512:528]).view("<f4")
+    s4 = np.ascontiguousarray(st4[:, 512:528]).view("<f4")
+    assert np.array_equal(s4[:, [0, 1, 3]], s1[:, [0, 1, 3]]) and np.array_equal(s4[:, 2], 4 * s1[:, 2])
+    # the RoPE key: the bf16 cache's codes
+    bf = ref.stored_row_bf16(bits, pos, 512, BASE)
+    assert np.array_equal(np.ascontiguousarray(st[:, 528:]).view("<u2"), bf[:, 512:])
+    assert np.array_equal(vals[:, 512:], ref.bf16_to_f64(bf[:, 512:]))
+
+
 ALL_PINS = [
     pin_rope_closed_forms, pin_rope_relative_position, pin_scale_worked_example,
     pin_naive_equals_absorbed, pin_rope_on_content_breaks_absorption, pin_closed_forms,
     pin_split_lse_identity, pin_one_shot_equals_incremental, pin_prefill_rows_are_decodes, pin_cache_bytes,
-    pin_mha_ratio_and_read_bytes,
+    pin_mha_ratio_and_read_bytes, pin_fp8_block_format,
 ]

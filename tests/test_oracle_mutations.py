@@ -103,6 +103,29 @@ def _prefill_with(strict_mask=False, chunk_position=False):
     return prefill
 
 
+def _fp8_block_with(per_row=False, sat=448.0, quantise_rope=False):
+    from oracle import e4m3
+
+    def stored(row_bf16_bits, pos, d_c, base):
+        bits = np.asarray(row_bf16_bits, np.uint16).reshape(-1, 576)
+        x = mla_ref.bf16_to_f64(bits).astype(np.float32)
+        n = x.shape[0]
+        lat = x[:, :d_c].reshape(n, 4, 128)
+        amax = np.max(np.abs(lat), axis=2)
+        if per_row:
+            amax = np.repeat(np.max(amax, axis=1, keepdims=True), 4, axis=1)
+        scale = (amax / np.float32(sat)).astype(np.float32)
+        safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+        codes = np.where(scale[:, :, None] > 0, e4m3.encode(lat / safe[:, :, None]), 0).astype(np.uint8)
+        rr = mla_ref.rope_row_fp32(x[:, d_c:], np.asarray(pos).reshape(-1) if np.ndim(pos) else pos, base)
+        if quantise_rope:
+            rr = e4m3.decode(e4m3.encode(rr)).astype(np.float32)
+        rope = mla_ref.bf16_round(rr)
+        return np.concatenate([codes.reshape(n, d_c), scale.astype("<f4").view(np.uint8).reshape(n, 16),
+                               rope.astype("<u2").view(np.uint8).reshape(n, -1)], axis=1)
+    return stored
+
+
 MUTATIONS = {
     "rope_rotates_backwards": ("rope", _rope_with(sign=-1.0)),
     "rope_frequency_step_1": ("rope", _rope_with(freq_step=1)),
@@ -113,6 +136,9 @@ MUTATIONS = {
     "naive_drops_rope_key": ("naive_decode", _naive_without_rope_key),
     "softmax_unnormalised": ("softmax", _softmax_unnormalised),
     "causal_mask_missing": ("causal_forward_naive", _causal_unmasked),
+    "fp8_block_one_scale_per_row": ("stored_row_fp8_block", _fp8_block_with(per_row=True)),
+    "fp8_block_saturation_127": ("stored_row_fp8_block", _fp8_block_with(sat=127.0)),
+    "fp8_block_rope_quantised": ("stored_row_fp8_block", _fp8_block_with(quantise_rope=True)),
     "prefill_mask_excludes_diagonal": ("prefill_naive", _prefill_with(strict_mask=True)),
     "prefill_queries_rotated_at_chunk_start": ("prefill_naive", _prefill_with(chunk_position=True)),
     "cache_bytes_without_rope": ("absorb_cache_bytes", lambda t, d_c, d_r, e: int(t) * int(d_c) * int(e)),
