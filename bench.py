@@ -87,16 +87,17 @@ def workload(name):
         wl.name = LAYER
         wl.extra["layer"] = inp
         return wl
+    if name in W.EXTRA:
+        return W.EXTRA[name]()
     if name not in W.NAMED:
-        raise SystemExit(f"unknown workload {name}; choose from {sorted(W.NAMED) + [LAYER, PREFILL]}")
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(W.NAMED) + sorted(W.EXTRA) + [LAYER, PREFILL]}")
     return W.NAMED[name]()
 
 
 def algorithmic(wl):
     """Bytes and FLOPs of one decode step (cache + W_UK + W_UV bytes; QK^T, P.c_kv, absorb, W_UV flops)."""
-    e = 1 if wl.cache_dtype == 2 else 2
     tokens = wl.total_tokens
-    cache = tokens * (wl.d_c + wl.d_rope) * e
+    cache = tokens * cache_bytes_per_token(wl)
     weights = 2 * wl.n_h * 128 * 512 * 2
     flops = 2 * wl.n_h * tokens * (576 + 512) + 4 * wl.B * wl.n_h * 128 * 512
     if "layer" in wl.extra:                            # + W_Q and W_DKV for the step's token
@@ -121,7 +122,12 @@ def prefill_flops(wl):
 
 
 def cache_bytes_per_token(wl):
-    return (wl.d_c + wl.d_rope) * (1 if wl.cache_dtype == 2 else 2)
+    from mla_absorbed_latent_decode_gb300 import workloads as W
+    return W.ROW_BYTES[wl.cache_dtype]          # 1152 bf16, 576 e4m3, 656 per-block e4m3 (+ scales, bf16 RoPE)
+
+
+def cache_name(wl):
+    return {1: "bf16", 2: "fp8_e4m3", 3: "fp8_e4m3_block"}[wl.cache_dtype]
 
 
 # ------------------------------------------------------------------ CPU oracle leg
@@ -149,7 +155,10 @@ def oracle_sample(wl, seconds):
         b = i % wl.B
         a, z = starts[b], starts[b + 1]
         if b not in cached:                 # the oracle's own cache contents (prefill, untimed)
-            if wl.cache_dtype == 2:
+            if wl.cache_dtype == 3:
+                st = mla_ref.stored_row_fp8_block(wl.rows[a:z], wl.row_pos[a:z], wl.d_c, wl.rope_base)
+                cached[b] = mla_ref.fp8_block_values(st, wl.d_c)
+            elif wl.cache_dtype == 2:
                 st = mla_ref.stored_row_e4m3(wl.rows[a:z], wl.row_pos[a:z], wl.d_c, wl.rope_base,
                                              np.float32(wl.fp8_scale))
                 cached[b] = e4m3.decode(st) * float(np.float32(wl.fp8_scale))
@@ -202,7 +211,7 @@ def run_reference(args):
         "ms_per_step": round(us_equiv / 1000.0, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "s_ctx": wl.max_ctx, "n_h": wl.n_h,
-                   "cache": "fp8_e4m3" if wl.cache_dtype == 2 else "bf16",
+                   "cache": cache_name(wl),
                    "note": "ms_per_step extrapolated from the sampled throughput to the whole batch"},
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s (latent KV)", "cores": blas_threads(), "kind": "oracle",
                          "sample": desc},
@@ -480,7 +489,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "s_ctx": wl.max_ctx, "n_h": wl.n_h, "d_c": wl.d_c,
-                       "d_rope": wl.d_rope, "cache": "fp8_e4m3" if wl.cache_dtype == 2 else "bf16",
+                       "d_rope": wl.d_rope, "cache": cache_name(wl),
                        "total_tokens": wl.total_tokens,
                        "l2": f"flushed between steps outside the timed events: write of {flush.numel() >> 20} MiB, "
                              f"then read of another {flush_rd.numel() >> 20} MiB (L2 left cold and clean); the "

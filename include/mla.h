@@ -69,7 +69,12 @@ typedef enum {
 
 typedef enum {
   MLA_CACHE_BF16 = 1,          /* 576 bf16 per row: 1152 bytes                  */
-  MLA_CACHE_FP8_E4M3 = 2       /* 576 OCP e4m3 bytes per row, one fp32 scale    */
+  MLA_CACHE_FP8_E4M3 = 2,      /* 576 OCP e4m3 bytes per row, one fp32 scale    */
+  MLA_CACHE_FP8_E4M3_BLOCK = 3 /* 656 bytes per row: 512 e4m3 latent codes, 4
+                                  fp32 scales (one per 128 latent values), 64
+                                  bf16 RoPE-key values ("G5 MLA KV 访存建模设计
+                                  规格" 附录 A: FlashMLA's FP8 row of 656 bytes
+                                  with per-block scales)                        */
 } mla_cache_dtype_t;
 
 /* Bits of the device check word (mla_get_status's *device_flags). */
@@ -98,7 +103,8 @@ typedef struct mla_config {
   float rope_base;      /* RoPE base (10000 for the configurations here).                 */
   float softmax_scale;  /* EXCEPTION: 0 means 1/sqrt(d_nope + d_rope).                    */
   float fp8_scale;      /* EXCEPTION: mandatory (> 0) only for MLA_CACHE_FP8_E4M3, where a
-                           stored code x represents x * fp8_scale; ignored for bf16.      */
+                           stored code x represents x * fp8_scale; ignored otherwise (the
+                           per-block format carries its scales in every row).             */
 } mla_config_t;
 
 /*
@@ -136,14 +142,18 @@ mla_status_t mla_destroy(mla_handle_t h);
  * cached; "80 行 PyTorch 从零写 DeepSeek 的 MLA" §2: keys rotated at their
  * absolute positions).  For an FP8 cache all d_c + d_rope stored values are
  * divided by fp8_scale in fp32 and encoded e4m3, nearest-even, saturating at
- * +-448.  The rotation is computed in fp32 with fp32 cos/sin, each product
- * and sum rounded separately.
+ * +-448.  For a per-block FP8 cache each block of 128 latent values gets the
+ * scale max|x| / 448 (fp32 division; 0 for an all-zero block, whose codes are
+ * 0), its values are divided by it in fp32 and encoded as above, and the RoPE
+ * key is stored in bf16 as in a bf16 cache.  The rotation is computed in fp32
+ * with fp32 cos/sin, each product and sum rounded separately.
  *
  *   rows         device [n][d_c + d_rope] bf16.
  *   seq, pos     device [n] int32.
  *   n            rows to write (0 is a no-op).
  *   block_table  device [bt_rows][bt_stride] int32 page ids.
- *   cache        device [num_pages][page_size][d_c + d_rope], bf16 or e4m3 bytes.
+ *   cache        device [num_pages][page_size][row], row = 1152 (bf16), 576 (e4m3) or
+ *                656 (per-block e4m3) bytes.
  *
  * Rows written by one call must target distinct slots.  Device checks: seq
  * outside [0, bt_rows), pos outside [0, max_position) or past the block-table
@@ -163,7 +173,8 @@ mla_status_t mla_kv_append(mla_handle_t h, const void* rows, const int32_t* seq,
  * hidden state to the [d_c | d_rope] row; the kv norm is the identity here), each value the
  * bf16 rounding of an fp32 sum, is then stored exactly as mla_kv_append stores a row (same
  * slot, rotation, encoding and device checks): the bytes equal those of mla_project into a
- * rows buffer followed by mla_kv_append.
+ * rows buffer followed by mla_kv_append.  A per-block FP8 cache is MLA_ERR_UNSUPPORTED here
+ * (its block scales need a whole row; use mla_project + mla_kv_append).
  *
  *   x            device [n][hidden] bf16, 16-byte aligned.
  *   hidden       a positive multiple of 256.

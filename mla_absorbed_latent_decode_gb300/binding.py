@@ -24,6 +24,7 @@ MLA_ERR_DEVICE_CHECK = 6
 
 MLA_CACHE_BF16 = 1
 MLA_CACHE_FP8_E4M3 = 2
+MLA_CACHE_FP8_E4M3_BLOCK = 3
 
 MLA_CHECK_CTX_LEN = 0x1
 MLA_CHECK_PAGE_ID = 0x2

@@ -59,7 +59,8 @@ mla_status_t check_config(const mla_config_t* c) {
     return fail(MLA_ERR_INVALID_ARG, "mla_config_t.rope_base = %g must be positive and finite", c->rope_base);
   if (c->softmax_scale < 0.0f || !std::isfinite(c->softmax_scale))
     return fail(MLA_ERR_INVALID_ARG, "mla_config_t.softmax_scale = %g must be >= 0 (0 selects 1/sqrt(d_nope + d_rope))", c->softmax_scale);
-  if (c->cache_dtype != MLA_CACHE_BF16 && c->cache_dtype != MLA_CACHE_FP8_E4M3)
+  if (c->cache_dtype != MLA_CACHE_BF16 && c->cache_dtype != MLA_CACHE_FP8_E4M3 &&
+      c->cache_dtype != MLA_CACHE_FP8_E4M3_BLOCK)
     return fail(MLA_ERR_INVALID_ARG, "mla_config_t.cache_dtype = %d is not an mla_cache_dtype_t", c->cache_dtype);
   if (c->cache_dtype == MLA_CACHE_FP8_E4M3) {
     if (c->fp8_scale == 0.0f)
@@ -274,6 +275,8 @@ mla_status_t mla_kv_project_append(mla_handle_t hh, const void* x, int32_t hidde
                 bt_rows, bt_stride, num_pages);
   if (!aligned(x, 16) || !aligned(w_dkv, 16) || !aligned(cache, 16))
     return fail(MLA_ERR_INVALID_ARG, "mla_kv_project_append: x, w_dkv and cache must be 16-byte aligned");
+  if (h->cfg.cache_dtype == MLA_CACHE_FP8_E4M3_BLOCK)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_kv_project_append: the per-block FP8 cache is written by mla_kv_append only");
   cudaError_t e = mla::launch_kv_project_append(*h, static_cast<const __nv_bfloat16*>(x), n, hidden,
                                                 static_cast<const __nv_bfloat16*>(w_dkv), seq, pos, block_table,
                                                 bt_rows, bt_stride, cache, num_pages,

@@ -4,12 +4,15 @@
 // key is rotated at the token's absolute position ("DeepSeek MLA 吸收式缓存：真实
 // 权重执行与 FlashMLA 架构边界" §2.4; rotation of interleaved pairs as in "80 行
 // PyTorch 从零写 DeepSeek 的 MLA" 附录 A).  An FP8 cache stores every value
-// divided by the tensor scale as OCP e4m3 (nearest even, saturating).
+// divided by the tensor scale as OCP e4m3 (nearest even, saturating).  A per-block
+// FP8 cache ("G5 MLA KV 访存建模设计规格" 附录 A: 656 bytes per token with per-block
+// scales) stores [512 e4m3 latent codes | 4 fp32 scales | 64 bf16 RoPE values]: each
+// block of 128 latent values is divided by its own scale max|x| / 448.
 //
 // One warp per row.  Lane l owns latent values [16 l, 16 l + 16) (32 bytes in,
-// 32 bytes (bf16) or 16 bytes (e4m3) out); lanes 0..3 also own RoPE values
-// [16 l, 16 l + 16) of the key.  HBM-bound: 1152 bytes read and 1152 (bf16) or
-// 576 (e4m3) bytes written per row.
+// 32 bytes (bf16) or 16 bytes (e4m3) out; the 8 lanes of a 128-value block find its
+// maximum by shuffles); lanes 0..3 also own RoPE values [16 l, 16 l + 16) of the key.
+// HBM-bound: 1152 bytes read and 1152 (bf16), 576 (e4m3) or 656 bytes written per row.
 #include "append_ops.cuh"
 #include "internal.cuh"
 #include "sm100_ptx.cuh"
@@ -17,7 +20,9 @@
 namespace mla {
 namespace {
 
-template <bool kFp8>
+enum AppendMode { kBf16 = 0, kFp8Tensor = 1, kFp8Block = 2 };
+
+template <int kMode>
 __global__ void __launch_bounds__(256) kv_append_kernel(
     const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ seq,
     const int32_t* __restrict__ pos, int n, const int32_t* __restrict__ block_table, int bt_rows,
@@ -39,23 +44,38 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     if (lane == 0) atomicOr(check, kCheckPageId);
     return;
   }
-  constexpr int kElem = kFp8 ? 1 : 2;
+  constexpr int kRowBytes = kMode == kBf16 ? kRow * 2 : kMode == kFp8Tensor ? kRow : kDc + 16 + 2 * kDr;
   const uint4* src = reinterpret_cast<const uint4*>(rows + (size_t)warp * kRow);
-  uint8_t* dst = cache + ((size_t)page * kPage + (p % kPage)) * (size_t)(kRow * kElem);
+  uint8_t* dst = cache + ((size_t)page * kPage + (p % kPage)) * (size_t)kRowBytes;
 
   // latent: values [16 lane, 16 lane + 16)
   const uint4 a = src[2 * lane];
   const uint4 b = src[2 * lane + 1];
-  if (!kFp8) {
+  if (kMode == kBf16) {
     reinterpret_cast<uint4*>(dst)[2 * lane] = a;
     reinterpret_cast<uint4*>(dst)[2 * lane + 1] = b;
   } else {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t o[4];
+    float scale = fp8_scale;
+    if (kMode == kFp8Block) {               // this lane's block: 128 values on lanes 8 k .. 8 k + 7
+      float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      o[i] = pack_e4m3x4(__fdiv_rn(bf16_lo(w[2 * i]), fp8_scale), __fdiv_rn(bf16_hi(w[2 * i]), fp8_scale),
-                         __fdiv_rn(bf16_lo(w[2 * i + 1]), fp8_scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), fp8_scale));
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+#pragma unroll
+      for (int off = 4; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      scale = __fdiv_rn(m, 448.0f);
+      if ((lane & 7) == 0) reinterpret_cast<float*>(dst + kDc)[lane >> 3] = scale;
+    }
+    uint32_t o[4];
+    if (kMode == kFp8Block && !(scale > 0.0f)) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = 0u;   // an all-zero block: zero codes
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        o[i] = pack_e4m3x4(__fdiv_rn(bf16_lo(w[2 * i]), scale), __fdiv_rn(bf16_hi(w[2 * i]), scale),
+                           __fdiv_rn(bf16_lo(w[2 * i + 1]), scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), scale));
+    }
     reinterpret_cast<uint4*>(dst)[lane] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 
@@ -68,11 +88,11 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     float r[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) rope_pair(bf16_lo(w[i]), bf16_hi(w[i]), cs[i], &r[2 * i], &r[2 * i + 1]);
-    if (!kFp8) {
+    if (kMode != kFp8Tensor) {             // bf16, after the latent (and, per-block, the 16 scale bytes)
       uint32_t o[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i] = pack_bf16(r[2 * i], r[2 * i + 1]);
-      uint4* d = reinterpret_cast<uint4*>(dst + kDc * kElem);
+      uint4* d = reinterpret_cast<uint4*>(dst + (kMode == kBf16 ? kDc * 2 : kDc + 16));
       d[2 * lane] = make_uint4(o[0], o[1], o[2], o[3]);
       d[2 * lane + 1] = make_uint4(o[4], o[5], o[6], o[7]);
     } else {
@@ -81,7 +101,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
       for (int i = 0; i < 4; ++i)
         o[i] = pack_e4m3x4(__fdiv_rn(r[4 * i], fp8_scale), __fdiv_rn(r[4 * i + 1], fp8_scale),
                            __fdiv_rn(r[4 * i + 2], fp8_scale), __fdiv_rn(r[4 * i + 3], fp8_scale));
-      reinterpret_cast<uint4*>(dst + kDc * kElem)[lane] = make_uint4(o[0], o[1], o[2], o[3]);
+      reinterpret_cast<uint4*>(dst + kDc)[lane] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
@@ -94,10 +114,14 @@ cudaError_t launch_kv_append(const Handle& h, const __nv_bfloat16* rows, const i
   const int threads = 256;
   const int blocks = (int)(((long long)n * 32 + threads - 1) / threads);
   if (h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3)
-    return launch_pdl(kv_append_kernel<true>, dim3(blocks), dim3(threads), 0, st, rows, seq, pos, n, block_table,
-                      bt_rows, bt_stride, static_cast<uint8_t*>(cache), num_pages, (const float2*)h.rope_cs,
-                      h.cfg.max_position, h.cfg.fp8_scale, h.check_word);
-  return launch_pdl(kv_append_kernel<false>, dim3(blocks), dim3(threads), 0, st, rows, seq, pos, n, block_table,
+    return launch_pdl(kv_append_kernel<kFp8Tensor>, dim3(blocks), dim3(threads), 0, st, rows, seq, pos, n,
+                      block_table, bt_rows, bt_stride, static_cast<uint8_t*>(cache), num_pages,
+                      (const float2*)h.rope_cs, h.cfg.max_position, h.cfg.fp8_scale, h.check_word);
+  if (h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3_BLOCK)
+    return launch_pdl(kv_append_kernel<kFp8Block>, dim3(blocks), dim3(threads), 0, st, rows, seq, pos, n,
+                      block_table, bt_rows, bt_stride, static_cast<uint8_t*>(cache), num_pages,
+                      (const float2*)h.rope_cs, h.cfg.max_position, 0.0f, h.check_word);
+  return launch_pdl(kv_append_kernel<kBf16>, dim3(blocks), dim3(threads), 0, st, rows, seq, pos, n, block_table,
                     bt_rows, bt_stride, static_cast<uint8_t*>(cache), num_pages, (const float2*)h.rope_cs,
                     h.cfg.max_position, 0.0f, h.check_word);
 }

@@ -66,7 +66,8 @@ using namespace sm100;
 constexpr int kStages = 4;                 // cache tiles in flight per CTA
 constexpr int kChunkBytes = kPage * 128;   // one 64-token x 64-column bf16 box (SW128): 8 KB
 constexpr int kRopeBytes = kPage * 64;     // one 64-token x 32-column bf16 box of the RoPE key (SW64): 4 KB
-constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes;
+constexpr int kScaleBytes = kPage * 16;   // per-block FP8 cache: the 4 fp32 block scales of 64 tokens: 1 KB
+constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes + kScaleBytes;
 constexpr int kQpeBytes = kMaxHeads * 64;              // 128 heads x 32 bf16 of the RoPE query, SW64 K-major
 constexpr int kSlots = 4;                              // partial-score receive slots
 constexpr int kSlotBytes = kMaxHeads * kPage * 2;      // 128 x 64 fp16 = 16 KB
@@ -78,7 +79,9 @@ constexpr int kOffXchg = kOffBars + 1024;             // running maxima / final 
 constexpr int kXchgBytes = 3 * 2 * kMaxHeads * 4;
 constexpr int kSmemBytes = kOffXchg + kXchgBytes + 1024;   // + alignment slack
 constexpr int kThreads = 352;                          // 2 tile groups of 4 warps, producer, 2 MMA warps
-constexpr int kThreadsFp8 = 512;                       // + 5 FP8 conversion warps
+constexpr int kThreadsFp8 = 512;                       // + 5 FP8 conversion warps (4 for the per-block format)
+// cache modes of the kernel: bf16 rows, e4m3 rows with one tensor scale, per-block e4m3 rows
+constexpr int kModeBf16 = 0, kModeFp8 = 1, kModeFp8Block = 2;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;                            // QK^T issuer (allocates TMEM)
 constexpr int kWarpPv = 10;                            // P . C issuer
@@ -92,7 +95,7 @@ constexpr uint32_t kTmP = 448;             // P slot b (64 bf16 per lane) at kTm
 
 struct Bars {                               // mbarriers (8 bytes each) and flags
   uint64_t full[kStages];                   // TMA tile landed                      (producer, tx)
-  uint64_t conv[kStages];                   // FP8 cache: tile converted to bf16    (5 conversion warps)
+  uint64_t conv[kStages];                   // FP8 cache: tile converted to bf16    (5 or 4 conversion warps)
   uint64_t empty[kStages];                  // tile consumed by P . C               (MMA commit)
   uint64_t sfull[2];                        // S_r(j) in TMEM, tile group j % 2     (MMA commit)
   uint64_t sfree[2];                        // S_r(j) loaded by its tile group      (4 warps)
@@ -166,18 +169,31 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
                     __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632));
 }
 
-// kFp8: the cache holds e4m3 codes.  The producer TMA-loads each 64 x 64 code box into the
+// Per-block FP8 cache: the exact values of four codes times their block scale, each product
+// rounded to fp32 and then to bf16 (nearest even); low half first, as above.
+__device__ __forceinline__ uint2 e4m3x4_scaled_to_bf16x4(uint32_t w, float scale) {
+  const float f0 = e4m3_at_top_to_f32(w << 24) * scale, f1 = e4m3_at_top_to_f32(w << 16) * scale;
+  const float f2 = e4m3_at_top_to_f32(w << 8) * scale, f3 = e4m3_at_top_to_f32(w) * scale;
+  return make_uint2(bf16x2_bits(f0, f1), bf16x2_bits(f2, f3));
+}
+
+// kMode != bf16: the cache holds e4m3 codes.  The producer TMA-loads each 64 x 64 code box into the
 // upper half of the 8 KB slot its bf16 chunk will occupy; one conversion warp per box converts
 // it in place (all its reads, then all its writes) before QK^T may use the tile.  The tensor
-// scale is folded into the softmax scale and the output scale by the launcher.
-template <bool kFp8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
+// scale is folded into the softmax scale and the output scale by the launcher.  The per-block
+// format brings each page's block scales in a 1 KB box and its RoPE key already in bf16: four
+// warps convert the latent boxes, each value times its token's block scale.
+template <int kMode>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMode != kModeBf16 ? kThreadsFp8 : kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_rope,
+                 const __grid_constant__ CUtensorMap tmap_scale,
                  const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_qpe,
                  const __grid_constant__ CUtensorMap tmap_o,
                  const int32_t* __restrict__ ctx_len, int n_h,
                  const int32_t* __restrict__ block_table, int bt_stride, int num_pages, float scale_log2,
                  float out_scale, Workspace ws, unsigned* check) {
+  constexpr bool kFp8 = kMode != kModeBf16;            // e4m3 codes, converted in shared memory
+  constexpr bool kBlock = kMode == kModeFp8Block;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base: swizzle atoms and TMA destinations need it
   const uint32_t raw = smem_u32(smem_raw);
@@ -197,7 +213,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
       mbar_init(smem_u32(&bars->empty[s]), 1);
-      mbar_init(smem_u32(&bars->conv[s]), 5);
+      mbar_init(smem_u32(&bars->conv[s]), kBlock ? 4 : 5);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->sfull[i]), 1);
@@ -217,6 +233,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   if (warp == kWarpProducer && lane == 0) {
     prefetch_tmap(&tmap);
     prefetch_tmap(&tmap_rope);
+    if (kBlock) prefetch_tmap(&tmap_scale);
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_qpe);
     prefetch_tmap(&tmap_o);
@@ -241,12 +258,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       page = 0;
     }
     const uint32_t full = smem_u32(&bars->full[s]);
-    mbar_arrive_expect_tx(full, (uint32_t)(kFp8 ? kStageBytes / 2 : kStageBytes));
+    constexpr uint32_t kTx = kBlock ? 2 * kChunkBytes + kRopeBytes + kScaleBytes
+                                    : (kFp8 ? 2 * kChunkBytes + kRopeBytes / 2 : 4 * kChunkBytes + kRopeBytes);
+    mbar_arrive_expect_tx(full, kTx);
     for (int c = 0; c < 4; ++c)            // FP8: each code box into the upper half of its chunk slot
       tma_load_2d(stage0 + s * kStageBytes + c * kChunkBytes + (kFp8 ? kChunkBytes / 2 : 0), &tmap,
                   (int)(rank * 256 + c * 64), page * kPage, full);
-    tma_load_2d(stage0 + s * kStageBytes + 4 * kChunkBytes + (kFp8 ? kRopeBytes / 2 : 0), &tmap_rope,
-                (int)(kDc + rank * 32), page * kPage, full);
+    // RoPE key: bf16 (its own map over the rows' last 128 bytes for the per-block format) or codes
+    tma_load_2d(stage0 + s * kStageBytes + 4 * kChunkBytes + (kMode == kModeFp8 ? kRopeBytes / 2 : 0), &tmap_rope,
+                (int)((kBlock ? 0 : kDc) + rank * 32), page * kPage, full);
+    if (kBlock)                            // the 4 block scales of every token of the page
+      tma_load_2d(stage0 + s * kStageBytes + 4 * kChunkBytes + kRopeBytes, &tmap_scale, kDc, page * kPage, full);
   };
   // the absorbed query of this CTA (latent half: 4 boxes of 64 columns x 128 heads, 128-byte
   // swizzle, staged in the still unused receive slots; RoPE half: straight into its 64-byte
@@ -265,7 +287,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       const int pg = bt_row[j];
       if (pg >= 0 && pg < num_pages) {
         for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tmap, (int)(rank * 256 + c * 64), pg * kPage);
-        tma_prefetch_2d(&tmap_rope, (int)(kDc + rank * 32), pg * kPage);
+        tma_prefetch_2d(&tmap_rope, (int)((kBlock ? 0 : kDc) + rank * 32), pg * kPage);
+        if (kBlock) tma_prefetch_2d(&tmap_scale, kDc, pg * kPage);
       }
     }
   }
@@ -320,7 +343,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
           const int pg = bt_row[j + kStages];
           if (pg >= 0 && pg < num_pages) {
             for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tmap, (int)(rank * 256 + c * 64), pg * kPage);
-            tma_prefetch_2d(&tmap_rope, (int)(kDc + rank * 32), pg * kPage);
+            tma_prefetch_2d(&tmap_rope, (int)((kBlock ? 0 : kDc) + rank * 32), pg * kPage);
+            if (kBlock) tma_prefetch_2d(&tmap_scale, kDc, pg * kPage);
           }
         }
         if (!mbar_wait(smem_u32(&bars->empty[s]), ((j / kStages) & 1) ^ 1, abort_flag)) {
@@ -401,16 +425,36 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // one warp per box makes that a warp-level order.  Every wait is bounded: a warp that
     // gives up aborts the kernel.
     if constexpr (kFp8) {
-      const int c = warp - kWarpConv;         // 0..3 latent chunk, 4 RoPE box
+      const int c = warp - kWarpConv;         // 0..3 latent chunk, 4 RoPE box (codes with one tensor scale)
       bool ok = true;
-      for (int t = 0; t < n_tiles; ++t) {
+      for (int t = 0; t < n_tiles && !(kBlock && c == 4); ++t) {
         const int s = t % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (t / kStages) & 1, abort_flag))) {
           ok = false;
           break;
         }
         uint8_t* st = smem + kOffStages + s * kStageBytes;
-        if (c < 4) {
+        if (c < 4 && kBlock) {
+          // as below, each value times its token's scale for this chunk's block of 128 latent
+          // values (block 2 rank + c / 2; the page's scales sit after the RoPE box, 16 bytes a token)
+          const int p = lane & 3;
+          uint8_t* box = st + c * kChunkBytes;
+          const float* scl = reinterpret_cast<const float*>(st + 4 * kChunkBytes + kRopeBytes) + 2 * rank + (c >> 1);
+          uint4 v[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            v[k] = *reinterpret_cast<const uint4*>(box + kChunkBytes / 2 + (8 * k + (lane >> 2)) * 64 + p * 16);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {       // 128-byte rows, 128-byte swizzle (the scales are not rewritten)
+            const int r = 8 * k + (lane >> 2);
+            const float sc = scl[r * 4];
+            const uint2 a = e4m3x4_scaled_to_bf16x4(v[k].x, sc), b = e4m3x4_scaled_to_bf16x4(v[k].y, sc);
+            const uint2 d = e4m3x4_scaled_to_bf16x4(v[k].z, sc), e = e4m3x4_scaled_to_bf16x4(v[k].w, sc);
+            *reinterpret_cast<uint4*>(box + r * 128 + (((2 * p) ^ (r & 7)) * 16)) = make_uint4(a.x, a.y, b.x, b.y);
+            *reinterpret_cast<uint4*>(box + r * 128 + (((2 * p + 1) ^ (r & 7)) * 16)) = make_uint4(d.x, d.y, e.x, e.y);
+          }
+        } else if (c < 4) {
           // lane = (row 8 k + lane / 4, 16 codes 16 (lane % 4) ..) for k = 0..7
           const int p = lane & 3;
           uint8_t* box = st + c * kChunkBytes;
@@ -765,20 +809,53 @@ cudaError_t make_latent_out_tensor_map(void* o_lat, int batch, int n_h, CUtensor
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Per-block FP8 cache [num_pages * 64 rows][656 bytes]: codes (boxes of 64 bytes x 64 rows,
+// no swizzle), the 16 scale bytes of a row (box 16 x 64), and the bf16 RoPE key at byte 528
+// of each row as its own bf16 matrix [rows][64] (boxes of 32 columns x 64 rows, 64-byte
+// swizzle, the operand layout of the bf16 cache's RoPE box).
+cudaError_t make_block_cache_maps(const void* cache, int num_pages, CUtensorMap* codes, CUtensorMap* scales,
+                                  CUtensorMap* rope) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  constexpr int kRowB = kDc + 16 + 2 * kDr;
+  const cuuint64_t rows = (cuuint64_t)num_pages * kPage;
+  const cuuint64_t dims8[2] = {(cuuint64_t)kRowB, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kRowB};
+  const cuuint32_t elem[2] = {1, 1};
+  const cuuint32_t box_c[2] = {64, (cuuint32_t)kPage}, box_s[2] = {16, (cuuint32_t)kPage};
+  CUresult r = enc(codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims8, strides, box_c, elem,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS)
+    r = enc(scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims8, strides, box_s, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) {
+    const cuuint64_t dims[2] = {(cuuint64_t)kDr, rows};
+    const cuuint32_t box_r[2] = {32, (cuuint32_t)kPage};
+    r = enc(rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(static_cast<const void*>(static_cast<const uint8_t*>(cache) + kDc + 16)), dims, strides,
+            box_r, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 namespace {
-template <bool kFp8>
+template <int kMode>
 cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table, int bt_stride,
-                             int num_pages, const CUtensorMap& map, const CUtensorMap& map_rope, const Workspace& ws,
-                             cudaStream_t st) {
+                             int num_pages, const CUtensorMap& map, const CUtensorMap& map_rope,
+                             const CUtensorMap& map_scale, const Workspace& ws, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e =
-        cudaFuncSetAttribute(decode_tc_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(decode_tc_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  // an FP8 cache holds codes of value / fp8_scale: the scale multiplies every score and the output
-  const float cache_scale = kFp8 ? h.cfg.fp8_scale : 1.0f;
+  // an FP8 cache with one tensor scale holds codes of value / fp8_scale: the scale multiplies
+  // every score and the output (the per-block format's values are scaled when converted)
+  const float cache_scale = kMode == kModeFp8 ? h.cfg.fp8_scale : 1.0f;
   const float scale_log2 = h.scale * cache_scale * 1.4426950408889634f;
   // the absorbed query [B][n_h][576] as (column, head, sequence): 64- and 32-column boxes of 128 heads
   alignas(64) CUtensorMap map_q, map_qpe;
@@ -787,24 +864,32 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch,
   if (e == cudaSuccess) e = make_query_tensor_map(ws.q_abs, batch, h.cfg.n_h, 32, &map_qpe);
   if (e == cudaSuccess) e = make_latent_out_tensor_map(ws.o_lat, batch, h.cfg.n_h, &map_o);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_tc_kernel<kFp8>, dim3(2 * ws.max_units), dim3(kFp8 ? kThreadsFp8 : kThreads), kSmemBytes,
-                    st, map, map_rope, map_q, map_qpe, map_o,
+  return launch_pdl(decode_tc_kernel<kMode>, dim3(2 * ws.max_units), dim3(kMode != kModeBf16 ? kThreadsFp8 : kThreads),
+                    kSmemBytes, st, map, map_rope, map_scale, map_q, map_qpe, map_o,
                     ctx_len,
                     h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, ws, h.check_word);
 }
 }  // namespace
 
-// TMA descriptors of a cache (64- and 32-column boxes of one page), rebuilt only when the
-// cache pointer or its page count changes.
+// TMA descriptors of a cache (64- and 32-column boxes of one page; for the per-block format
+// also its scale boxes), rebuilt only when the cache pointer or its page count changes.
 cudaError_t cache_maps(const Handle& h, const void* cache, int num_pages) {
-  const bool fp8 = h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3;
+  const int dt = h.cfg.cache_dtype;
   Handle& hm = const_cast<Handle&>(h);
   if (hm.tmap_cache != cache || hm.tmap_pages != num_pages) {
     CUtensorMap* m = reinterpret_cast<CUtensorMap*>(hm.tmap);
     CUtensorMap* mr = reinterpret_cast<CUtensorMap*>(hm.tmap_rope);
-    cudaError_t e = fp8 ? make_cache_tensor_map_fp8(cache, num_pages, 64, m) : make_cache_tensor_map(cache, num_pages, 64, m);
-    if (e == cudaSuccess)
-      e = fp8 ? make_cache_tensor_map_fp8(cache, num_pages, 32, mr) : make_cache_tensor_map(cache, num_pages, 32, mr);
+    CUtensorMap* ms = reinterpret_cast<CUtensorMap*>(hm.tmap_scale);
+    cudaError_t e;
+    if (dt == MLA_CACHE_FP8_E4M3_BLOCK) {
+      e = make_block_cache_maps(cache, num_pages, m, ms, mr);
+    } else {
+      const bool fp8 = dt == MLA_CACHE_FP8_E4M3;
+      e = fp8 ? make_cache_tensor_map_fp8(cache, num_pages, 64, m) : make_cache_tensor_map(cache, num_pages, 64, m);
+      if (e == cudaSuccess)
+        e = fp8 ? make_cache_tensor_map_fp8(cache, num_pages, 32, mr) : make_cache_tensor_map(cache, num_pages, 32, mr);
+      if (e == cudaSuccess) *ms = *m;      // unused by these formats; any valid map
+    }
     if (e != cudaSuccess) return e;
     hm.tmap_cache = cache;
     hm.tmap_pages = num_pages;
@@ -816,13 +901,22 @@ cudaError_t cache_maps(const Handle& h, const void* cache, int num_pages) {
 // conversion for an FP8 cache.
 cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table,
                           int bt_stride, const void* cache, int num_pages, const Workspace& ws, cudaStream_t st) {
-  const bool fp8 = h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3;
   cudaError_t e = cache_maps(h, cache, num_pages);
   if (e != cudaSuccess) return e;
   const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(h.tmap);
   const CUtensorMap& map_rope = *reinterpret_cast<const CUtensorMap*>(h.tmap_rope);
-  return fp8 ? launch_decode_tc<true>(h, ctx_len, batch, block_table, bt_stride, num_pages, map, map_rope, ws, st)
-             : launch_decode_tc<false>(h, ctx_len, batch, block_table, bt_stride, num_pages, map, map_rope, ws, st);
+  const CUtensorMap& map_scale = *reinterpret_cast<const CUtensorMap*>(h.tmap_scale);
+  switch (h.cfg.cache_dtype) {
+    case MLA_CACHE_FP8_E4M3:
+      return launch_decode_tc<kModeFp8>(h, ctx_len, batch, block_table, bt_stride, num_pages, map, map_rope,
+                                        map_scale, ws, st);
+    case MLA_CACHE_FP8_E4M3_BLOCK:
+      return launch_decode_tc<kModeFp8Block>(h, ctx_len, batch, block_table, bt_stride, num_pages, map, map_rope,
+                                             map_scale, ws, st);
+    default:
+      return launch_decode_tc<kModeBf16>(h, ctx_len, batch, block_table, bt_stride, num_pages, map, map_rope,
+                                         map_scale, ws, st);
+  }
 }
 
 }  // namespace mla

@@ -69,6 +69,7 @@ struct Handle {
   int prof_prefill;         // the last profiled call was mla_prefill (else mla_decode)
   alignas(64) unsigned char tmap[128];   // TMA descriptor (CUtensorMap) of the last cache seen
   alignas(64) unsigned char tmap_rope[128];  // same cache, RoPE-key columns (32-column boxes)
+  alignas(64) unsigned char tmap_scale[128]; // per-block FP8 cache: the rows' scale bytes
   alignas(64) unsigned char tmap_wuk[128];  // TMA descriptors of the handle's weight copies
   alignas(64) unsigned char tmap_wuv[128];
   const void* tmap_cache;

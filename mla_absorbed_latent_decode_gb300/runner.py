@@ -9,7 +9,7 @@ import numpy as np
 import torch
 
 from . import binding as B
-from .workloads import CACHE_FP8, Workload
+from .workloads import CACHE_FP8, ROW_BYTES, Workload
 
 # Byte pattern of cache memory before anything is appended: 0xFF makes every
 # bf16 value NaN and every e4m3 byte NaN, so a read of an unwritten slot that
@@ -36,7 +36,7 @@ class DecodeSession:
         self.mla = B.Mla(self.config, self.w_uk, self.w_uv, stream)
         if splits:
             self.mla.set_option(B.MLA_OPT_SPLITS, splits)
-        row_bytes = 576 * (1 if fp8 else 2)
+        row_bytes = ROW_BYTES[wl.cache_dtype]
         self.cache = torch.full((wl.num_pages, wl.page_size, row_bytes), SENTINEL, dtype=torch.uint8,
                                 device=self.device)
         self.block_table = torch.from_numpy(wl.block_table).to(self.device)

@@ -31,6 +31,8 @@ ROPE_BASE = 10000.0
 WEIGHT_STD = 0.02
 CACHE_BF16 = 1
 CACHE_FP8 = 2
+CACHE_FP8_BLOCK = 3          # 656-byte rows: 512 e4m3 latent codes, 4 fp32 block scales, 64 bf16 RoPE values
+ROW_BYTES = {1: 1152, 2: 576, 3: 656}
 
 
 def to_bf16_bits(x) -> np.ndarray:
@@ -240,6 +242,14 @@ def v3_fp8_decode(seed=3, B=128, s_ctx=4096, n_h=128) -> Workload:
     return _finish_decode(rng, "v3_b128_s4096_fp8", seed, n_h, ctx, CACHE_FP8, True, 8, 1.0, 1.0)
 
 
+def v3_fp8_block_decode(seed=3, B=128, s_ctx=4096, n_h=128) -> Workload:
+    """The FP8 configuration's shapes and draws (B=128, 4096 tokens each) with the per-block
+    format: each row 512 e4m3 latent codes, 4 fp32 block scales and the bf16 RoPE key."""
+    rng = np.random.default_rng(seed)
+    ctx = np.full(B, s_ctx, np.int32)
+    return _finish_decode(rng, "v3_b128_s4096_fp8blk", seed, n_h, ctx, CACHE_FP8_BLOCK, True, 8, 1.0, 1.0)
+
+
 def v3_long_decode(seed=4, B=8, short=32768, long=65536, n_h=128) -> Workload:
     """DeepSeek-V3 shapes, B=8: the first half of the sequences 32768 tokens, the rest 65536."""
     rng = np.random.default_rng(seed)
@@ -252,4 +262,9 @@ NAMED = {
     "v3_b64_s4096_bf16": v3_decode,
     "v3_b128_s4096_fp8": v3_fp8_decode,
     "v3_b8_long": v3_long_decode,
+}
+
+# further workloads (not among the five configurations)
+EXTRA = {
+    "v3_b128_s4096_fp8blk": v3_fp8_block_decode,
 }

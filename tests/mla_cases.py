@@ -12,17 +12,22 @@ FP8_TOL = 5e-2       # same, FP8 cache, against the oracle on its own dequantise
 
 
 def tolerance(wl) -> float:
-    return FP8_TOL if wl.cache_dtype == W.CACHE_FP8 else BF16_TOL
+    return BF16_TOL if wl.cache_dtype == W.CACHE_BF16 else FP8_TOL
 
 
 def oracle_stored(wl) -> np.ndarray:
     """The codes the oracle's cache holds for every workload row, in row order (chunked)."""
     fp8 = wl.cache_dtype == W.CACHE_FP8
-    out = np.empty(wl.rows.shape, np.uint8 if fp8 else np.uint16)
+    if wl.cache_dtype == W.CACHE_FP8_BLOCK:
+        out = np.empty((wl.rows.shape[0], W.ROW_BYTES[W.CACHE_FP8_BLOCK]), np.uint8)
+    else:
+        out = np.empty(wl.rows.shape, np.uint8 if fp8 else np.uint16)
     step = 1 << 15
     for a in range(0, wl.rows.shape[0], step):
         r, p = wl.rows[a:a + step], wl.row_pos[a:a + step]
-        if fp8:
+        if wl.cache_dtype == W.CACHE_FP8_BLOCK:
+            out[a:a + step] = mla_ref.stored_row_fp8_block(r, p, wl.d_c, wl.rope_base)
+        elif fp8:
             out[a:a + step] = mla_ref.stored_row_e4m3(r, p, wl.d_c, wl.rope_base, np.float32(wl.fp8_scale))
         else:
             out[a:a + step] = mla_ref.stored_row_bf16(r, p, wl.d_c, wl.rope_base)
@@ -30,7 +35,9 @@ def oracle_stored(wl) -> np.ndarray:
 
 
 def oracle_values(wl, stored) -> np.ndarray:
-    """float64 values of stored codes (e4m3 codes times the tensor scale)."""
+    """float64 values of stored codes (e4m3 codes times the tensor or block scale)."""
+    if wl.cache_dtype == W.CACHE_FP8_BLOCK:
+        return mla_ref.fp8_block_values(stored, wl.d_c)
     if wl.cache_dtype == W.CACHE_FP8:
         return e4m3.decode(stored) * float(np.float32(wl.fp8_scale))
     return mla_ref.bf16_to_f64(stored)
@@ -70,7 +77,7 @@ def oracle_decode_paged(wl, values) -> np.ndarray:
 
 def gpu_rows(wl, cache_bytes: np.ndarray) -> np.ndarray:
     """Read every workload row back out of a GPU cache image (codes, row order)."""
-    fp8 = wl.cache_dtype == W.CACHE_FP8
+    fp8 = wl.cache_dtype != W.CACHE_BF16
     flat = cache_bytes.reshape(wl.num_pages * wl.page_size, -1)
     pages = wl.block_table[wl.row_seq, wl.row_pos // wl.page_size].astype(np.int64)
     slots = pages * wl.page_size + wl.row_pos % wl.page_size
