@@ -263,7 +263,7 @@ mla_status_t mla_prefill_workspace_size(mla_handle_t h, int32_t batch, int32_t m
  *   ctx_len, batch, max_ctx, block_table, bt_stride, num_pages: as in mla_decode.
  *   cache        device, a bf16 cache (an FP8 cache is MLA_ERR_UNSUPPORTED), 128-byte aligned.
  *   workspace    device, >= mla_prefill_workspace_size bytes, 256-byte aligned; overwritten.
- *   out          device [total_q][n_h][d_v] bf16, 16-byte aligned: row q_start[b] + i is the
+ *   out          device [total_q][n_h][d_v] bf16, 32-byte aligned: row q_start[b] + i is the
  *                output of query i of sequence b; other rows are not written.
  *
  * Device checks (mla_get_status): a sequence whose q_start / q_len do not fit [0, total_q)

@@ -400,8 +400,8 @@ mla_status_t mla_prefill(mla_handle_t hh, const void* q, const int32_t* q_start,
   const long long rows = (long long)batch * h->cfg.n_h * ((max_ctx + 127) / 128 * 128);
   if (rows >= (1LL << 31))
     return fail(MLA_ERR_INVALID_ARG, "mla_prefill: batch x n_h x max_ctx = %lld expanded rows exceed 2^31", rows);
-  if (!aligned(q, 16) || !aligned(cache, 128) || !aligned(out, 16))
-    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: q and out must be 16-byte aligned, cache 128-byte aligned");
+  if (!aligned(q, 16) || !aligned(cache, 128) || !aligned(out, 32))
+    return fail(MLA_ERR_INVALID_ARG, "mla_prefill: q must be 16-byte aligned, out 32-byte, cache 128-byte");
   if (!aligned(workspace, 256)) return fail(MLA_ERR_WORKSPACE, "mla_prefill: workspace must be 256-byte aligned");
   const size_t need = mla::prefill_workspace_bytes(h->cfg.n_h, batch, max_ctx);
   if (workspace_bytes < need)

@@ -63,6 +63,13 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ bool page_ok(int p, int num_pages) { return p >= 0 && p < num_pages; }
 
+// One 32-byte global store (a whole sector; the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_32B(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // One expansion item: 128 tokens of a sequence for one head.  Items are numbered with the head
 // fastest, so the CTAs working at the same time share the token tile (its cache rows stay in L2).
 struct ExItem {
@@ -213,12 +220,13 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
         tmem_ld_wait();
         uint4* d = (g < 4 ? dk : dv) + 4 * (g & 3);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          d[i] = row_ok ? make_uint4(bf16x2(__uint_as_float(x[8 * i]), __uint_as_float(x[8 * i + 1])),
-                                     bf16x2(__uint_as_float(x[8 * i + 2]), __uint_as_float(x[8 * i + 3])),
-                                     bf16x2(__uint_as_float(x[8 * i + 4]), __uint_as_float(x[8 * i + 5])),
-                                     bf16x2(__uint_as_float(x[8 * i + 6]), __uint_as_float(x[8 * i + 7])))
-                        : make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < 2; ++i) {        // whole 32-byte sectors (a row's 64 bytes of the group)
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            w[e] = row_ok ? bf16x2(__uint_as_float(x[16 * i + 2 * e]), __uint_as_float(x[16 * i + 2 * e + 1])) : 0u;
+          st_global_32B(d + 2 * i, w);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -580,11 +588,13 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tmem_ld_wait();
         if (r < nrows) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[4 * g + i] = make_uint4(bf16x2(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv),
-                                        bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv),
-                                        bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv),
-                                        bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv));
+          for (int i = 0; i < 2; ++i) {      // whole 32-byte sectors of this row
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w[e] = bf16x2(__uint_as_float(o[16 * i + 2 * e]) * inv, __uint_as_float(o[16 * i + 2 * e + 1]) * inv);
+            st_global_32B(dst + 4 * g + 2 * i, w);
+          }
         }
       }
     }
