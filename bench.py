@@ -130,6 +130,22 @@ def cache_name(wl):
     return {1: "bf16", 2: "fp8_e4m3", 3: "fp8_e4m3_block"}[wl.cache_dtype]
 
 
+def ranks_max(values, device, world):
+    """Each value's maximum over the ranks: the slowest rank sets a whole-job time."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_rate(world, units_per_rank, ms):
+    """Whole-job throughput per second: every rank processes `units_per_rank` (replicas, weak
+    scaling) and the job takes the slowest rank's `ms`."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ------------------------------------------------------------------ CPU oracle leg
 
 def oracle_sample(wl, seconds):
@@ -479,16 +495,12 @@ def run_ours(args):
     e2e = statistics.mean(e2e_ms)
     naive = naive_ab(args, wl, sess, flush_l2, stream) if args.naive_ab and not layer else None
 
-    # max over ranks
-    t = torch.tensor([ms, e2e, warm], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms, e2e, warm = float(t[0]), float(t[1]), float(t[2])
+    ms, e2e, warm, graph_mean = ranks_max([ms, e2e, warm, statistics.mean(graph_ms)], dev, world)
 
     cache_b, weight_b, flops = algorithmic(wl)
     hbm, tc_burst, tc_sust, peak_kind = peaks()
-    value = world * cache_b / (ms * 1e-3) / 1e9
-    e2e_value = world * cache_b / (e2e * 1e-3) / 1e9
+    value = job_rate(world, cache_b, ms) / 1e9
+    e2e_value = job_rate(world, cache_b, e2e) / 1e9
     roof_us = max((cache_b + weight_b) / (hbm * 1e9), flops / (tc_burst * 1e12)) * 1e6
     dec_ms = statistics.mean(k.get("mla_decode_splitkv", float("nan")) for k in kernel_ms)
     per_kernel = {k: round(statistics.mean(km[k] for km in kernel_ms) * 1000.0, 2) for k in kernel_ms[0]}
@@ -502,13 +514,13 @@ def run_ours(args):
             "us_per_step": round(ms * 1000.0, 2), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
             "roofline_us": round(roof_us, 2), "roofline_frac_step": round(roof_us / (ms * 1000.0), 4),
             "us_per_step_median": round(ms_median * 1000.0, 2),
-            "total_gbs": round(world * (cache_b + weight_b) / (ms * 1e-3) / 1e9, 1),
+            "total_gbs": round(job_rate(world, cache_b + weight_b, ms) / 1e9, 1),
             "warm_l2": {"us_per_step": round(warm * 1000.0, 2),
-                        "value": round(world * cache_b / (warm * 1e-3) / 1e9, 2), "unit": "GB/s (latent KV)",
+                        "value": round(job_rate(world, cache_b, warm) / 1e9, 2), "unit": "GB/s (latent KV)",
                         "note": "the same K steps back to back with no flush between them (weights and "
                                 "part of the cache may stay in L2); not the headline"},
-            "graph_replay": {"us_per_step": round(statistics.mean(graph_ms) * 1000.0, 2),
-                             "value": round(world * cache_b / (statistics.mean(graph_ms) * 1e-3) / 1e9, 2),
+            "graph_replay": {"us_per_step": round(graph_mean * 1000.0, 2),
+                             "value": round(job_rate(world, cache_b, graph_mean) / 1e9, 2),
                              "unit": "GB/s (latent KV)",
                              "note": "the same step captured once in a CUDA graph and replayed, L2 flushed "
                                      "between replays; not the headline"},
@@ -776,10 +788,7 @@ def run_prefill(args, wl):
         e2e_ms.append(a.elapsed_time(z))
     e2e = statistics.mean(e2e_ms)
 
-    t = torch.tensor([ms, e2e], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms, e2e = float(t[0]), float(t[1])
+    ms, e2e = ranks_max([ms, e2e], dev, world)
     fe, fa = prefill_flops(wl)
     hbm, tc_burst, tc_sust, peak_kind = peaks()
     per_kernel = {k: round(statistics.mean(km[k] for km in kernel_ms) * 1000.0, 2) for k in kernel_ms[0]}
@@ -788,7 +797,7 @@ def run_prefill(args, wl):
     achieved = fa / (attn_ms * 1e-3) / 1e12
     if rank == 0:
         line = {
-            "metric": PREFILL_METRIC, "value": round(world * (fe + fa) / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "metric": PREFILL_METRIC, "value": round(job_rate(world, fe + fa, ms) / 1e12, 2), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "us_per_step": round(ms * 1000.0, 2), "us_per_step_median": round(statistics.median(step_ms) * 1000.0, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -808,7 +817,7 @@ def run_prefill(args, wl):
                          "algorithmic_flops_per_launch": int(fa),
                          "expansion": {"achieved": round(fe / (exp_ms * 1e-3) / 1e12, 1),
                                        "frac": round(fe / (exp_ms * 1e-3) / 1e12 / tc_burst, 4)}},
-            "e2e": {"value": round(world * (fe + fa) / (e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "e2e": {"value": round(job_rate(world, fe + fa, e2e) / 1e12, 2), "unit": "TFLOP/s",
                     "ms_per_step": round(e2e, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
             "gpu_launches": args.steps * 3,
             "clocks": clock_info,
@@ -826,10 +835,12 @@ def run_prefill(args, wl):
 
 def main():
     args = parse()
+    if args.impl == "reference" and int(os.environ.get("RANK", "0")) != 0:
+        return 0                             # the reference arm runs on rank 0 alone
     if args.workload == PREFILL:
         wl = workload(args.workload)
         if args.impl == "reference":
-            return 0 if int(os.environ.get("RANK", "0")) != 0 else run_prefill_reference(args, wl)
+            return run_prefill_reference(args, wl)
         return run_prefill(args, wl)
     if args.impl == "reference":
         return run_reference(args)
