@@ -47,6 +47,8 @@ def _oracle(wl, seqs=None):
 
 
 CASES = {
+    "odd_heads_empty_and_single_token_chunks": (5, [1, 200, 77, 130], [1, 0, 77, 129]),
+    "single_query_chunks_long_prefix": (16, [700, 4100], [1, 3]),
     "whole_prompts_16h": (16, [1, 64, 127, 128, 129, 300, 515], None),
     "chunks_after_prefix_16h": (16, [200, 300, 64, 700, 5], [37, 300, 1, 129, 5]),
     "whole_prompts_128h": (128, [130, 257], None),
@@ -64,6 +66,8 @@ def test_prefill_matches_the_oracle(case):
     p = wl.extra["prefill"]
     for b, ref in _oracle(wl).items():
         a, n = int(p["q_start"][b]), int(p["q_len"][b])
+        if n == 0:                                    # an empty chunk: nothing to compare
+            continue
         err = compare(out[a:a + n], ref, BF16_TOL)
         assert err[0] <= BF16_TOL, (b, err)
     s.close()

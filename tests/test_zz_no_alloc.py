@@ -28,12 +28,13 @@ def _second_query(wl, seed):
     (128, RAGGED, W.CACHE_BF16),
     (128, [4096] * 4 + [3001] * 4, W.CACHE_BF16),
     (40, RAGGED, W.CACHE_FP8),
+    (24, RAGGED, W.CACHE_FP8_BLOCK),
 ])
 def test_fixed_scratch_matches_workspace_decode(n_h, lengths, dtype):
     wl = W.make_decode("fixed", 77 + n_h, n_h, lengths, cache_dtype=dtype)
     s = DecodeSession(wl)
     s.append_rows()
-    tol = BF16_TOL if dtype == W.CACHE_BF16 else FP8_TOL
+    tol = BF16_TOL if dtype != W.CACHE_FP8 else FP8_TOL
     queries = [s.q, bf16_tensor(_second_query(wl, 1234 + n_h), s.device)]
     for q in queries:                                     # two calls in a row, different inputs
         ref = bf16_out_to_f64(s.decode(q=q).clone())
