@@ -310,6 +310,63 @@ def ncu_traffic(wl):
     return d.get("bytes_per_launch")
 
 
+def pipelined_e2e(stream, dev, h_pack, d_packs, outs, h_outs, slot_step, steps, warmup):
+    """End-to-end steps as a serving loop runs them: two slots of device inputs and outputs; the
+    host-to-device copy of step i + 1 and the read-back of step i - 1 run on their own streams
+    while step i computes.  `slot_step(k)` issues the step on slot k's buffers (the public API
+    calls) on the current stream; each slot's step is captured once in a CUDA graph and replayed.
+    The timed region starts before the first copy in and ends when the last result is on the
+    host.  Returns ms per step."""
+    import torch
+    side = torch.cuda.Stream(device=dev)
+    graphs = []
+    for k in range(2):
+        g = torch.cuda.CUDAGraph()
+        side.wait_stream(stream)
+        with torch.cuda.graph(g, stream=side):
+            slot_step(k)
+        graphs.append(g)
+    stream.wait_stream(side)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    read = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def run(k_steps, start=None):
+        if start is not None:
+            s_in.wait_event(start)
+        for i in range(k_steps):
+            k = i % 2
+            if i >= 2:
+                s_in.wait_event(done[k])             # step i - 2 has read this slot's inputs
+            with torch.cuda.stream(s_in):
+                d_packs[k].copy_(h_pack, non_blocking=True)
+            in_ready[k].record(s_in)
+            stream.wait_event(in_ready[k])
+            if i >= 2:
+                stream.wait_event(read[k])           # step i - 2's result has left this slot
+            graphs[k].replay()
+            done[k].record(stream)
+            s_out.wait_event(done[k])
+            with torch.cuda.stream(s_out):
+                h_outs[k].copy_(outs[k].view(torch.int16), non_blocking=True)
+            read[k].record(s_out)
+        stream.wait_event(read[(k_steps - 1) % 2])
+
+    run(max(2, warmup))
+    torch.cuda.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    run(steps, start=p0)
+    p1.record(stream)
+    p1.synchronize()
+    return p0.elapsed_time(p1) / steps
+
+
+E2E_MODE = ("pipelined: the copies of steps i + 1 (in) and i - 1 (out) overlap step i's compute; each of the "
+            "two buffer slots' steps (the same public calls) replayed from a CUDA graph captured once")
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -497,10 +554,8 @@ def run_ours(args):
         e2e_ms.append(s0.elapsed_time(s1))
     e2e_serial = statistics.mean(e2e_ms)
 
-    # the same steps as a serving loop runs them: two slots of device inputs and outputs; the
-    # host-to-device copy of step i + 1 and the read-back of step i - 1 run on their own streams
-    # while step i computes.  Every step's copies lie inside the timed region (it ends when the
-    # last result is on the host); the inputs (the 288 MiB cache read per step) exceed L2.
+    # the same steps as a serving loop runs them (the inputs, the 288 MiB cache read per step,
+    # exceed L2)
     d_packs = [d_pack, torch.empty_like(d_pack)]
     views_k = [views, {}]
     for name, a in parts:
@@ -509,50 +564,8 @@ def run_ours(args):
         views_k[1][name] = d_packs[1][offs[name]:offs[name] + n].view(dt).view(a.shape)
     outs = [sess.out, torch.empty_like(sess.out)]
     h_outs = [h_out, torch.empty_like(h_out).pin_memory()]
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    # each slot's step (the public API calls on that slot's buffers) captured once in a CUDA
-    # graph, so the host issues one replay per step instead of the calls' argument marshalling
-    slot_graphs = []
-    for k in range(2):
-        g_k = torch.cuda.CUDAGraph()
-        side.wait_stream(stream)
-        with torch.cuda.graph(g_k, stream=side):
-            compute(views_k[k], outs[k])
-        slot_graphs.append(g_k)
-    stream.wait_stream(side)
-    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
-    done = [torch.cuda.Event(), torch.cuda.Event()]
-    read = [torch.cuda.Event(), torch.cuda.Event()]
-
-    def pipelined(k_steps, start=None):
-        if start is not None:
-            s_in.wait_event(start)
-        for i in range(k_steps):
-            k = i % 2
-            if i >= 2:
-                s_in.wait_event(done[k])         # step i - 2 has read this slot's inputs
-            with torch.cuda.stream(s_in):
-                d_packs[k].copy_(h_pack, non_blocking=True)
-            in_ready[k].record(s_in)
-            stream.wait_event(in_ready[k])
-            if i >= 2:
-                stream.wait_event(read[k])       # step i - 2's result has left this slot
-            slot_graphs[k].replay()
-            done[k].record(stream)
-            s_out.wait_event(done[k])
-            with torch.cuda.stream(s_out):
-                h_outs[k].copy_(outs[k].view(torch.int16), non_blocking=True)
-            read[k].record(s_out)
-        stream.wait_event(read[(k_steps - 1) % 2])
-
-    pipelined(max(2, args.warmup))
-    torch.cuda.synchronize()
-    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    p0.record(stream)
-    pipelined(args.steps, start=p0)
-    p1.record(stream)
-    p1.synchronize()
-    e2e = p0.elapsed_time(p1) / args.steps
+    e2e = pipelined_e2e(stream, dev, h_pack, d_packs, outs, h_outs, lambda k: compute(views_k[k], outs[k]),
+                        args.steps, args.warmup)
     naive = naive_ab(args, wl, sess, flush_l2, stream) if args.naive_ab and not layer else None
 
     ms, e2e, warm, graph_mean = ranks_max([ms, e2e, warm, statistics.mean(graph_ms)], dev, world)
@@ -604,9 +617,7 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": cache_b},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s (latent KV)", "ms_per_step": round(e2e, 5),
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "mode": "pipelined: the copies of steps i + 1 (in) and i - 1 (out) overlap step i's compute; "
-                            "each of the two buffer slots' steps (the same public calls) replayed from a CUDA graph "
-                            "captured once",
+                    "mode": E2E_MODE,
                     "serial_ms_per_step": round(e2e_serial, 5)},
             "gpu_launches": args.steps * ((2 if layer else 1) + len(kernel_ms[0])),
             "clocks": clock_info,
@@ -769,10 +780,10 @@ def run_prefill(args, wl):
         flush.zero_()
         flush_rd.view(torch.int32).amax()
 
-    def step(rows=rows, seq=seq, pos=pos, q=q, q_start=q_start, q_len=q_len, ctx=sess.ctx_len):
+    def step(rows=rows, seq=seq, pos=pos, q=q, q_start=q_start, q_len=q_len, ctx=sess.ctx_len, o=out):
         sess.mla.kv_append(rows, seq, pos, sess.block_table, sess.cache, wl.num_pages)
         sess.mla.prefill(q, q_start, q_len, max_q, ctx, wl.max_ctx, sess.block_table, sess.cache, wl.num_pages,
-                         ws, out)
+                         ws, o)
 
     for _ in range(max(3, args.warmup)):
         flush_l2()
@@ -850,7 +861,21 @@ def run_prefill(args, wl):
         z.record(stream)
         z.synchronize()
         e2e_ms.append(a.elapsed_time(z))
-    e2e = statistics.mean(e2e_ms)
+    e2e_serial = statistics.mean(e2e_ms)
+    d_packs = [d_pack, torch.empty_like(d_pack)]
+    views_k = [views, {}]
+    for name, a in parts:
+        n = np.ascontiguousarray(a).nbytes
+        dt = torch.int16 if np.asarray(a).dtype == np.int16 else torch.int32
+        views_k[1][name] = d_packs[1][offs[name]:offs[name] + n].view(dt).view(a.shape)
+    outs = [out, torch.empty_like(out)]
+    h_outs = [h_out, torch.empty_like(h_out).pin_memory()]
+
+    def slot_step(k):
+        v = views_k[k]
+        step(v["rows"].view(torch.bfloat16), v["seq"], v["pos"], v["q"].view(torch.bfloat16), v["q_start"],
+             v["q_len"], v["ctx"], outs[k])
+    e2e = pipelined_e2e(stream, dev, h_pack, d_packs, outs, h_outs, slot_step, args.steps, args.warmup)
 
     ms, e2e = ranks_max([ms, e2e], dev, world)
     fe, fa = prefill_flops(wl)
@@ -882,7 +907,8 @@ def run_prefill(args, wl):
                          "expansion": {"achieved": round(fe / (exp_ms * 1e-3) / 1e12, 1),
                                        "frac": round(fe / (exp_ms * 1e-3) / 1e12 / tc_burst, 4)}},
             "e2e": {"value": round(job_rate(world, fe + fa, e2e) / 1e12, 2), "unit": "TFLOP/s",
-                    "ms_per_step": round(e2e, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+                    "ms_per_step": round(e2e, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "mode": E2E_MODE, "serial_ms_per_step": round(e2e_serial, 5)},
             "gpu_launches": args.steps * 3,
             "clocks": clock_info,
         }
