@@ -237,7 +237,8 @@ mla_status_t mla_decode_naive(mla_handle_t h, const void* q, const int32_t* ctx_
                               void* workspace, size_t workspace_bytes, void* out, mla_stream_t stream);
 
 /* mla_prefill_workspace_size -- device workspace bytes of mla_prefill:
- * batch * round_up(max_ctx, 128) * (2 n_h d_nope + d_rope) * 2 (the expanded keys and values). */
+ * batch * round_up(max_ctx, 128) * (2 n_h d_nope + d_rope) * 2 (the expanded keys and values)
+ * + 256 (the attention kernel's work counter).  Calls sharing a workspace run in stream order. */
 mla_status_t mla_prefill_workspace_size(mla_handle_t h, int32_t batch, int32_t max_ctx, size_t* bytes);
 
 /*

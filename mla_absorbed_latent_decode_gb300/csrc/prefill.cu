@@ -13,8 +13,9 @@
 //      item = (head, 128 tokens): D[128 tokens][256] = C[128][512] . [W_UK[h] ; W_UV[h]]^T,
 //      A = two cache pages by TMA, B = the head's weight rows, K-major, 4-stage ring;
 //      persistent CTAs, two TMEM accumulators (the epilogue of an item under the next's MMAs).
-//   2. prefill_attn_kernel: CTA = (128 queries, head, sequence); query i of sequence b sits at
-//      position ctx_len - q_len + i and sees keys 0 .. that position.  Per 128-key tile j:
+//   2. prefill_attn_kernel: item = (128 queries, head, sequence), persistent CTAs taking items in
+//      turn; query i of sequence b sits at position ctx_len - q_len + i and sees keys 0 .. that
+//      position.  Per 128-key tile j:
 //        S = Q K^T (M = 128 queries, N = 128 keys, K = 128 + 64) into one of two TMEM score
 //        buffers; online softmax (base 2, lazy rescale of O when the running maximum grows by
 //        more than 2^8) by warps 0-3, one query row per thread; P (bf16) into TMEM; O += P V
@@ -102,7 +103,7 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
                  const __grid_constant__ CUtensorMap tm_wuv, const __nv_bfloat16* __restrict__ cache,
                  const int32_t* __restrict__ ctx_len, int n_h, int max_ctx, const int32_t* __restrict__ block_table,
                  int bt_stride, int num_pages, int lpad, int n_items, __nv_bfloat16* __restrict__ kn,
-                 __nv_bfloat16* __restrict__ vv, __nv_bfloat16* __restrict__ kr, unsigned* check) {
+                 __nv_bfloat16* __restrict__ vv, __nv_bfloat16* __restrict__ kr, int* sched, unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -131,6 +132,9 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
   const uint32_t tmem = bars->tmem_base;
   griddep_wait();                          // the rows may have been appended by the previous kernel
   griddep_launch_dependents();
+  // the attention kernel's work counter (after the wait: an earlier call's attention, still the
+  // previous kernel in the stream, may have been using it)
+  if (blockIdx.x == 0 && tid == 0) *sched = 0;
 
   if (warp == 4) {
     // ---------------------------------------------------------------- producer
@@ -253,7 +257,8 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
 }
 
 // ------------------------------------------------------------------ attention
-constexpr int kAtThreads = 256;        // warps 0-3 softmax + epilogue, 4 K / 5 V producers, 6 QK^T / 7 P V issuers
+constexpr int kAtThreads = 256;        // warps 0-3 softmax + epilogue, 4 K / 5 V producers,
+                                       // 6 query RoPE + QK^T issuer, 7 P V issuer
 constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6, kWarpPv = 7;
 constexpr int kOffQ = 0;                               // q_nope 0..63, q_nope 64..127, q_pe: 3 boxes
 constexpr int kOffK = 3 * kBox;                        // 2 stages x (k_nope 0..63, 64..127, k_r)
@@ -264,13 +269,36 @@ constexpr uint32_t kTmO = 0, kTmS = 128, kTmP = 384;   // TMEM columns
 constexpr float kRescaleLog2 = 8.0f;                   // rescale O when the row maximum grows by > 2^8
 
 struct AtBars {
-  uint64_t qfull, qready;
+  uint64_t qfull;            // the item's queries landed                    (K producer, tx)
+  uint64_t qfree;            // every QK^T of the item done: the query buffer may be refilled
   uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
   uint64_t sfull[2], sfree[2], pfull[2], pdone[2];
-  uint64_t ofinal, qkdrain;
+  uint64_t ofinal;           // the item's last P V done                     (MMA commit)
+  uint64_t ofree;            // the epilogue has read O                      (4 softmax warps)
+  uint64_t qkdrain, pvdrain;
+  uint64_t item_full[4];     // ring entry written by the scheduling thread (the K producer)
+  uint64_t item_free[4];     // ring entry read by the other six roles
+  int ring[4];               // item indices handed out to this CTA, in order (-1: no more)
   uint32_t tmem_base;
   int abort;
 };
+constexpr int kRingReaders = 7;        // V producer, QK^T warp, P V issuer, 4 softmax warps
+
+// The next item of a role that reads the ring: n-th entry, -1 when there are no more, -2 when
+// a wait ran out (or another role aborted).  `arrive` is set on one thread per role.
+__device__ __forceinline__ int at_next(AtBars* bars, int n, bool arrive, volatile int* abort_flag) {
+  const int slot = n & 3;
+  if (!mbar_wait(smem_u32(&bars->item_full[slot]), (n >> 2) & 1, abort_flag)) return -2;
+  const int idx = *reinterpret_cast<volatile int*>(&bars->ring[slot]);
+  if (arrive) mbar_arrive(smem_u32(&bars->item_free[slot]));
+  return idx;
+}
+
+// Whether an item loop goes on with `idx`; a failed wait (-2) also clears ok.
+__device__ __forceinline__ bool at_more(int idx, bool& ok) {
+  if (idx == -2) ok = false;
+  return idx >= 0;
+}
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
@@ -298,13 +326,53 @@ __device__ __forceinline__ void at_fail(AtBars* bars, unsigned* check) {
   if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
 }
 
+// One attention item: 128 queries of one head of one sequence.  Items are numbered with the
+// query block fastest (longest first), then the head, then the sequence, so the items in work
+// at the same time share a head's keys and values in L2.  Every role of the CTA derives the
+// same description from the same inputs.
+struct AtItem {
+  int b, h, qs, nq, L, r0, nrows, p_first, n_kt;
+  bool rows_ok;              // q_start / q_len fit the query rows: outputs may be written
+  bool live;                 // a valid item with queries: every role takes part
+  bool zero;                 // queries of a sequence with an invalid length: zero rows only
+};
+
+__device__ __forceinline__ AtItem at_item(int idx, int nqb, int n_h, const int32_t* q_start, const int32_t* q_len,
+                                          int total_q, int max_q, const int32_t* ctx_len, int max_ctx) {
+  AtItem it;
+  const int qb = nqb - 1 - idx % nqb;
+  it.h = (idx / nqb) % n_h;
+  it.b = idx / (nqb * n_h);
+  it.L = ctx_len[it.b];
+  it.nq = q_len[it.b];
+  it.qs = q_start[it.b];
+  it.rows_ok = it.nq >= 0 && it.nq <= max_q && it.qs >= 0 && (long long)it.qs + it.nq <= total_q;
+  const bool seq_ok = it.rows_ok && it.L >= 1 && it.L <= max_ctx && it.nq <= it.L;
+  it.r0 = qb * kQBlk;
+  const bool has_rows = it.rows_ok && it.r0 < it.nq;
+  it.nrows = has_rows ? min(kQBlk, it.nq - it.r0) : 0;
+  it.live = has_rows && seq_ok;
+  it.zero = has_rows && !seq_ok;
+  it.p_first = it.live ? it.L - it.nq + it.r0 : 0;
+  it.n_kt = it.live ? (it.p_first + it.nrows - 1 + kTile) / kTile : 0;   // key tiles 0 .. n_kt - 1
+  return it;
+}
+
+// Persistent: each CTA takes the next item from a global counter (longest query blocks of a head
+// first, a head's blocks together) and hands it to its roles through a 4-entry ring in shared
+// memory, so a CTA that finishes early takes more work.  The key/value rings, the score buffers
+// and their barriers run on across items (a global tile count g); the next item's queries load
+// as soon as the previous item's last QK^T is done and the QK^T warp rotates their RoPE part,
+// so the next item's QK^T does not wait for the epilogue; its first P V waits only for the
+// epilogue to have read O.
 __global__ void __launch_bounds__(kAtThreads, 1)
 prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kn,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kr,
                     const int32_t* __restrict__ q_start, const int32_t* __restrict__ q_len, int total_q, int max_q,
                     const int32_t* __restrict__ ctx_len, int n_h, int max_ctx, const int32_t* __restrict__ block_table,
                     int bt_stride, int num_pages, const float2* __restrict__ rope_cs, int max_position,
-                    float scale_log2, int lpad, __nv_bfloat16* __restrict__ out, unsigned* check) {
+                    float scale_log2, int lpad, int nqb, int n_items, int* sched, __nv_bfloat16* __restrict__ out,
+                    unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -312,41 +380,9 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   AtBars* bars = reinterpret_cast<AtBars*>(smem + kOffBars);
   volatile int* abort_flag = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qb = gridDim.x - 1 - blockIdx.x;           // the longest query blocks start first
-  const int h = blockIdx.y, b = blockIdx.z;
-  griddep_wait();                                      // the expanded keys and values
-  griddep_launch_dependents();
-  const int L = ctx_len[b], nq = q_len[b], qs = q_start[b];
-  const bool rows_ok = nq >= 0 && nq <= max_q && qs >= 0 && (long long)qs + nq <= total_q;
-  const bool seq_ok = rows_ok && L >= 1 && L <= max_ctx && nq <= L;
-  const int r0 = qb * kQBlk;
-  if (!rows_ok) {                                      // nowhere to write: flag only
-    if (tid == 0 && qb == 0 && h == 0) atomicOr(check, kCheckCtxLen);
-    return;
-  }
-  if (r0 >= nq) return;
-  const int nrows = min(kQBlk, nq - r0);
-  const int p_first = L - nq + r0, p_last = p_first + nrows - 1;   // positions of the block's queries
-  // every page the block's keys come from must be a valid page id
-  bool bad = !seq_ok;
-  if (seq_ok) {
-    const int npages = (p_last + kPage) / kPage;
-    for (int i = tid; i < npages; i += kAtThreads) bad |= !page_ok(block_table[(size_t)b * bt_stride + i], num_pages);
-  }
-  bad = __syncthreads_or(bad);
-  if (bad) {                                           // zero output rows, flag
-    if (tid == 0) atomicOr(check, seq_ok ? kCheckPageId : kCheckCtxLen);
-    for (int i = tid; i < nrows * (kDv / 8); i += kAtThreads) {
-      const int r = i / (kDv / 8), c = i % (kDv / 8);
-      reinterpret_cast<uint4*>(out + ((size_t)(qs + r0 + r) * n_h + h) * kDv)[c] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    return;
-  }
-  const int n_kt = (p_last + kTile) / kTile;            // key tiles 0 .. n_kt - 1
-
   if (tid == 0) {
     mbar_init(smem_u32(&bars->qfull), 1);
-    mbar_init(smem_u32(&bars->qready), 4);
+    mbar_init(smem_u32(&bars->qfree), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->kfull[i]), 1);
       mbar_init(smem_u32(&bars->kempty[i]), 1);
@@ -358,7 +394,13 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_init(smem_u32(&bars->pdone[i]), 1);
     }
     mbar_init(smem_u32(&bars->ofinal), 1);
+    mbar_init(smem_u32(&bars->ofree), 4);
     mbar_init(smem_u32(&bars->qkdrain), 1);
+    mbar_init(smem_u32(&bars->pvdrain), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(smem_u32(&bars->item_full[i]), 1);
+      mbar_init(smem_u32(&bars->item_free[i]), kRingReaders);
+    }
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -367,238 +409,337 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const int kv_row0 = (b * n_h + h) * lpad;            // this head's first expanded row
+  griddep_wait();                                      // the expanded keys and values
+  griddep_launch_dependents();
+// item loops of the ring readers: one thread (AT_ITEMS_T) or a whole warp whose lane 0 reads the
+// entry and broadcasts it (AT_ITEMS_W); a failed wait ends the loop with ok = false
+#define AT_ITEMS_T for (int n = 0, idx = 0; at_more(idx = at_next(bars, n, true, abort_flag), ok); ++n)
+#define AT_ITEMS_W                                                                                      \
+  for (int n = 0, idx = 0;                                                                              \
+       at_more(idx = __shfl_sync(0xffffffffu, lane == 0 ? at_next(bars, n, true, abort_flag) : 0, 0), ok); ++n)
+#define AT_ITEM() at_item(idx, nqb, n_h, q_start, q_len, total_q, max_q, ctx_len, max_ctx)
 
   if (warp == kWarpK) {
-    // ---------------------------------------------------------------- Q, then the key tiles
+    // ---------------------------------------------------------------- queries, then the key tiles
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_kn);
       prefetch_tmap(&tm_kr);
-      const uint32_t qf = smem_u32(&bars->qfull);
-      mbar_arrive_expect_tx(qf, 3 * kBox);
-      for (int c = 0; c < 3; ++c) tma_load_3d(sbase + kOffQ + c * kBox, &tm_q, 64 * c, h, qs + r0, qf);
-      int issued = 0;
+      prefetch_tmap(&tm_v);
+      int g = 0, u = 0;
       bool ok = true;
-      for (int j = 0; j < n_kt; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(smem_u32(&bars->kempty[s]), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-        const uint32_t st = sbase + kOffK + s * 3 * kBox, fb = smem_u32(&bars->kfull[s]);
-        mbar_arrive_expect_tx(fb, 3 * kBox);
-        tma_load_2d(st, &tm_kn, 0, kv_row0 + kTile * j, fb);
-        tma_load_2d(st + kBox, &tm_kn, 64, kv_row0 + kTile * j, fb);
-        tma_load_2d(st + 2 * kBox, &tm_kr, 0, b * lpad + kTile * j, fb);
-        issued = j + 1;
+      for (int n = 0;; ++n) {
+        // the scheduler: the next item from the global counter into ring entry n % 4, once the
+        // six other roles have read that entry's previous item
+        const int slot = n & 3;
+        if (n >= 4 && !mbar_wait(smem_u32(&bars->item_free[slot]), ((n >> 2) - 1) & 1, abort_flag)) { ok = false; break; }
+        int idx = atomicAdd(sched, 1);
+        if (idx >= n_items) idx = -1;
+        *reinterpret_cast<volatile int*>(&bars->ring[slot]) = idx;
+        mbar_arrive(smem_u32(&bars->item_full[slot]));
+        if (idx < 0) break;
+        const AtItem it = AT_ITEM();
+        if (!it.live) continue;
+        // into L2 now (about two key tiles before the previous item ends): this item's queries,
+        // which come from HBM, and its first key and value tiles
+        for (int c = 0; c < 3; ++c) tma_prefetch_3d(&tm_q, 64 * c, it.h, it.qs + it.r0);
+        {
+          const int row0 = (it.b * n_h + it.h) * lpad;
+          tma_prefetch_2d(&tm_kn, 0, row0);
+          tma_prefetch_2d(&tm_kn, 64, row0);
+          tma_prefetch_2d(&tm_kr, 0, it.b * lpad);
+          tma_prefetch_2d(&tm_v, 0, row0);
+          tma_prefetch_2d(&tm_v, 64, row0);
+        }
+        // the previous item's QK^T are done with the query buffer
+        if (u >= 1 && !mbar_wait(smem_u32(&bars->qfree), (u - 1) & 1, abort_flag)) { ok = false; break; }
+        const uint32_t qf = smem_u32(&bars->qfull);
+        mbar_arrive_expect_tx(qf, 3 * kBox);
+        for (int c = 0; c < 3; ++c) tma_load_3d(sbase + kOffQ + c * kBox, &tm_q, 64 * c, it.h, it.qs + it.r0, qf);
+        ++u;
+        const int kv_row0 = (it.b * n_h + it.h) * lpad;
+        for (int j = 0; j < it.n_kt; ++j, ++g) {
+          const int s = g & 1;
+          if (g >= 2 && !mbar_wait(smem_u32(&bars->kempty[s]), ((g - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+          const uint32_t st = sbase + kOffK + s * 3 * kBox, fb = smem_u32(&bars->kfull[s]);
+          mbar_arrive_expect_tx(fb, 3 * kBox);
+          tma_load_2d(st, &tm_kn, 0, kv_row0 + kTile * j, fb);
+          tma_load_2d(st + kBox, &tm_kn, 64, kv_row0 + kTile * j, fb);
+          tma_load_2d(st + 2 * kBox, &tm_kr, 0, it.b * lpad + kTile * j, fb);
+        }
+        if (!ok) break;
       }
       if (!ok) at_fail(bars, check);
-      volatile int never = 0;
-      mbar_wait(qf, 0, &never);
-      for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(smem_u32(&bars->kfull[j & 1]), (j >> 1) & 1, &never);
+      volatile int never = 0;                          // every copy lands before exit
+      if (u >= 1) mbar_wait(smem_u32(&bars->qfull), (u - 1) & 1, &never);
+      for (int k = max(0, g - 2); k < g; ++k) mbar_wait(smem_u32(&bars->kfull[k & 1]), (k >> 1) & 1, &never);
     }
   } else if (warp == kWarpV) {
     // ---------------------------------------------------------------- value tiles
     if (lane == 0) {
       prefetch_tmap(&tm_v);
-      int issued = 0;
+      int g = 0;
       bool ok = true;
-      for (int j = 0; j < n_kt; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(smem_u32(&bars->vempty[s]), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-        const uint32_t st = sbase + kOffV + s * 2 * kBox, fb = smem_u32(&bars->vfull[s]);
-        mbar_arrive_expect_tx(fb, 2 * kBox);
-        tma_load_2d(st, &tm_v, 0, kv_row0 + kTile * j, fb);
-        tma_load_2d(st + kBox, &tm_v, 64, kv_row0 + kTile * j, fb);
-        issued = j + 1;
+      AT_ITEMS_T {
+        const AtItem it = AT_ITEM();
+        if (!it.live) continue;
+        const int kv_row0 = (it.b * n_h + it.h) * lpad;
+        for (int j = 0; j < it.n_kt; ++j, ++g) {
+          const int s = g & 1;
+          if (g >= 2 && !mbar_wait(smem_u32(&bars->vempty[s]), ((g - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+          const uint32_t st = sbase + kOffV + s * 2 * kBox, fb = smem_u32(&bars->vfull[s]);
+          mbar_arrive_expect_tx(fb, 2 * kBox);
+          tma_load_2d(st, &tm_v, 0, kv_row0 + kTile * j, fb);
+          tma_load_2d(st + kBox, &tm_v, 64, kv_row0 + kTile * j, fb);
+        }
+        if (!ok) break;
       }
       if (!ok) at_fail(bars, check);
       volatile int never = 0;
-      for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(smem_u32(&bars->vfull[j & 1]), (j >> 1) & 1, &never);
+      for (int k = max(0, g - 2); k < g; ++k) mbar_wait(smem_u32(&bars->vfull[k & 1]), (k >> 1) & 1, &never);
     }
   } else if (warp == kWarpMma) {
-    // ---------------------------------------------------------------- QK^T issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-      const uint64_t qd = sdesc_sw128(sbase + kOffQ, 16, 1024);
-      bool ok = mbar_wait(smem_u32(&bars->qready), 0, abort_flag);
-      for (int j = 0; ok && j < n_kt; ++j) {
-        const int s = j & 1;
-        // K(j) has landed and the score buffer's previous tile, j - 2, has been read
-        if (!mbar_wait(smem_u32(&bars->kfull[s]), (j >> 1) & 1, abort_flag) ||
-            (j >= 2 && !mbar_wait(smem_u32(&bars->sfree[s]), ((j - 2) >> 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t kd = sdesc_sw128(sbase + kOffK + s * 3 * kBox, 16, 1024);
+    // ---------------------------------------------------------------- query RoPE, then QK^T
+    // The item's first QK^T needs its rotated queries anyway, so this warp rotates them: row
+    // r's q_pe in place at its position (lane = rows lane, lane + 32, ...; swizzled box: chunk
+    // c at c ^ (r & 7)); then lane 0 issues the item's QK^T.
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+    const uint64_t qd = sdesc_sw128(sbase + kOffQ, 16, 1024);
+    int g = 0, u = 0;
+    bool ok = true;
+    AT_ITEMS_W {
+      const AtItem it = AT_ITEM();
+      if (!it.live) continue;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->qfull), u & 1, abort_flag));
+      if (!ok) break;
 #pragma unroll
-        for (int k = 0; k < kDq / 16; ++k) {  // box k / 4 (k_nope, k_nope, k_r), 32-byte step k % 4
-          const uint64_t off = (uint64_t)(((k >> 2) * kBox + (k & 3) * 32) >> 4);
-          mma_ss(tmem + kTmS + 128 * s, qd + off, kd + off, idesc_qk, k > 0 ? 1u : 0u);
+      for (int k = 0; k < kQBlk / 32; ++k) {
+        const int r = lane + 32 * k;
+        const int lim = min(it.p_first + r, it.L - 1);    // rows past the block clamp (never stored)
+        uint8_t* row = smem + kOffQ + 2 * kBox + r * 128;
+        // (cos, sin) of pairs 4 c .. 4 c + 3 in two 16-byte loads per chunk
+        const float4* cs = reinterpret_cast<const float4*>(rope_cs + (size_t)min(lim, max_position - 1) * (kDr / 2));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4* p = reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4));
+          const uint4 v = *p;
+          const float4 c01 = cs[2 * c], c23 = cs[2 * c + 1];
+          const float2 cc[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
+                                make_float2(c23.z, c23.w)};
+          uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float y0, y1;
+            rope_pair(bf16_lo(w[i]), bf16_hi(w[i]), cc[i], &y0, &y1);
+            w[i] = pack_bf16(y0, y1);
+          }
+          *p = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        mma_commit(smem_u32(&bars->sfull[s]));
-        mma_commit(smem_u32(&bars->kempty[s]));
       }
+      fence_proxy_async_smem();                        // the rotated rows, before the MMAs read them
+      __syncwarp();
+      if (lane == 0) {
+        for (int j = 0; j < it.n_kt; ++j, ++g) {
+          const int s = g & 1;
+          // K(g) has landed and the score buffer's previous tile, g - 2, has been read
+          if (!mbar_wait(smem_u32(&bars->kfull[s]), (g >> 1) & 1, abort_flag) ||
+              (g >= 2 && !mbar_wait(smem_u32(&bars->sfree[s]), ((g - 2) >> 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kd = sdesc_sw128(sbase + kOffK + s * 3 * kBox, 16, 1024);
+#pragma unroll
+          for (int k = 0; k < kDq / 16; ++k) {  // box k / 4 (k_nope, k_nope, k_r), 32-byte step k % 4
+            const uint64_t off = (uint64_t)(((k >> 2) * kBox + (k & 3) * 32) >> 4);
+            mma_ss(tmem + kTmS + 128 * s, qd + off, kd + off, idesc_qk, k > 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&bars->sfull[s]));
+          mma_commit(smem_u32(&bars->kempty[s]));
+        }
+        if (ok) mma_commit(smem_u32(&bars->qfree));    // the item's QK^T are done with the queries
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      g = __shfl_sync(0xffffffffu, g, 0);
+      if (!ok) break;
+      ++u;
+    }
+    if (lane == 0) {
       if (!ok) at_fail(bars, check);
-      mma_commit(smem_u32(&bars->qkdrain));   // every QK^T issued above has finished ...
+      mma_commit(smem_u32(&bars->qkdrain));            // every QK^T issued above has finished ...
       volatile int never = 0;
-      mbar_wait(smem_u32(&bars->qkdrain), 0, &never);   // ... before the CTA frees its TMEM
+      mbar_wait(smem_u32(&bars->qkdrain), 0, &never);  // ... before the CTA frees its TMEM
     }
   } else if (warp == kWarpPv) {
     // ---------------------------------------------------------------- P V issuer (its own thread:
     // a P V never waits behind a QK^T issue; the two write disjoint TMEM, O and P against S)
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
+      int g = 0, u = 0;
       bool ok = true;
-      for (int jj = 0; ok && jj < n_kt; ++jj) {
-        const int s = jj & 1;
-        if (!mbar_wait(smem_u32(&bars->pfull[s]), (jj >> 1) & 1, abort_flag) ||
-            !mbar_wait(smem_u32(&bars->vfull[s]), (jj >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // V tile: 128 key rows (K) x 128 value columns (N) in two 64-column boxes, MN-major
-        const uint64_t vd = sdesc_sw128(sbase + kOffV + s * 2 * kBox, kBox, 1024);
+      AT_ITEMS_T {
+        const AtItem it = AT_ITEM();
+        if (!it.live) continue;
+        for (int j = 0; j < it.n_kt; ++j, ++g) {
+          const int s = g & 1;
+          if (!mbar_wait(smem_u32(&bars->pfull[s]), (g >> 1) & 1, abort_flag) ||
+              !mbar_wait(smem_u32(&bars->vfull[s]), (g >> 1) & 1, abort_flag) ||
+              (j == 0 && u >= 1 && !mbar_wait(smem_u32(&bars->ofree), (u - 1) & 1, abort_flag))) {
+            ok = false;                                // (j == 0: the previous item's O has been read)
+            break;
+          }
+          tc_fence_after();
+          // V tile: 128 key rows (K) x 128 value columns (N) in two 64-column boxes, MN-major
+          const uint64_t vd = sdesc_sw128(sbase + kOffV + s * 2 * kBox, kBox, 1024);
 #pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)
-          mma_ts(tmem + kTmO, tmem + kTmP + 64 * s + 8 * k, vd + (uint64_t)(128 * k), idesc_pv,
-                 (jj > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bars->vempty[s]));
-        mma_commit(smem_u32(&bars->pdone[s]));
+          for (int k = 0; k < kTile / 16; ++k)
+            mma_ts(tmem + kTmO, tmem + kTmP + 64 * s + 8 * k, vd + (uint64_t)(128 * k), idesc_pv,
+                   (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bars->vempty[s]));
+          mma_commit(smem_u32(&bars->pdone[s]));
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&bars->ofinal));
+        ++u;
       }
       if (!ok) at_fail(bars, check);
-      mma_commit(smem_u32(&bars->ofinal));   // after a failure too: every issued P V has finished
+      mma_commit(smem_u32(&bars->pvdrain));            // every P V issued above has finished
       volatile int never = 0;
-      mbar_wait(smem_u32(&bars->ofinal), 0, &never);
+      mbar_wait(smem_u32(&bars->pvdrain), 0, &never);
     }
-  } else {
+  } else if (warp < 4) {
     // ---------------------------------------------------------------- softmax: thread = query row
     const int r = 32 * warp + lane;
-    const int qpos = p_first + r;
-    const int lim = min(qpos, L - 1);                  // last visible key (rows past the block clamp)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    bool ok = mbar_wait(smem_u32(&bars->qfull), 0, abort_flag);
-    if (ok) {
-      // rotate this row's q_pe in place at its position (swizzled box: chunk c at c ^ (r & 7))
-      uint8_t* row = smem + kOffQ + 2 * kBox + r * 128;
-      const float2* cs = rope_cs + (size_t)min(lim, max_position - 1) * (kDr / 2);
+    int g = 0, u = 0;
+    bool ok = true;
+    AT_ITEMS_W {
+      const AtItem it = AT_ITEM();
+      if (it.zero || (!it.rows_ok && it.r0 == 0 && it.h == 0)) {   // bad length or rows: flag (and zero)
+        if (r == 0) atomicOr(check, kCheckCtxLen);
+        if (it.zero && r < it.nrows) {
+          uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(it.qs + it.r0 + r) * n_h + it.h) * kDv);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4* p = reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4));
-        uint4 v = *p;
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float y0, y1;
-          rope_pair(bf16_lo(w[i]), bf16_hi(w[i]), cs[4 * c + i], &y0, &y1);
-          w[i] = pack_bf16(y0, y1);
-        }
-        *p = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      fence_proxy_async_smem();
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&bars->qready));
-    float m_ref = -INFINITY, l = 0.0f;
-    for (int j = 0; ok && j < n_kt; ++j) {
-      const int s = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sfull[s]), (j >> 1) & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t x[kTile];                               // scores, then scaled base-2 logits (float bits)
-#pragma unroll
-      for (int g = 0; g < 4; ++g) tmem_ld32(tmem + lane_off + kTmS + 128 * s + 32 * g, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * g]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->sfree[s]));
-      if (kTile * j + kTile - 1 > p_first) {           // a tile on the diagonal: hide keys past the row
-#pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          if (kTile * j + c > lim) x[c] = __float_as_uint(-INFINITY);
-      }
-      // the scale is positive, so the maximum of the raw scores gives the scaled one
-      const float m_new = fmaxf(m_ref, max128(x) * scale_log2);
-      if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleLog2)) {
-        const float alpha = ex2_approx(m_ref - m_new);
-        l *= alpha;
-        m_ref = m_new;
-        if (j > 0) {                                   // O holds P V of tiles < j: rescale it
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pdone[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-          const float2 al2 = make_float2(alpha, alpha);
-#pragma unroll 1
-          for (int g = 0; g < 4; ++g) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_off + kTmO + 32 * g, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), al2);
-              o[2 * i] = __float_as_uint(v.x);
-              o[2 * i + 1] = __float_as_uint(v.y);
-            }
-            tmem_st32(tmem + lane_off + kTmO + 32 * g, o);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < kDv / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      if (j >= 2) {                                    // P V(j - 2) has read this P buffer
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pdone[s]), ((j - 2) >> 1) & 1, abort_flag));
+      if (!it.live) continue;
+      // every page the item's keys come from must be a valid page id (else zero output rows)
+      bool bad = false;
+      const int npages = (it.p_first + it.nrows - 1 + kPage) / kPage;
+      for (int i = lane; i < npages; i += 32) bad |= !page_ok(block_table[(size_t)it.b * bt_stride + i], num_pages);
+      bad = __any_sync(0xffffffffu, bad);
+      if (bad && r == 0) atomicOr(check, kCheckPageId);
+      const int lim = min(it.p_first + r, it.L - 1);      // last visible key of this row
+      float m_ref = -INFINITY, l = 0.0f;
+      for (int j = 0; j < it.n_kt; ++j, ++g) {
+        const int s = g & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->sfull[s]), (g >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-      }
-      // p = 2^(score * scale_log2 - m): one packed FMA per pair, four independent partial sums
-      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m_ref, -m_ref);
-      float2 ps[4];
+        uint32_t x[kTile];                               // scores, then scaled base-2 logits (float bits)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ps[i] = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 d = __ffma2_rn(make_float2(__uint_as_float(x[64 * hf + 2 * c]),
-                                                  __uint_as_float(x[64 * hf + 2 * c + 1])), sc2, nm2);
-          const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
-          ps[c & 3] = __fadd2_rn(ps[c & 3], pp);
-          pk[c] = bf16x2(pp.x, pp.y);
-        }
-        tmem_st32(tmem + lane_off + kTmP + 64 * s + 32 * hf, pk);
-      }
-      const float2 sum2 = __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3]));
-      const float sum = sum2.x + sum2.y;
-      l += sum;
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->pfull[s]));
-    }
-    // ---------------------------------------------------------------- epilogue
-    ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->ofinal), 0, abort_flag)) && !*abort_flag;
-    tc_fence_after();
-    if (ok) {
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(qs + r0 + r) * n_h + h) * kDv);
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + kTmO + 32 * g, o);
+        for (int q = 0; q < 4; ++q)
+          tmem_ld32(tmem + lane_off + kTmS + 128 * s + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * q]));
         tmem_ld_wait();
-        if (r < nrows) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->sfree[s]));
+        if (kTile * j + kTile - 1 > it.p_first) {        // a tile on the diagonal: hide keys past the row
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {      // whole 32-byte sectors of this row
+          for (int c = 0; c < kTile; ++c)
+            if (kTile * j + c > lim) x[c] = __float_as_uint(-INFINITY);
+        }
+        // the scale is positive, so the maximum of the raw scores gives the scaled one
+        const float m_new = fmaxf(m_ref, max128(x) * scale_log2);
+        if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleLog2)) {
+          const float alpha = ex2_approx(m_ref - m_new);
+          l *= alpha;
+          m_ref = m_new;
+          if (j > 0) {                                   // O holds P V of the item's tiles < j: rescale it
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pdone[(g - 1) & 1]), ((g - 1) >> 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            const float2 al2 = make_float2(alpha, alpha);
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+              uint32_t o[32];
+              tmem_ld32(tmem + lane_off + kTmO + 32 * q, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), al2);
+                o[2 * i] = __float_as_uint(v.x);
+                o[2 * i + 1] = __float_as_uint(v.y);
+              }
+              tmem_st32(tmem + lane_off + kTmO + 32 * q, o);
+            }
+            tmem_st_wait();
+          }
+        }
+        if (g >= 2) {                                    // P V(g - 2) has read this P buffer
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pdone[s]), ((g - 2) >> 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // p = 2^(score * scale_log2 - m): one packed FMA per pair, four independent partial sums
+        const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m_ref, -m_ref);
+        float2 ps[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ps[i] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 d = __ffma2_rn(make_float2(__uint_as_float(x[64 * hf + 2 * c]),
+                                                    __uint_as_float(x[64 * hf + 2 * c + 1])), sc2, nm2);
+            const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
+            ps[c & 3] = __fadd2_rn(ps[c & 3], pp);
+            pk[c] = bf16x2(pp.x, pp.y);
+          }
+          tmem_st32(tmem + lane_off + kTmP + 64 * s + 32 * hf, pk);
+        }
+        const float2 sum2 = __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3]));
+        l += sum2.x + sum2.y;
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->pfull[s]));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------------- epilogue of the item
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->ofinal), u & 1, abort_flag)) && !*abort_flag;
+      if (!ok) break;
+      tc_fence_after();
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;      // (a bad page id: zero rows)
+      uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(it.qs + it.r0 + r) * n_h + it.h) * kDv);
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + kTmO + 32 * q, o);
+        tmem_ld_wait();
+        if (r < it.nrows) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {                  // whole 32-byte sectors of this row
             uint32_t w[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              w[e] = bf16x2(__uint_as_float(o[16 * i + 2 * e]) * inv, __uint_as_float(o[16 * i + 2 * e + 1]) * inv);
-            st_global_32B(dst + 4 * g + 2 * i, w);
+              w[e] = bad ? 0u : bf16x2(__uint_as_float(o[16 * i + 2 * e]) * inv, __uint_as_float(o[16 * i + 2 * e + 1]) * inv);
+            st_global_32B(dst + 4 * q + 2 * i, w);
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->ofree));   // the next item's first P V may overwrite O
+      ++u;
     }
+    if (!ok) at_fail(bars, check);
   }
+#undef AT_ITEMS_T
+#undef AT_ITEMS_W
+#undef AT_ITEM
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -653,9 +794,9 @@ int padded_ctx(int max_ctx) { return (max_ctx + kTile - 1) / kTile * kTile; }
 }  // namespace
 
 // Workspace of a prefill: K_nope and V [B][n_h][lpad][128] and K_r [B][lpad][64], bf16,
-// lpad = max_ctx rounded up to 128 tokens.
+// lpad = max_ctx rounded up to 128 tokens, then the attention kernel's work counter.
 size_t prefill_workspace_bytes(int n_h, int batch, int max_ctx) {
-  return (size_t)batch * padded_ctx(max_ctx) * (2 * (size_t)n_h * kDn + kDr) * 2;
+  return (size_t)batch * padded_ctx(max_ctx) * (2 * (size_t)n_h * kDn + kDr) * 2 + 256;   // + the work counter
 }
 
 cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_start, const int32_t* q_len, int total_q,
@@ -676,6 +817,7 @@ cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_star
   __nv_bfloat16* kn = static_cast<__nv_bfloat16*>(workspace);
   __nv_bfloat16* vv = kn + (size_t)batch * n_h * lpad * kDn;
   __nv_bfloat16* kr = vv + (size_t)batch * n_h * lpad * kDv;
+  int* sched = reinterpret_cast<int*>(kr + (size_t)batch * lpad * kDr);   // 256-byte aligned: every region is
   alignas(64) CUtensorMap tm_q, tm_kn, tm_v, tm_kr;
   if ((e = query_map(q, total_q, n_h, &tm_q)) != cudaSuccess) return e;
   if ((e = rows_map_2d(kn, (long long)batch * n_h * lpad, kDn, &tm_kn)) != cudaSuccess) return e;
@@ -685,14 +827,15 @@ cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_star
   e = launch_pdl(expand_tc_kernel, dim3(min(n_items, h.num_sms)), dim3(kExThreads), kExSmem, st,
                  *reinterpret_cast<const CUtensorMap*>(h.tmap), *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk),
                  *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv), static_cast<const __nv_bfloat16*>(cache), ctx_len,
-                 n_h, max_ctx, block_table, bt_stride, num_pages, lpad, n_items, kn, vv, kr, h.check_word);
+                 n_h, max_ctx, block_table, bt_stride, num_pages, lpad, n_items, kn, vv, kr, sched, h.check_word);
   if (e != cudaSuccess) return e;
   if (between && (e = cudaEventRecord(between, st)) != cudaSuccess) return e;   // profiling: splits the two kernels
   const float scale_log2 = h.scale * 1.4426950408889634f;
-  return launch_pdl(prefill_attn_kernel, dim3((max_q + kQBlk - 1) / kQBlk, n_h, batch), dim3(kAtThreads), kAtSmem, st,
+  const int nqb = (max_q + kQBlk - 1) / kQBlk, n_att = nqb * n_h * batch;
+  return launch_pdl(prefill_attn_kernel, dim3(min(n_att, h.num_sms)), dim3(kAtThreads), kAtSmem, st,
                     tm_q, tm_kn, tm_v, tm_kr, q_start, q_len, total_q, max_q, ctx_len, n_h, max_ctx, block_table,
-                    bt_stride, num_pages, (const float2*)h.rope_cs, h.cfg.max_position, scale_log2, lpad,
-                    static_cast<__nv_bfloat16*>(out), h.check_word);
+                    bt_stride, num_pages, (const float2*)h.rope_cs, h.cfg.max_position, scale_log2, lpad, nqb, n_att,
+                    sched, static_cast<__nv_bfloat16*>(out), h.check_word);
 }
 
 }  // namespace mla

@@ -140,6 +140,13 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
                : "memory");
 }
 
+// Same for a 3-D tile.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // 16-byte store into another CTA's shared memory that completes 16 bytes of
 // transaction count on an mbarrier of that CTA.
 __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c, float d,
