@@ -257,8 +257,8 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
 }
 
 // ------------------------------------------------------------------ attention
-constexpr int kAtThreads = 256;        // warps 0-3 softmax + epilogue, 4 K / 5 V producers,
-                                       // 6 query RoPE + QK^T issuer, 7 P V issuer
+constexpr int kAtThreads = 256;        // warps 0-3 query RoPE + softmax + epilogue, 4 K / 5 V
+                                       // producers, 6 QK^T / 7 P V issuers
 constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6, kWarpPv = 7;
 constexpr int kOffQ = 0;                               // q_nope 0..63, q_nope 64..127, q_pe: 3 boxes
 constexpr int kOffK = 3 * kBox;                        // 2 stages x (k_nope 0..63, 64..127, k_r)
@@ -270,6 +270,7 @@ constexpr float kRescaleLog2 = 8.0f;                   // rescale O when the row
 
 struct AtBars {
   uint64_t qfull;            // the item's queries landed                    (K producer, tx)
+  uint64_t qready;           // their RoPE part rotated in shared memory     (4 softmax warps)
   uint64_t qfree;            // every QK^T of the item done: the query buffer may be refilled
   uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
   uint64_t sfull[2], sfree[2], pfull[2], pdone[2];
@@ -362,9 +363,9 @@ __device__ __forceinline__ AtItem at_item(int idx, int nqb, int n_h, const int32
 // first, a head's blocks together) and hands it to its roles through a 4-entry ring in shared
 // memory, so a CTA that finishes early takes more work.  The key/value rings, the score buffers
 // and their barriers run on across items (a global tile count g); the next item's queries load
-// as soon as the previous item's last QK^T is done and the QK^T warp rotates their RoPE part,
-// so the next item's QK^T does not wait for the epilogue; its first P V waits only for the
-// epilogue to have read O.
+// as soon as the previous item's last QK^T is done and the softmax warps rotate their RoPE part
+// before the previous item's epilogue, so the next item's QK^T overlaps that epilogue; its first
+// P V waits only for the epilogue to have read O.
 __global__ void __launch_bounds__(kAtThreads, 1)
 prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kn,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kr,
@@ -382,6 +383,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     mbar_init(smem_u32(&bars->qfull), 1);
+    mbar_init(smem_u32(&bars->qready), 4);
     mbar_init(smem_u32(&bars->qfree), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->kfull[i]), 1);
@@ -499,46 +501,16 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       for (int k = max(0, g - 2); k < g; ++k) mbar_wait(smem_u32(&bars->vfull[k & 1]), (k >> 1) & 1, &never);
     }
   } else if (warp == kWarpMma) {
-    // ---------------------------------------------------------------- query RoPE, then QK^T
-    // The item's first QK^T needs its rotated queries anyway, so this warp rotates them: row
-    // r's q_pe in place at its position (lane = rows lane, lane + 32, ...; swizzled box: chunk
-    // c at c ^ (r & 7)); then lane 0 issues the item's QK^T.
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-    const uint64_t qd = sdesc_sw128(sbase + kOffQ, 16, 1024);
-    int g = 0, u = 0;
-    bool ok = true;
-    AT_ITEMS_W {
-      const AtItem it = AT_ITEM();
-      if (!it.live) continue;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->qfull), u & 1, abort_flag));
-      if (!ok) break;
-#pragma unroll
-      for (int k = 0; k < kQBlk / 32; ++k) {
-        const int r = lane + 32 * k;
-        const int lim = min(it.p_first + r, it.L - 1);    // rows past the block clamp (never stored)
-        uint8_t* row = smem + kOffQ + 2 * kBox + r * 128;
-        // (cos, sin) of pairs 4 c .. 4 c + 3 in two 16-byte loads per chunk
-        const float4* cs = reinterpret_cast<const float4*>(rope_cs + (size_t)min(lim, max_position - 1) * (kDr / 2));
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4* p = reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4));
-          const uint4 v = *p;
-          const float4 c01 = cs[2 * c], c23 = cs[2 * c + 1];
-          const float2 cc[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
-                                make_float2(c23.z, c23.w)};
-          uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float y0, y1;
-            rope_pair(bf16_lo(w[i]), bf16_hi(w[i]), cc[i], &y0, &y1);
-            w[i] = pack_bf16(y0, y1);
-          }
-          *p = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-      fence_proxy_async_smem();                        // the rotated rows, before the MMAs read them
-      __syncwarp();
-      if (lane == 0) {
+    // ---------------------------------------------------------------- QK^T issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+      const uint64_t qd = sdesc_sw128(sbase + kOffQ, 16, 1024);
+      int g = 0, u = 0;
+      bool ok = true;
+      AT_ITEMS_T {
+        const AtItem it = AT_ITEM();
+        if (!it.live) continue;
+        if (!mbar_wait(smem_u32(&bars->qready), u & 1, abort_flag)) { ok = false; break; }   // rotated queries
         for (int j = 0; j < it.n_kt; ++j, ++g) {
           const int s = g & 1;
           // K(g) has landed and the score buffer's previous tile, g - 2, has been read
@@ -557,14 +529,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           mma_commit(smem_u32(&bars->sfull[s]));
           mma_commit(smem_u32(&bars->kempty[s]));
         }
-        if (ok) mma_commit(smem_u32(&bars->qfree));    // the item's QK^T are done with the queries
+        if (!ok) break;
+        mma_commit(smem_u32(&bars->qfree));            // the item's QK^T are done with the queries
+        ++u;
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      g = __shfl_sync(0xffffffffu, g, 0);
-      if (!ok) break;
-      ++u;
-    }
-    if (lane == 0) {
       if (!ok) at_fail(bars, check);
       mma_commit(smem_u32(&bars->qkdrain));            // every QK^T issued above has finished ...
       volatile int never = 0;
@@ -608,22 +576,67 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_wait(smem_u32(&bars->pvdrain), 0, &never);
     }
   } else if (warp < 4) {
-    // ---------------------------------------------------------------- softmax: thread = query row
+    // ---------------------------------------------------------------- query RoPE, softmax, epilogue:
+    // thread = query row.  The warps rotate the next live item's queries as soon as they have
+    // written the current item's last P, before its epilogue, so the next item's QK^T overlaps
+    // the epilogue (one row per thread: each row's (cos, sin) in 16-byte loads, all in flight).
     const int r = 32 * warp + lane;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    int g = 0, u = 0;
+    int g = 0, u = 0, n = 0;
     bool ok = true;
-    AT_ITEMS_W {
-      const AtItem it = AT_ITEM();
-      if (it.zero || (!it.rows_ok && it.r0 == 0 && it.h == 0)) {   // bad length or rows: flag (and zero)
-        if (r == 0) atomicOr(check, kCheckCtxLen);
-        if (it.zero && r < it.nrows) {
-          uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(it.qs + it.r0 + r) * n_h + it.h) * kDv);
+    // the next live item from the ring; queries of a sequence with a bad length are zeroed (and
+    // flagged) on the way; false at the end of the work or on a failed wait
+    auto next_live = [&](AtItem& it) -> bool {
+      while (true) {
+        const int idx = __shfl_sync(0xffffffffu, lane == 0 ? at_next(bars, n, true, abort_flag) : 0, 0);
+        ++n;
+        if (!at_more(idx, ok)) return false;
+        it = AT_ITEM();
+        if (it.zero || (!it.rows_ok && it.r0 == 0 && it.h == 0)) {
+          if (r == 0) atomicOr(check, kCheckCtxLen);
+          if (it.zero && r < it.nrows) {
+            uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(it.qs + it.r0 + r) * n_h + it.h) * kDv);
 #pragma unroll
-          for (int i = 0; i < kDv / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+            for (int i = 0; i < kDv / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
+        if (it.live) return true;
       }
-      if (!it.live) continue;
+    };
+    // row r's q_pe of live item number uu rotated in place at its position once the queries have
+    // landed (swizzled box: chunk c at c ^ (r & 7))
+    auto rotate = [&](const AtItem& it, int uu) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->qfull), uu & 1, abort_flag))) return false;
+      const int lim = min(it.p_first + r, it.L - 1);    // rows past the block clamp (never stored)
+      uint8_t* row = smem + kOffQ + 2 * kBox + r * 128;
+      const float4* cs = reinterpret_cast<const float4*>(rope_cs + (size_t)min(lim, max_position - 1) * (kDr / 2));
+      float4 cv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) cv[i] = cs[i];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4* p = reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4));
+        const uint4 v = *p;
+        const float2 cc[4] = {make_float2(cv[2 * c].x, cv[2 * c].y), make_float2(cv[2 * c].z, cv[2 * c].w),
+                              make_float2(cv[2 * c + 1].x, cv[2 * c + 1].y), make_float2(cv[2 * c + 1].z, cv[2 * c + 1].w)};
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float y0, y1;
+          rope_pair(bf16_lo(w[i]), bf16_hi(w[i]), cc[i], &y0, &y1);
+          w[i] = pack_bf16(y0, y1);
+        }
+        *p = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();                          // the rotated rows, before the MMAs read them
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->qready));
+      return true;
+    };
+    AtItem it;
+    bool have = next_live(it);
+    if (have && !rotate(it, 0)) { ok = false; have = false; }
+    while (have) {
       // every page the item's keys come from must be a valid page id (else zero output rows)
       bool bad = false;
       const int npages = (it.p_first + it.nrows - 1 + kPage) / kPage;
@@ -708,6 +721,11 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (lane == 0) mbar_arrive(smem_u32(&bars->pfull[s]));
       }
       if (!ok) break;
+      // the next live item's queries, rotated before this item's epilogue
+      AtItem nxt;
+      const bool have_next = next_live(nxt);
+      if (!ok) break;
+      if (have_next && !rotate(nxt, u + 1)) { ok = false; break; }
       // ---------------------------------------------------------------- epilogue of the item
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->ofinal), u & 1, abort_flag)) && !*abort_flag;
       if (!ok) break;
@@ -734,6 +752,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->ofree));   // the next item's first P V may overwrite O
       ++u;
+      it = nxt;
+      have = have_next;
     }
     if (!ok) at_fail(bars, check);
   }
