@@ -211,6 +211,34 @@ def project_inputs(x, w_dkv, w_q, n_h, d_c):
     return kv[:, :d_c], kv[:, d_c:], q
 
 
+def rms_norm(x, w, eps):
+    """RMSNorm of each row (Zhang & Sennrich, "Root Mean Square Layer Normalization", 2019):
+    ``y = x / sqrt(mean(x^2) + eps) * w``, float64.
+
+    The pages name the norm of the KV latent ("DeepSeek MLA 吸收式缓存：真实权重执行与
+    FlashMLA 架构边界" §3.3: ``kv_a_layernorm.weight`` is the reference's ``kv_norm.weight``;
+    §3.1: the layer's input RMSNorm) without restating it; this is the published definition.
+    x [..., n], w [n].
+    """
+    x = np.asarray(x, np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + float(eps)) * np.asarray(w, np.float64)
+
+
+def low_rank_query(x, w_dq, w_uq, w_qr, n_h):
+    """The low-rank query path: ``qz = W_DQ x``, ``q_c = W_UQ qz`` (content, n_h x d_nope),
+    ``q_r = W_QR qz`` (rope, n_h x d_rope), joined per head as ``[q_c ; q_r]``.
+
+    "80 行 PyTorch 从零写 DeepSeek 的 MLA" §2: the query also goes through a low-rank
+    factorisation (``Wdq``, then ``Wuq`` and ``Wqr``).  x [L, d_model]; returns
+    [L, n_h, d_nope + d_rope].
+    """
+    qz = np.asarray(x, np.float64) @ np.asarray(w_dq, np.float64).T
+    q_c = (qz @ np.asarray(w_uq, np.float64).T).reshape(qz.shape[0], n_h, -1)
+    q_r = (qz @ np.asarray(w_qr, np.float64).T).reshape(qz.shape[0], n_h, -1)
+    return np.concatenate([q_c, q_r], axis=2)
+
+
 def causal_forward_naive(x, w_dkv, w_q, w_uk, w_uv, scale, base):
     """One-shot causal forward over all L tokens with expanded K/V.
 

@@ -307,9 +307,46 @@ def pin_fp8_block_format(ref):
     assert np.array_equal(vals[:, 512:], ref.bf16_to_f64(bf[:, 512:]))
 
 
+def pin_rms_norm(ref):
+    """RMSNorm against closed forms: a constant row c gives sign(c) w (eps = 0); the output
+    does not change when a row is scaled by a > 0 (eps = 0); with unit weights every row's
+    mean square is 1 (eps = 0), and eps enters under the root (a row of 3s with eps = 7 gives
+    3 / 4 = 0.75)."""
+    rng = np.random.default_rng(41)
+    n = 48
+    w = rng.standard_normal(n)
+    for c in (2.5, -0.25):
+        assert np.max(np.abs(ref.rms_norm(np.full((1, n), c), w, 0.0) - np.sign(c) * w)) <= 1e-15
+    x = rng.standard_normal((4, n))
+    assert np.max(np.abs(ref.rms_norm(3.7 * x, w, 0.0) - ref.rms_norm(x, w, 0.0))) <= 1e-14
+    y = ref.rms_norm(x, np.ones(n), 0.0)
+    assert np.max(np.abs(np.mean(y * y, axis=1) - 1.0)) <= 1e-14
+    assert abs(ref.rms_norm(np.full((1, n), 3.0), np.ones(n), 7.0)[0, 0] - 0.75) <= 1e-15
+
+
+def pin_low_rank_query(ref):
+    """The low-rank query path is the composition of its three maps: with W_DQ the identity it
+    is [W_UQ x ; W_QR x] per head, and it is linear in x."""
+    rng = np.random.default_rng(42)
+    n_h, d, dn, dr = 3, 8, 4, 2
+    x = rng.standard_normal((5, d))
+    w_uq, w_qr = rng.standard_normal((n_h * dn, d)), rng.standard_normal((n_h * dr, d))
+    q = ref.low_rank_query(x, np.eye(d), w_uq, w_qr, n_h)
+    assert q.shape == (5, n_h, dn + dr)
+    for h in range(n_h):
+        assert np.max(np.abs(q[:, h, :dn] - x @ w_uq[h * dn:(h + 1) * dn].T)) <= 1e-13
+        assert np.max(np.abs(q[:, h, dn:] - x @ w_qr[h * dr:(h + 1) * dr].T)) <= 1e-13
+    w_dq, w_uq2, w_qr2 = rng.standard_normal((6, d)), rng.standard_normal((n_h * dn, 6)), rng.standard_normal((n_h * dr, 6))
+    a = ref.low_rank_query(2.0 * x, w_dq, w_uq2, w_qr2, n_h)
+    b = ref.low_rank_query(x, w_dq, w_uq2, w_qr2, n_h)
+    assert np.max(np.abs(a - 2.0 * b)) <= 1e-12
+    qz = x @ w_dq.T                                  # and the composition, head by head
+    assert np.max(np.abs(b[:, 1, :dn] - qz @ w_uq2[dn:2 * dn].T)) <= 1e-13
+
+
 ALL_PINS = [
     pin_rope_closed_forms, pin_rope_relative_position, pin_scale_worked_example,
     pin_naive_equals_absorbed, pin_rope_on_content_breaks_absorption, pin_closed_forms,
     pin_split_lse_identity, pin_one_shot_equals_incremental, pin_prefill_rows_are_decodes, pin_cache_bytes,
-    pin_mha_ratio_and_read_bytes, pin_fp8_block_format,
+    pin_mha_ratio_and_read_bytes, pin_fp8_block_format, pin_rms_norm, pin_low_rank_query,
 ]

@@ -139,6 +139,9 @@ MUTATIONS = {
     "fp8_block_one_scale_per_row": ("stored_row_fp8_block", _fp8_block_with(per_row=True)),
     "fp8_block_saturation_127": ("stored_row_fp8_block", _fp8_block_with(sat=127.0)),
     "fp8_block_rope_quantised": ("stored_row_fp8_block", _fp8_block_with(quantise_rope=True)),
+    "rms_norm_without_root": ("rms_norm", lambda x, w, eps: np.asarray(x, float) / (np.mean(np.asarray(x, float) ** 2, axis=-1, keepdims=True) + eps) * w),
+    "rms_norm_eps_outside_root": ("rms_norm", lambda x, w, eps: np.asarray(x, float) / (np.sqrt(np.mean(np.asarray(x, float) ** 2, axis=-1, keepdims=True)) + eps) * w),
+    "low_rank_query_swaps_content_and_rope": ("low_rank_query", lambda x, w_dq, w_uq, w_qr, n_h: _orig["low_rank_query"](x, w_dq, w_qr, w_uq, n_h) if w_uq.shape == w_qr.shape else np.concatenate([(np.asarray(x) @ np.asarray(w_dq).T @ np.asarray(w_qr).T).reshape(len(x), n_h, -1), (np.asarray(x) @ np.asarray(w_dq).T @ np.asarray(w_uq).T).reshape(len(x), n_h, -1)], axis=2)),
     "prefill_mask_excludes_diagonal": ("prefill_naive", _prefill_with(strict_mask=True)),
     "prefill_queries_rotated_at_chunk_start": ("prefill_naive", _prefill_with(chunk_position=True)),
     "cache_bytes_without_rope": ("absorb_cache_bytes", lambda t, d_c, d_r, e: int(t) * int(d_c) * int(e)),
