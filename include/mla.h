@@ -202,6 +202,25 @@ mla_status_t mla_project(mla_handle_t h, const void* x, int32_t m, int32_t k, co
                          void* y, mla_stream_t stream);
 
 /*
+ * mla_rmsnorm -- RMSNorm of m rows: y = x / sqrt(mean(x^2) + eps) * w (Zhang & Sennrich 2019;
+ * "DeepSeek MLA 吸收式缓存：真实权重执行与 FlashMLA 架构边界" §3.3 names the latent's norm,
+ * kv_a_layernorm / kv_norm).  Sum of squares and scaling in fp32, each value (x * inv) * w
+ * rounded to bf16.  Rows are strided, so the latent part of [d_c + d_rope] rows can be
+ * normalised in place (y == x, ld_y == ld_x) between mla_project and mla_kv_append, and the
+ * low-rank query's qz between its two projections.
+ *
+ *   x            device [m][ld_x] bf16, 16-byte aligned; values 0 .. n - 1 of each row are used.
+ *   m            rows (0 is a no-op).
+ *   n            a positive multiple of 8, at most 8192.
+ *   ld_x, ld_y   row strides in values: multiples of 8, >= n.
+ *   w            device [n] bf16, 16-byte aligned (caller-owned).
+ *   eps          >= 0, added to the mean square under the root.
+ *   y            device [m][ld_y] bf16, 16-byte aligned; may be x.
+ */
+mla_status_t mla_rmsnorm(mla_handle_t h, const void* x, int32_t m, int32_t n, int32_t ld_x, const void* w, float eps,
+                         void* y, int32_t ld_y, mla_stream_t stream);
+
+/*
  * mla_expand_kv -- the standard-mode (naive) cache of an MLA layer, for comparison with the
  * absorbed path ("80 行 PyTorch 从零写 DeepSeek 的 MLA" §3/§5: the naive mode caches each
  * head's key and value; "DeepSeek-V2-Lite 真实权重执行审计" §3.2: 10,240 bytes per token at

@@ -38,7 +38,7 @@ MLA_FIXED_SCRATCH_BYTES = 32 << 20     # include/mla.h: scratch of mla_decode_fi
 
 EXPORTED = [
     "mla_create", "mla_destroy", "mla_kv_append", "mla_kv_project_append", "mla_project",
-    "mla_expand_kv", "mla_decode_naive_workspace_size", "mla_decode_naive",
+    "mla_rmsnorm", "mla_expand_kv", "mla_decode_naive_workspace_size", "mla_decode_naive",
     "mla_prefill_workspace_size", "mla_prefill",
     "mla_decode_workspace_size", "mla_decode",
     "mla_decode_fixed_scratch",
@@ -82,6 +82,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_kv_append.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, vp, i32, vp]
     lib.mla_kv_project_append.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp, i32, i32, vp, i32, vp]
     lib.mla_project.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp]
+    lib.mla_rmsnorm.argtypes = [vp, vp, i32, i32, i32, vp, ctypes.c_float, vp, i32, vp]
     lib.mla_expand_kv.argtypes = [vp, vp, i32, vp, vp]
     lib.mla_decode_naive_workspace_size.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
     lib.mla_decode_naive.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp, i32, vp, sz, vp, vp]
@@ -178,6 +179,12 @@ class Mla:
     def project(self, x, w, y, stream=None) -> None:
         m, k, n_out = int(x.shape[0]), int(x.shape[1]), int(w.shape[0])
         _check(self._lib.mla_project(self._h, _ptr(x), m, k, _ptr(w), n_out, _ptr(y), _stream(stream)))
+
+    def rmsnorm(self, x, n: int, w, eps: float, y, stream=None) -> None:
+        """RMSNorm of the first n values of every row of the 2-D tensor x into y (may be x)."""
+        m, ld_x, ld_y = int(x.shape[0]), int(x.stride(0)), int(y.stride(0))
+        _check(self._lib.mla_rmsnorm(self._h, _ptr(x), m, int(n), ld_x, _ptr(w), float(eps), _ptr(y), ld_y,
+                                     _stream(stream)))
 
     def expand_kv(self, cache, num_pages: int, kvx, stream=None) -> None:
         _check(self._lib.mla_expand_kv(self._h, _ptr(cache), int(num_pages), _ptr(kvx), _stream(stream)))

@@ -304,6 +304,29 @@ mla_status_t mla_project(mla_handle_t hh, const void* x, int32_t m, int32_t k, c
   return MLA_OK;
 }
 
+mla_status_t mla_rmsnorm(mla_handle_t hh, const void* x, int32_t m, int32_t n, int32_t ld_x, const void* w, float eps,
+                         void* y, int32_t ld_y, mla_stream_t stream) {
+  g_last_error.clear();
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  if (!h) return fail(MLA_ERR_INVALID_ARG, "mla_rmsnorm: handle is NULL");
+  if (m < 0) return fail(MLA_ERR_INVALID_ARG, "mla_rmsnorm: m = %d is negative", m);
+  if (n <= 0 || n % 8 != 0 || n > 8192)
+    return fail(MLA_ERR_INVALID_ARG, "mla_rmsnorm: n = %d must be a positive multiple of 8, at most 8192", n);
+  if (ld_x < n || ld_y < n || ld_x % 8 != 0 || ld_y % 8 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "mla_rmsnorm: ld_x = %d and ld_y = %d must be multiples of 8, at least n = %d",
+                ld_x, ld_y, n);
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(MLA_ERR_INVALID_ARG, "mla_rmsnorm: eps = %g must be >= 0", eps);
+  if (m == 0) return MLA_OK;
+  if (!x || !w || !y) return fail(MLA_ERR_INVALID_ARG, "mla_rmsnorm: x, w or y is NULL");
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16))
+    return fail(MLA_ERR_INVALID_ARG, "mla_rmsnorm: x, w and y must be 16-byte aligned");
+  cudaError_t e = mla::launch_rmsnorm(static_cast<const __nv_bfloat16*>(x), m, n, ld_x,
+                                      static_cast<const __nv_bfloat16*>(w), eps, static_cast<__nv_bfloat16*>(y), ld_y,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
+  return MLA_OK;
+}
+
 mla_status_t mla_expand_kv(mla_handle_t hh, const void* cache, int32_t num_pages, void* kvx, mla_stream_t stream) {
   g_last_error.clear();
   Handle* h = reinterpret_cast<Handle*>(hh);

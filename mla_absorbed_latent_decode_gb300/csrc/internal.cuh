@@ -101,6 +101,9 @@ cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_star
                            int max_q, const int32_t* ctx_len, int batch, int max_ctx, const int32_t* block_table,
                            int bt_stride, const void* cache, int num_pages, void* workspace, void* out,
                            cudaStream_t st, cudaEvent_t between = nullptr);
+// RMSNorm of m strided rows of n values (n a multiple of 8); y may be x.
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, int m, int n, int ld_x, const __nv_bfloat16* w, float eps,
+                           __nv_bfloat16* y, int ld_y, cudaStream_t st);
 // y[m][n_out] = bf16(x[m][k] . w[n_out][k]^T); k a multiple of 256, n_out of 16.
 cudaError_t launch_project(const __nv_bfloat16* x, int m, int k, const __nv_bfloat16* w, int n_out,
                            __nv_bfloat16* y, cudaStream_t st);

@@ -124,7 +124,50 @@ __global__ void __launch_bounds__(kPThreads) kv_project_append_kernel(
   }
 }
 
+// RMSNorm of a row (Zhang & Sennrich 2019): y = x / sqrt(mean(x^2) + eps) * w, the sum of squares
+// in fp32 (each lane over its 8-value chunks, then a shuffle tree), y = bf16((x * inv) * w).
+// One warp per row; a lane reads its chunks in both passes and writes only them, so y may be x.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, int m, int n, int ld_x,
+                                                      const __nv_bfloat16* __restrict__ w, float eps,
+                                                      __nv_bfloat16* y, int ld_y) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  sm100::griddep_wait();
+  sm100::griddep_launch_dependents();
+  if (row >= m) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * ld_x);
+  float ss = 0.0f;
+  for (int c = lane; c < n / 8; c += 32) {
+    const uint4 v = xr[c];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = bf16_lo(u[i]), b = bf16_hi(u[i]);
+      ss = fmaf(a, a, ss);
+      ss = fmaf(b, b, ss);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float inv = 1.0f / sqrtf(ss / (float)n + eps);
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  uint4* yr = reinterpret_cast<uint4*>(y + (size_t)row * ld_y);
+  for (int c = lane; c < n / 8; c += 32) {
+    const uint4 v = xr[c], g = wr[c];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w}, q[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = pack_bf16((bf16_lo(u[i]) * inv) * bf16_lo(q[i]), (bf16_hi(u[i]) * inv) * bf16_hi(q[i]));
+    yr[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, int m, int n, int ld_x, const __nv_bfloat16* w, float eps,
+                           __nv_bfloat16* y, int ld_y, cudaStream_t st) {
+  return launch_pdl(rmsnorm_kernel, dim3((m + 7) / 8), dim3(256), 0, st, x, m, n, ld_x, w, eps, y, ld_y);
+}
 
 cudaError_t launch_project(const __nv_bfloat16* x, int m, int k, const __nv_bfloat16* w, int n_out,
                            __nv_bfloat16* y, cudaStream_t st) {

@@ -118,3 +118,62 @@ def test_v2lite_layer_step_entirely_on_the_gpu():
                                         mla_ref.default_scale(128, 64), 10000.0)
     assert np.max(np.abs(out - full[-1])) <= 2e-2 * np.max(np.abs(full[-1]))
     assert compare(out, out_host, BF16_TOL)[0] <= BF16_TOL
+
+
+@pytest.mark.parametrize("m,n,ld,in_place", [(70, 512, 576, True), (33, 1536, 1536, False), (1, 8, 8, False)])
+def test_rmsnorm_matches_float64(m, n, ld, in_place):
+    rng = np.random.default_rng(m + n)
+    xb = _bits(rng, (m, ld), 1.7)
+    wb = W.to_bf16_bits(1.0 + 0.1 * rng.standard_normal(n))
+    mla = _handle()
+    x = bf16_tensor(xb, "cuda")
+    y = x if in_place else torch.empty((m, ld), dtype=torch.bfloat16, device="cuda")
+    mla.rmsnorm(x, n, bf16_tensor(wb, "cuda"), 1e-6, y)
+    got = bf16_out_to_f64(y)
+    ref = mla_ref.rms_norm(mla_ref.bf16_to_f64(xb)[:, :n], mla_ref.bf16_to_f64(wb), 1e-6)
+    # bf16 rounding of the fp32 result plus the fp32 sum of squares
+    assert np.all(np.abs(got[:, :n] - ref) <= 2.0 ** -8 * np.abs(ref) + 2.0 ** -14 * np.max(np.abs(ref)))
+    if in_place:                                   # the RoPE part of the rows is left alone
+        assert np.array_equal(got[:, n:], mla_ref.bf16_to_f64(xb)[:, n:])
+    with pytest.raises(B.MlaError):
+        mla.rmsnorm(x, 12, bf16_tensor(wb, "cuda"), 1e-6, y)
+    mla.close()
+
+
+def test_layer_step_with_low_rank_query_and_kv_norm():
+    """x -> W_DQ -> [W_UQ ; W_QR] (the low-rank query of "80 行 PyTorch 从零写 DeepSeek 的 MLA"
+    section 2), x -> W_DKV -> kv_norm (RMSNorm of the latent) -> cache -> absorbed decode, all on
+    the GPU, against the oracle's float64 forward of the same layer (multi-stage bf16 rounding:
+    2e-2 of the output's largest magnitude)."""
+    rng = np.random.default_rng(77)
+    T, hidden, d_cq, n_h = 40, 1024, 512, 16
+    eps = 1e-6
+    xb = _bits(rng, (T, hidden), 1.0)
+    w_dq, w_uq, w_qr = _bits(rng, (d_cq, hidden), 0.02), _bits(rng, (n_h * 128, d_cq), 0.05), _bits(rng, (n_h * 64, d_cq), 0.05)
+    w_dkv = _bits(rng, (576, hidden), 0.02)
+    w_kvn = W.to_bf16_bits(1.0 + 0.1 * rng.standard_normal(512))
+    w_uk, w_uv = _bits(rng, (n_h, 128, 512), 0.02), _bits(rng, (n_h, 128, 512), 0.02)
+    # the query weights joined per head as [content rows ; rope rows], so one projection gives q
+    w_uqr = np.concatenate([w_uq.reshape(n_h, 128, d_cq), w_qr.reshape(n_h, 64, d_cq)], axis=1).reshape(n_h * 192, d_cq)
+    wl = W.v2lite_single_step(np.zeros((T, 576), np.uint16), np.zeros((n_h, 192), np.uint16), w_uk, w_uv, n_h=n_h)
+    s = DecodeSession(wl)
+    x = bf16_tensor(xb, "cuda")
+    qz = torch.empty((T, d_cq), dtype=torch.bfloat16, device="cuda")
+    s.mla.project(x, bf16_tensor(w_dq, "cuda"), qz)
+    q_all = torch.empty((T, n_h * 192), dtype=torch.bfloat16, device="cuda")
+    s.mla.project(qz, bf16_tensor(w_uqr, "cuda"), q_all)
+    rows = torch.empty((T, 576), dtype=torch.bfloat16, device="cuda")
+    s.mla.project(x, bf16_tensor(w_dkv, "cuda"), rows)
+    s.mla.rmsnorm(rows, 512, bf16_tensor(w_kvn, "cuda"), eps, rows)          # kv_norm, in place
+    s.append_step(rows, torch.zeros(T, dtype=torch.int32, device="cuda"), torch.arange(T, dtype=torch.int32, device="cuda"))
+    out = bf16_out_to_f64(s.decode(q=q_all[-1:].reshape(1, n_h, 192).contiguous()))[0]
+    assert s.status() == 0
+    s.close()
+    xf = mla_ref.bf16_to_f64(xb)
+    kv = xf @ mla_ref.bf16_to_f64(w_dkv).T
+    c = mla_ref.rms_norm(kv[:, :512], mla_ref.bf16_to_f64(w_kvn), eps)
+    kr = mla_ref.rope(kv[:, 512:], np.arange(T), 10000.0)
+    q = mla_ref.low_rank_query(xf, mla_ref.bf16_to_f64(w_dq), mla_ref.bf16_to_f64(w_uq), mla_ref.bf16_to_f64(w_qr), n_h)
+    ref = mla_ref.absorbed_decode(q[-1], c, kr, mla_ref.bf16_to_f64(w_uk), mla_ref.bf16_to_f64(w_uv), T - 1,
+                                  mla_ref.default_scale(128, 64), 10000.0)
+    assert np.max(np.abs(out - ref)) <= 2e-2 * np.max(np.abs(ref))
