@@ -1,6 +1,7 @@
 // api.cu -- host side of the libmla.so C ABI (include/mla.h): argument and
 // configuration checks, the handle (weights, RoPE table, device check word),
 // workspace layout and the launch sequence of a decode step.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -94,11 +95,15 @@ mla_status_t set_last_error(mla_status_t s, const char* msg) {
   return s;
 }
 
-size_t workspace_bytes(const Handle& h, int batch, Workspace* ws, char* base) {
+size_t workspace_bytes(const Handle& h, int batch, int max_ctx, Workspace* ws, char* base) {
   const int n_h = h.cfg.n_h;
-  // The planner makes at most sum_b ceil(pages_b / target) <= batch + num_pairs units,
-  // or batch * forced splits when the split count is forced.
-  const int max_units = batch * (h.force_splits > 0 ? h.force_splits : 1) + h.num_pairs;
+  // The planner makes at most sum_b ceil(pages_b / target) <= batch + num_pairs units, or
+  // batch * forced splits when the split count is forced; and never more units than a sequence
+  // has pages, at most ceil(max_ctx / 64) each.  The decode grid is sized by this bound, so a
+  // small step (one short sequence) launches one CTA pair, not one per SM pair.
+  const long long by_pages = (long long)batch * ((max_ctx + kPage - 1) / kPage);
+  const int max_units = (int)std::min<long long>(batch * (h.force_splits > 0 ? h.force_splits : 1) + h.num_pairs,
+                                                 std::max<long long>(1, by_pages));
   const int max_parts = max_units;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return base ? base + o : nullptr; };
@@ -452,7 +457,7 @@ mla_status_t mla_decode_workspace_size(mla_handle_t hh, int32_t batch, int32_t m
   if (max_ctx <= 0 || max_ctx > h->cfg.max_position)
     return fail(MLA_ERR_INVALID_ARG, "mla_decode_workspace_size: max_ctx = %d must be in [1, max_position=%d]",
                 max_ctx, h->cfg.max_position);
-  *bytes = mla::workspace_bytes(*h, batch, nullptr, nullptr);
+  *bytes = mla::workspace_bytes(*h, batch, max_ctx, nullptr, nullptr);
   return MLA_OK;
 }
 
@@ -479,7 +484,7 @@ mla_status_t mla_decode(mla_handle_t hh, const void* q, const int32_t* ctx_len, 
   if (!workspace) return fail(MLA_ERR_WORKSPACE, "mla_decode: workspace is NULL");
   if (!aligned(workspace, 256)) return fail(MLA_ERR_WORKSPACE, "mla_decode: workspace must be 256-byte aligned");
   mla::Workspace ws;
-  const size_t need = mla::workspace_bytes(*h, batch, &ws, static_cast<char*>(workspace));
+  const size_t need = mla::workspace_bytes(*h, batch, max_ctx, &ws, static_cast<char*>(workspace));
   if (workspace_bytes < need)
     return fail(MLA_ERR_WORKSPACE, "mla_decode: workspace has %zu bytes, %zu needed", workspace_bytes, need);
 

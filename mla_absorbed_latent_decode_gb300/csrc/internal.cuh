@@ -82,7 +82,7 @@ cudaError_t prepare_weight_maps(Handle& h);
 cudaError_t cache_maps(const Handle& h, const void* cache, int num_pages);
 
 // Workspace sizing and carving (host).
-size_t workspace_bytes(const Handle& h, int batch, Workspace* carve, char* base);
+size_t workspace_bytes(const Handle& h, int batch, int max_ctx, Workspace* carve, char* base);
 
 // The calling thread's message for mla_last_error (kept in api.cu).
 void clear_last_error();

@@ -50,7 +50,7 @@ def test_fixed_scratch_matches_workspace_decode(n_h, lengths, dtype):
 
 
 def test_fixed_scratch_rejects_a_batch_beyond_its_size():
-    wl = W.make_decode("fixed_big", 5, 128, [1] * 26)
+    wl = W.make_decode("fixed_big", 5, 128, [4096] * 26)   # split partials for 26 + 76 units: > 32 MiB
     s = DecodeSession(wl)
     need = s.mla.decode_workspace_size(wl.B, wl.max_ctx)
     assert need > B.MLA_FIXED_SCRATCH_BYTES
