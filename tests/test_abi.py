@@ -104,6 +104,16 @@ def test_null_arguments(lib):
     assert lib.mla_profile_kernel_name(1) == b"mla_decode_splitkv"
     assert lib.mla_profile_kernel_name(0) == b"mla_q_absorb_plan"
     assert lib.mla_profile_kernel_name(3) == b""
+    # the entry points beyond the decode step
+    assert lib.mla_kv_project_append(None, 1, 256, 1, 1, 1, 1, 1, 1, 1, 1, 1, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_project(None, 1, 1, 256, 1, 16, 1, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_rmsnorm(None, 1, 1, 8, 8, 1, 1e-6, 1, 8, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_expand_kv(None, 1, 1, 1, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_naive_workspace_size(None, 1, 1, ctypes.byref(sz)) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_naive(None, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_prefill_workspace_size(None, 1, 1, ctypes.byref(sz)) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_prefill(None, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, None) == B.MLA_ERR_INVALID_ARG
+    assert lib.mla_profile_last_name(None, 0) == b""
 
 
 def test_valid_config_without_gpu_fails_cleanly(lib):

@@ -55,3 +55,23 @@ def test_named_shapes_small_draws():
     assert wl.w_uv.shape == (128, 128, 512)
     w = mla_ref.bf16_to_f64(wl.w_uk)
     assert 0.015 < w.std() < 0.025
+
+
+def test_prefill_inputs_follow_the_decode_draws():
+    """make_prefill keeps make_decode's rows, weights and pages (same seed, same stream) and adds
+    the chunk's queries from a second stream: packed in sequence order, deterministic."""
+    a = W.make_prefill("p", 9, 16, [130, 5, 64], [30, 5, 1])
+    d = W.make_decode("p", 9, 16, [130, 5, 64])
+    assert np.array_equal(a.rows, d.rows) and np.array_equal(a.block_table, d.block_table)
+    assert np.array_equal(a.w_uk, d.w_uk) and np.array_equal(a.q, d.q)
+    p = a.extra["prefill"]
+    assert p["q"].shape == (36, 16, 192)
+    assert list(p["q_start"]) == [0, 30, 35] and list(p["q_len"]) == [30, 5, 1]
+    b = W.make_prefill("p", 9, 16, [130, 5, 64], [30, 5, 1])
+    assert np.array_equal(p["q"], b.extra["prefill"]["q"])
+    whole = W.make_prefill("p", 9, 16, [130, 5, 64])
+    assert list(whole.extra["prefill"]["q_len"]) == [130, 5, 64]
+
+
+def test_cache_row_bytes():
+    assert W.ROW_BYTES == {W.CACHE_BF16: 1152, W.CACHE_FP8: 576, W.CACHE_FP8_BLOCK: 656}
