@@ -42,6 +42,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "absorbed-MLA decode µs/step, latent-KV GB/s and % of roofline at B×s_ctx"
 DECODE_SOURCES = ["mla_absorbed_latent_decode_gb300/csrc/decode_tc.cu"]
+PREFILL_SOURCES = ["mla_absorbed_latent_decode_gb300/csrc/prefill.cu"]
 
 
 def parse():
@@ -288,24 +289,24 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sms)}
 
 
-def decode_source_hash():
+def source_hash(sources=DECODE_SOURCES):
     h = hashlib.sha256()
-    for rel in DECODE_SOURCES:
+    for rel in sources:
         p = os.path.join(ROOT, rel)
         if os.path.exists(p):
             h.update(open(p, "rb").read())
     return h.hexdigest()
 
 
-def ncu_traffic(wl):
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if it was
-    taken on the current decode source for this workload; else None."""
-    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+def ncu_traffic(wl, summary="decode_traffic.json", sources=DECODE_SOURCES):
+    """Per-launch DRAM bytes of a kernel from a committed ncu summary, if it was taken on the
+    current source of that kernel for this workload; else None."""
+    p = os.path.join(ROOT, "profiles", summary)
     try:
         d = json.load(open(p))
     except Exception:
         return None
-    if d.get("source_sha256") != decode_source_hash() or d.get("workload") != wl.name:
+    if d.get("source_sha256") != source_hash(sources) or d.get("workload") != wl.name:
         return None
     return d.get("bytes_per_launch")
 
@@ -901,7 +902,8 @@ def run_prefill(args, wl):
                        "parallelism": f"replicas x{world}"},
             "per_kernel_us": per_kernel,
             "roofline": {"bound": "tensor", "kernel": "mla_prefill_attention", "achieved": round(achieved, 1),
-                         "peak": tc_burst, "unit": "TFLOP/s", "frac": round(achieved / tc_burst, 4), "traffic": None,
+                         "peak": tc_burst, "unit": "TFLOP/s", "frac": round(achieved / tc_burst, 4),
+                         "traffic": ncu_traffic(wl, "prefill_traffic.json", PREFILL_SOURCES),
                          "peak_source": f"{peak_kind} bf16_tflops (burst)",
                          "algorithmic_flops_per_launch": int(fa),
                          "expansion": {"achieved": round(fe / (exp_ms * 1e-3) / 1e12, 1),
