@@ -371,6 +371,13 @@ mla_status_t mla_get_status(mla_handle_t h, mla_stream_t stream, uint32_t* devic
 #define MLA_OPT_PROFILE 2   /* value 1: record CUDA events around each kernel mla_decode and
                                mla_prefill launch (which serialises them); mla_profile_read
                                returns the durations. 0: off. */
+#define MLA_OPT_TEST_STALL 3 /* test of the bounded in-kernel waits.  value 1: every later
+                               mla_decode's query-absorb kernel withholds its query copy, so
+                               the thread waiting for it gives up after about a second (of
+                               2e9 clocks), the step still completes, mla_get_status reports
+                               MLA_CHECK_TIMEOUT and that step's output is undefined.  0 (the
+                               default): off.  A CUDA graph keeps the value it was captured
+                               with. */
 
 mla_status_t mla_set_option(mla_handle_t h, int32_t option, int64_t value);
 

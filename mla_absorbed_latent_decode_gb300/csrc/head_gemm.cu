@@ -71,8 +71,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_out, int B, int n_h,
                 int max_ctx, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ ctx_len,
-                const float2* __restrict__ rope_cs, int max_position, int num_pairs, int forced, Workspace ws,
-                unsigned* check) {
+                const float2* __restrict__ rope_cs, int max_position, int num_pairs, int forced, int stall,
+                Workspace ws, unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int red[64];
   const uint32_t raw = smem_u32(smem_raw);
@@ -111,9 +111,11 @@ q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     griddep_wait();                        // the queries may come from the previous kernel
     griddep_launch_dependents();
     const uint32_t qf = smem_u32(&bars->full[0]);
-    mbar_arrive_expect_tx(qf, 2u * kBox);
-    load_rows(a_st, &tm_q, 0, h, n0, qf);
-    load_rows(a_st + kBox, &tm_q, 64, h, n0, qf);
+    if (!stall) {                          // (a test of the bounded waits withholds the copy)
+      mbar_arrive_expect_tx(qf, 2u * kBox);
+      load_rows(a_st, &tm_q, 0, h, n0, qf);
+      load_rows(a_st + kBox, &tm_q, 64, h, n0, qf);
+    }
     bool ok = mbar_wait(qf, 0, abort_flag);
     constexpr uint32_t idesc = idesc_bf16_f32(128, 256, false, true);
     const uint64_t a0 = sdesc_sw128(a_st, 16, 1024), b0 = sdesc_sw128(w_st, kBox, 1024);
@@ -422,7 +424,8 @@ cudaError_t launch_q_absorb(const Handle& h, const __nv_bfloat16* q, const int32
   dim3 grid(h.cfg.n_h + 1, 1, (batch + kQaM - 1) / kQaM);     // + 1: the planner CTA
   return launch_pdl(q_absorb_kernel, grid, dim3(kThreads), kQaSmem, st,
                     *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk), tq, tout, batch, h.cfg.n_h, max_ctx, q, ctx_len,
-                    (const float2*)h.rope_cs, h.cfg.max_position, h.num_pairs, h.force_splits, ws, h.check_word);
+                    (const float2*)h.rope_cs, h.cfg.max_position, h.num_pairs, h.force_splits, h.test_stall, ws,
+                    h.check_word);
 }
 
 cudaError_t launch_combine_uv(const Handle& h, int batch, const Workspace& ws, __nv_bfloat16* out, cudaStream_t st) {

@@ -64,6 +64,7 @@ struct Handle {
   unsigned* check_word;     // device check word
   int force_splits;         // MLA_OPT_SPLITS
   int profile;              // MLA_OPT_PROFILE
+  int test_stall;           // MLA_OPT_TEST_STALL
   cudaEvent_t ev[8];
   int n_ev_recorded;
   int prof_prefill;         // the last profiled call was mla_prefill (else mla_decode)

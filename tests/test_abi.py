@@ -126,3 +126,15 @@ def test_valid_config_without_gpu_fails_cleanly(lib):
     s = lib.mla_create(ctypes.byref(cfg), 1, 1, None, ctypes.byref(h))
     assert s in (B.MLA_ERR_CUDA, B.MLA_ERR_UNSUPPORTED)
     assert not h.value
+
+
+def test_header_constants_match_the_binding():
+    """Every integer #define of include/mla.h that the binding also names has the same value."""
+    import re
+    text = open(HEADER).read()
+    found = 0
+    for name, val in re.findall(r"#define\s+(MLA_\w+)\s+(0x[0-9a-fA-F]+|\d+)u?\b", text):
+        if hasattr(B, name):
+            assert getattr(B, name) == int(val, 0), name
+            found += 1
+    assert found >= 7          # the check bits and the options
