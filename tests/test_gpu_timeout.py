@@ -20,6 +20,8 @@ def test_a_wait_that_never_completes_times_out_and_the_context_survives():
     s = DecodeSession(wl)
     s.append_rows()
     assert s.status() == 0
+    with pytest.raises(B.MlaError, match="MLA_OPT_TEST_STALL"):
+        s.mla.set_option(B.MLA_OPT_TEST_STALL, 2)
     s.mla.set_option(B.MLA_OPT_TEST_STALL, 1)
     t0 = time.monotonic()
     s.decode()
