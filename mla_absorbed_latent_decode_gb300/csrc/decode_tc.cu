@@ -727,6 +727,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       volatile int never = 0;
       mbar_wait<true>(smem_u32(&bars->recvfull[(armed - 1) & (kSlots - 1)]), ((armed - 1) >> 2) & 1, &never);
     }
+    // and every copy this warp sent has landed in the peer before the cluster may exit (after a
+    // timeout the peer need not have waited for it)
+    if (lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
