@@ -95,3 +95,119 @@ def compare(out_gpu: np.ndarray, ref: np.ndarray, tol: float):
 
 def bf16_out_to_f64(t) -> np.ndarray:
     return mla_ref.bf16_to_f64(t.view(__import__("torch").int16).cpu().numpy().view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# inputs that force the online softmax's lazy rescale
+# ---------------------------------------------------------------------------
+
+LOG2E = 1.4426950408889634
+RESCALE_STEP = 8.0        # the kernels rescale O when a row's running maximum grows by more than this (log2 units)
+
+
+def controlled_rows(q_lat, q_pe_rot, k_r, targets, scale, seed):
+    """Latent rows whose scores against the given queries are prescribed.
+
+    q_lat [P, d_c] and q_pe_rot [P, d_rope] are the absorbed queries (latent part; RoPE part
+    rotated at the query's position) of P (query, head) pairs; k_r [T, d_rope] the RoPE keys of
+    the T rows as cached (rotated at their positions); targets [T, P] the wanted scores
+    ``scale * (q_lat . c_t + q_pe . k_r,t)`` in log2 units.  Returns the latent rows c [T, d_c]:
+    the minimum-norm solution in the span of the q_lat rows plus a random component
+    orthogonal to that span (which leaves every score unchanged).  P <= d_c."""
+    sc = scale * LOG2E
+    want = targets / sc - k_r @ q_pe_rot.T                     # [T, P]: latent part of each raw score
+    gram = q_lat @ q_lat.T
+    u = (q_lat.T @ np.linalg.solve(gram, want.T)).T           # [T, d_c]
+    r = np.random.default_rng(seed).standard_normal(u.shape)
+    r -= (q_lat.T @ np.linalg.solve(gram, q_lat @ r.T)).T
+    return u + r
+
+
+def rescale_targets(n_rows, n_pairs, tile, visible, seed, plateau=16.0, jump=9.0, groups=6):
+    """Scores [n_rows, n_pairs] (log2 units) that force every (query, head) pair to rescale once.
+
+    Pair p sees rows 0 .. visible[p] - 1.  Its rows in key tiles 0 .. g(p) - 1 score within
+    0.25 of ``plateau``; one row of tile g(p) scores ``plateau + jump`` (jump > the rescale
+    step, so the running maximum must grow there, at a tile j = g(p) > 0); every later row scores
+    about ``plateau - 12``.  g(p) cycles through 1 .. groups (both parities), capped by the
+    pair's last visible tile.  The plateau's 64 g(p) rows keep a weight of about
+    64 g(p) 2^-jump against the single high row, so a wrong rescale factor shows in the output.
+    Returns (targets, g, row of the jump)."""
+    rng = np.random.default_rng(seed)
+    d = plateau - 12.0 + rng.uniform(-0.5, 0.5, (n_rows, n_pairs))
+    tile_of = np.arange(n_rows)[:, None] // tile
+    last_tile = (np.asarray(visible) - 1) // tile
+    g = np.minimum(1 + np.arange(n_pairs) % groups, last_tile)
+    early = tile_of < g[None, :]
+    d[early] = plateau + rng.uniform(-0.25, 0.25, int(early.sum()))
+    hit = np.minimum(g * tile + (np.arange(n_pairs) * 7) % tile, np.asarray(visible) - 1)
+    d[hit, np.arange(n_pairs)] = plateau + jump
+    return d, g, hit
+
+
+def force_decode_rescale(wl, seed=3, jump=None):
+    """Rewrite the latent part of every sequence's rows (of at least 3 pages) so that each head
+    rescales at a tile of its own (:func:`rescale_targets` with 64-token tiles, the decode
+    kernel's tile).  An e4m3 cache moves scores by up to ~0.3 (log2 units), so its jump is 10
+    instead of 9.  Returns {sequence: g per head} for the sequences rewritten."""
+    if jump is None:
+        jump = 9.0 if wl.cache_dtype == W.CACHE_BF16 else 10.0
+    q = mla_ref.bf16_to_f64(wl.q)
+    w_uk = mla_ref.bf16_to_f64(wl.w_uk)
+    scale = mla_ref.default_scale(wl.d_nope, wl.d_rope)
+    starts = np.concatenate([[0], np.cumsum(wl.ctx_len.astype(np.int64))])
+    forced = {}
+    for b in range(wl.B):
+        L = int(wl.ctx_len[b])
+        if L < 2 * wl.page_size + 1:
+            continue
+        qa = mla_ref.absorb_query(q[b], w_uk, L - 1, wl.rope_base)             # [n_h, 576]
+        rows = mla_ref.bf16_to_f64(wl.rows[starts[b]:starts[b + 1]])
+        k_r = mla_ref.rope(rows[:, wl.d_c:], np.arange(L), wl.rope_base)
+        d, g, _ = rescale_targets(L, wl.n_h, wl.page_size, np.full(wl.n_h, L), seed + b, jump=jump)
+        c = controlled_rows(qa[:, :wl.d_c], qa[:, wl.d_c:], k_r, d, scale, seed + 1000 + b)
+        rows[:, :wl.d_c] = c
+        wl.rows[starts[b]:starts[b + 1]] = mla_ref.bf16_round(rows.astype(np.float32))
+        forced[b] = g
+    if wl.cache_dtype == W.CACHE_FP8:                  # the tensor scale bounds the rewritten rows too
+        wl.fp8_scale = W.fp8_tensor_scale(wl.rows, wl.d_c)
+    return forced
+
+
+PREFILL_KEY_TILE = 128    # keys per tile of the prefill attention kernel
+
+
+def force_prefill_rescale(wl, seed=5):
+    """Same for a prefill workload: every (query, head) pair of every sequence whose chunk sees at
+    least three key tiles rescales at a key tile of its own (128-key tiles).  The chunk's
+    q_len * n_h pairs must not exceed d_c.  Returns {sequence: g per pair}."""
+    p = wl.extra["prefill"]
+    q = mla_ref.bf16_to_f64(p["q"])
+    w_uk = mla_ref.bf16_to_f64(wl.w_uk)
+    scale = mla_ref.default_scale(wl.d_nope, wl.d_rope)
+    starts = np.concatenate([[0], np.cumsum(wl.ctx_len.astype(np.int64))])
+    forced = {}
+    for b in range(wl.B):
+        L, n, a = int(wl.ctx_len[b]), int(p["q_len"][b]), int(p["q_start"][b])
+        pos0 = L - n
+        if n == 0 or pos0 + 1 < 2 * PREFILL_KEY_TILE + 1:
+            continue
+        assert n * wl.n_h <= wl.d_c, "too many (query, head) pairs to prescribe every score"
+        qa = np.concatenate([mla_ref.absorb_query(q[a + i], w_uk, pos0 + i, wl.rope_base) for i in range(n)])
+        visible = np.repeat(pos0 + 1 + np.arange(n), wl.n_h)
+        rows = mla_ref.bf16_to_f64(wl.rows[starts[b]:starts[b + 1]])
+        k_r = mla_ref.rope(rows[:, wl.d_c:], np.arange(L), wl.rope_base)
+        d, g, _ = rescale_targets(L, n * wl.n_h, PREFILL_KEY_TILE, visible, seed + b)
+        rows[:, :wl.d_c] = controlled_rows(qa[:, :wl.d_c], qa[:, wl.d_c:], k_r, d, scale, seed + 1000 + b)
+        wl.rows[starts[b]:starts[b + 1]] = mla_ref.bf16_round(rows.astype(np.float32))
+        forced[b] = g
+    return forced
+
+
+def decode_scores_log2(wl, values, b):
+    """The oracle's scores of sequence b in log2 units [n_h, L] (fp64, from its cached values)."""
+    starts = np.concatenate([[0], np.cumsum(wl.ctx_len.astype(np.int64))])
+    L = int(wl.ctx_len[b])
+    rows = values[starts[b]:starts[b + 1]]
+    qa = mla_ref.absorb_query(mla_ref.bf16_to_f64(wl.q[b]), mla_ref.bf16_to_f64(wl.w_uk), L - 1, wl.rope_base)
+    return mla_ref.default_scale(wl.d_nope, wl.d_rope) * LOG2E * (qa @ rows.T)

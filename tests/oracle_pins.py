@@ -344,9 +344,61 @@ def pin_low_rank_query(ref):
     assert np.max(np.abs(b[:, 1, :dn] - qz @ w_uq2[dn:2 * dn].T)) <= 1e-13
 
 
+# --------------------------------------------------------------------------- paged cache
+
+def pin_paged_cache(ref):
+    """The paged indirection (a reading of "DeepSeek-V2-Lite 真实权重执行审计" §3.3, which asks
+    for a paged latent-only cache without fixing its layout): token ``pos`` of a sequence
+    lives in the page its block-table row names at ``pos // page``, slot ``pos % page``.
+
+    Fixed by hand on a 3-sequence table with 4-token pages (slots and pages written out,
+    not computed); gathering follows block-table order, not page-id order; and the batched
+    decode over a shuffled paged cache equals the contiguous decode of each sequence's
+    rows with the query at position ``len - 1``."""
+    bt = np.array([[5, 2, -1], [0, 7, 3], [4, -1, -1]], np.int32)
+    expect = {(0, 0): (5, 0), (0, 3): (5, 3), (0, 5): (2, 1), (1, 3): (0, 3), (1, 4): (7, 0),
+              (1, 9): (3, 1), (1, 11): (3, 3), (2, 2): (4, 2)}
+    for (seq, pos), ps in expect.items():
+        assert ref.page_slot(bt, seq, pos, 4) == ps, (seq, pos, ref.page_slot(bt, seq, pos, 4))
+    # value of a cached row = 1000 page + slot: sequence 1's first 10 rows, written out
+    cache = np.full((8, 4, 2), np.nan)
+    for page in range(8):
+        for slot in range(4):
+            cache[page, slot] = (1000.0 * page + slot, -1.0)
+    got = ref.gather_sequence(cache, bt, 1, 10, 4)[:, 0]
+    assert got.tolist() == [0, 1, 2, 3, 7000, 7001, 7002, 7003, 3000, 3001], got
+    assert ref.gather_sequence(cache, bt, 0, 6, 4)[:, 0].tolist() == [5000, 5001, 5002, 5003, 2000, 2001]
+    assert ref.gather_sequence(cache, bt, 2, 1, 4)[:, 0].tolist() == [4000]
+    # decode over a shuffled pool (NaN everywhere no row was written) = contiguous decode
+    rng = np.random.default_rng(31)
+    n_h, d_c, d_r, lens, page = 3, 6, 4, [5, 9, 1], 4
+    q = rng.standard_normal((3, n_h, 4 + d_r))
+    w_uk = rng.standard_normal((n_h, 4, d_c)) * 0.5
+    w_uv = rng.standard_normal((n_h, 5, d_c)) * 0.5
+    rows = [rng.standard_normal((L, d_c + d_r)) for L in lens]
+    order = rng.permutation(9)                       # 2 + 3 + 1 pages used out of 9
+    table = np.full((3, 3), -1, np.int32)
+    pool = np.full((9, page, d_c + d_r), np.nan)
+    nxt = 0
+    for b, L in enumerate(lens):
+        for i in range(-(-L // page)):               # whole pages copied block by block
+            table[b, i] = order[nxt]
+            blk = rows[b][i * page:(i + 1) * page]
+            pool[order[nxt], :len(blk)] = blk
+            nxt += 1
+    s = ref.default_scale(4, d_r)
+    out = ref.decode_batch(q, pool, table, np.array(lens), w_uk, w_uv, d_c, page, s, BASE)
+    for b, L in enumerate(lens):
+        want = ref.absorbed_decode(q[b], rows[b][:, :d_c], rows[b][:, d_c:], w_uk, w_uv, L - 1, s, BASE)
+        assert np.all(np.isfinite(out[b])) and np.max(np.abs(out[b] - want)) <= 1e-13
+    nv = ref.decode_batch(q, pool, table, np.array(lens), w_uk, w_uv, d_c, page, s, BASE, path="naive")
+    assert np.max(np.abs(nv - out)) <= 1e-12
+
+
 ALL_PINS = [
     pin_rope_closed_forms, pin_rope_relative_position, pin_scale_worked_example,
     pin_naive_equals_absorbed, pin_rope_on_content_breaks_absorption, pin_closed_forms,
     pin_split_lse_identity, pin_one_shot_equals_incremental, pin_prefill_rows_are_decodes, pin_cache_bytes,
     pin_mha_ratio_and_read_bytes, pin_fp8_block_format, pin_rms_norm, pin_low_rank_query,
+    pin_paged_cache,
 ]

@@ -8,8 +8,8 @@ import torch
 from mla_absorbed_latent_decode_gb300 import binding as B
 from mla_absorbed_latent_decode_gb300 import workloads as W
 from mla_absorbed_latent_decode_gb300.runner import DecodeSession
-from tests.mla_cases import (BF16_TOL, FP8_TOL, bf16_out_to_f64, compare, oracle_decode,
-                             oracle_decode_paged, oracle_stored, oracle_values)
+from tests.mla_cases import (BF16_TOL, FP8_TOL, bf16_out_to_f64, compare, force_decode_rescale, oracle_decode,
+                             oracle_decode_paged, oracle_stored, oracle_values, tolerance)
 
 pytestmark = pytest.mark.gpu
 
@@ -158,4 +158,30 @@ def test_decode_host_argument_errors():
     with pytest.raises(B.MlaError) as e:
         s.mla.decode(s.q, s.ctx_len, 10 ** 6, s.block_table, s.cache, wl.num_pages, s.workspace, s.out)
     assert e.value.status == B.MLA_ERR_INVALID_ARG
+    s.close()
+
+
+RESCALE_LENS = [1000, 700, 300, 129, 65, 1]
+
+
+@pytest.mark.parametrize("n_h,splits,dtype", [
+    (16, 0, W.CACHE_BF16), (16, 3, W.CACHE_BF16), (40, 0, W.CACHE_BF16),
+    (128, 0, W.CACHE_BF16), (128, 1, W.CACHE_BF16), (128, 3, W.CACHE_BF16), (128, 64, W.CACHE_BF16),
+    (128, 0, W.CACHE_FP8), (24, 2, W.CACHE_FP8_BLOCK),
+])
+def test_forced_rescale_matches_oracle(n_h, splits, dtype):
+    """Every head of every sequence of at least 3 pages has a score plateau, then a row more than
+    the rescale step above it in a tile j >= 1 of its own (both tile parities), so the running
+    maximum grows inside a unit and O, the row sums and the two tile groups' maxima are re-based
+    there (tests/test_rescale_inputs.py checks the construction on the oracle's scores); the
+    plateau keeps 13-60 % of the final weight, so a wrong rescale factor shows.  Forced splits
+    move the unit boundaries (64: one page per unit, the rescale then happens in the merge)."""
+    wl = W.make_decode("rescale", 90 + n_h, n_h, RESCALE_LENS, cache_dtype=dtype)
+    forced = force_decode_rescale(wl)
+    assert sorted(forced) == [0, 1, 2, 3]
+    s, out, flags = _run(wl, splits=splits)
+    assert flags == 0
+    ref = oracle_decode_paged(wl, oracle_values(wl, oracle_stored(wl)))
+    rel, err, scale = compare(out, ref, tolerance(wl))
+    assert rel <= tolerance(wl), (rel, err, scale)
     s.close()

@@ -10,7 +10,7 @@ from mla_absorbed_latent_decode_gb300 import binding as B
 from mla_absorbed_latent_decode_gb300 import workloads as W
 from mla_absorbed_latent_decode_gb300.runner import DecodeSession, bf16_tensor
 from oracle import mla_ref
-from tests.mla_cases import BF16_TOL, bf16_out_to_f64, compare, oracle_stored, oracle_values
+from tests.mla_cases import BF16_TOL, bf16_out_to_f64, compare, force_prefill_rescale, oracle_stored, oracle_values
 
 pytestmark = pytest.mark.gpu
 
@@ -133,4 +133,24 @@ def test_prefill_argument_errors():
     with pytest.raises(B.MlaError) as e:
         s.mla.prefill(q, i, i, 10, s.ctx_len, 10, s.block_table, s.cache, wl.num_pages, ws[:-1], out)
     assert e.value.status == B.MLA_ERR_WORKSPACE
+    s.close()
+
+
+@pytest.mark.parametrize("n_h,ctx,ql", [(16, [700, 1100, 64], [8, 4, 64]), (5, [900, 300], [100, 40])])
+def test_prefill_forced_rescale_matches_the_oracle(n_h, ctx, ql):
+    """Every (query, head) pair of the long chunks has a score plateau and then, in a key tile
+    j >= 1 of its own, a key more than the rescale step above it, so the prefill's running row
+    maximum grows and O is re-based there (tests/test_rescale_inputs.py checks the construction)."""
+    wl = W.make_prefill("prefill_rescale", 95 + n_h, n_h, ctx, ql)
+    forced = force_prefill_rescale(wl)
+    assert forced
+    s = DecodeSession(wl)
+    s.append_rows()
+    out = bf16_out_to_f64(_prefill(s, wl))
+    assert s.status() == 0
+    p = wl.extra["prefill"]
+    for b, ref in _oracle(wl).items():
+        a, n = int(p["q_start"][b]), int(p["q_len"][b])
+        err = compare(out[a:a + n], ref, BF16_TOL)
+        assert err[0] <= BF16_TOL, (b, err)
     s.close()

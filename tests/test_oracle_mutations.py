@@ -126,6 +126,24 @@ def _fp8_block_with(per_row=False, sat=448.0, quantise_rope=False):
     return stored
 
 
+def _gather_pages_sorted(cache_values, block_table, seq, length, page_size):
+    n_pages = (length + page_size - 1) // page_size
+    ids = sorted(int(block_table[seq][i]) for i in range(n_pages))
+    pages = [cache_values[i] for i in ids]
+    return np.concatenate(pages, axis=0)[:length] if pages else np.zeros((0, cache_values.shape[-1]))
+
+
+def _decode_batch_query_at_len(q, cache_values, block_table, ctx_len, w_uk, w_uv, d_c, page_size, scale, base,
+                               seqs=None, path="absorbed"):
+    fn = _orig["absorbed_decode"] if path == "absorbed" else _orig["naive_decode"]
+    out = []
+    for b in (range(q.shape[0]) if seqs is None else seqs):
+        L = int(ctx_len[b])
+        rows = _orig["gather_sequence"](cache_values, block_table, b, L, page_size)
+        out.append(fn(q[b], rows[:, :d_c], rows[:, d_c:], w_uk, w_uv, L, scale, base))
+    return np.stack(out)
+
+
 MUTATIONS = {
     "rope_rotates_backwards": ("rope", _rope_with(sign=-1.0)),
     "rope_frequency_step_1": ("rope", _rope_with(freq_step=1)),
@@ -149,6 +167,10 @@ MUTATIONS = {
     "read_bytes_times_heads": ("decode_kv_read_bytes", lambda B, s, d_c, d_r, e: _orig["decode_kv_read_bytes"](B, s, d_c, d_r, e) * 2),
     "split_merge_weighted_by_length": ("split_latent", _split_linear_merge),
     "up_projection_skipped": ("up_project", lambda o_lat, w_uv: o_lat[:, : w_uv.shape[1]]),
+    "page_slot_divides_the_wrong_way": ("page_slot", lambda bt, seq, pos, ps: (int(bt[seq][pos % ps]), int(pos // ps))),
+    "page_slot_off_by_one_page": ("page_slot", lambda bt, seq, pos, ps: (int(bt[seq][(pos + 1) // ps]), int(pos % ps))),
+    "gather_pages_in_id_order": ("gather_sequence", _gather_pages_sorted),
+    "decode_batch_query_at_len": ("decode_batch", _decode_batch_query_at_len),
 }
 
 
