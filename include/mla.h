@@ -348,9 +348,11 @@ mla_status_t mla_decode(mla_handle_t h, const void* q, const int32_t* ctx_len, i
  *   - All calls on one device share the array, whatever the handle or stream:
  *     calls whose execution overlaps race and corrupt each other's results.
  *     Order them on one stream, or with events.
- *   - The first call on a device looks the array up (cudaGetSymbolAddress),
+ *   - The first call in a CUDA context looks the array up (cudaGetSymbolAddress),
  *     which may load the library's module there: make it before any stream
- *     capture begins.
+ *     capture begins.  The address is cached with the context it was taken in;
+ *     after a device reset, or with another context current, the next call looks
+ *     it up again, and that call too must come before any stream capture.
  */
 mla_status_t mla_decode_fixed_scratch(mla_handle_t h, const void* q, const int32_t* ctx_len,
                                       int32_t batch, int32_t max_ctx, const int32_t* block_table,
@@ -371,13 +373,18 @@ mla_status_t mla_get_status(mla_handle_t h, mla_stream_t stream, uint32_t* devic
 #define MLA_OPT_PROFILE 2   /* value 1: record CUDA events around each kernel mla_decode and
                                mla_prefill launch (which serialises them); mla_profile_read
                                returns the durations. 0: off. */
-#define MLA_OPT_TEST_STALL 3 /* test of the bounded in-kernel waits.  value 1: every later
-                               mla_decode's query-absorb kernel withholds its query copy, so
-                               the thread waiting for it gives up after about a second (of
-                               2e9 clocks), the step still completes, mla_get_status reports
-                               MLA_CHECK_TIMEOUT and that step's output is undefined.  0 (the
-                               default): off.  A CUDA graph keeps the value it was captured
-                               with. */
+#define MLA_OPT_TEST_STALL 3 /* test of the bounded in-kernel waits: every later mla_decode
+                               withholds one copy, so the thread waiting for it gives up after
+                               about a second (of 2e9 clocks), the kernel drains what it has in
+                               flight, the step still completes, mla_get_status reports
+                               MLA_CHECK_TIMEOUT and that step's output is undefined.
+                               value 1: the query-absorb kernel's query copy; 2: one cache tile
+                               of the first decode work unit (its first CTA's tile 1); 3: one
+                               partial-score copy between the two CTAs of that unit (tile 1, the
+                               second CTA's first lane quarter).  For mla_prefill: 4: one weight
+                               box of the expansion kernel's first CTA; 5: one key box of the
+                               attention kernel (sequence 0, head 0, first query block).  0 (the default): off.  A CUDA
+                               graph keeps the value it was captured with. */
 
 mla_status_t mla_set_option(mla_handle_t h, int32_t option, int64_t value);
 

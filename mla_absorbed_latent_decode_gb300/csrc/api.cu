@@ -95,15 +95,19 @@ mla_status_t set_last_error(mla_status_t s, const char* msg) {
   return s;
 }
 
-size_t workspace_bytes(const Handle& h, int batch, int max_ctx, Workspace* ws, char* base) {
-  const int n_h = h.cfg.n_h;
+long long decode_unit_bound(const Handle& h, int batch, int max_ctx) {
   // The planner makes at most sum_b ceil(pages_b / target) <= batch + num_pairs units, or
   // batch * forced splits when the split count is forced; and never more units than a sequence
   // has pages, at most ceil(max_ctx / 64) each.  The decode grid is sized by this bound, so a
   // small step (one short sequence) launches one CTA pair, not one per SM pair.
   const long long by_pages = (long long)batch * ((max_ctx + kPage - 1) / kPage);
-  const int max_units = (int)std::min<long long>(batch * (h.force_splits > 0 ? h.force_splits : 1) + h.num_pairs,
-                                                 std::max<long long>(1, by_pages));
+  const long long by_plan = (long long)batch * (h.force_splits > 0 ? h.force_splits : 1) + h.num_pairs;
+  return std::min<long long>(by_plan, std::max<long long>(1, by_pages));
+}
+
+size_t workspace_bytes(const Handle& h, int batch, int max_ctx, Workspace* ws, char* base) {
+  const int n_h = h.cfg.n_h;
+  const int max_units = (int)decode_unit_bound(h, batch, max_ctx);   // callers reject bounds > kMaxUnits
   const int max_parts = max_units;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return base ? base + o : nullptr; };
@@ -457,6 +461,9 @@ mla_status_t mla_decode_workspace_size(mla_handle_t hh, int32_t batch, int32_t m
   if (max_ctx <= 0 || max_ctx > h->cfg.max_position)
     return fail(MLA_ERR_INVALID_ARG, "mla_decode_workspace_size: max_ctx = %d must be in [1, max_position=%d]",
                 max_ctx, h->cfg.max_position);
+  if (mla::decode_unit_bound(*h, batch, max_ctx) > mla::kMaxUnits)
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode_workspace_size: batch = %d with the split option gives more than %d work units",
+                batch, mla::kMaxUnits);
   *bytes = mla::workspace_bytes(*h, batch, max_ctx, nullptr, nullptr);
   return MLA_OK;
 }
@@ -483,6 +490,9 @@ mla_status_t mla_decode(mla_handle_t hh, const void* q, const int32_t* ctx_len, 
     return fail(MLA_ERR_INVALID_ARG, "mla_decode: q and out must be 16-byte aligned, cache 128-byte aligned");
   if (!workspace) return fail(MLA_ERR_WORKSPACE, "mla_decode: workspace is NULL");
   if (!aligned(workspace, 256)) return fail(MLA_ERR_WORKSPACE, "mla_decode: workspace must be 256-byte aligned");
+  if (mla::decode_unit_bound(*h, batch, max_ctx) > mla::kMaxUnits)
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode: batch = %d with the split option gives more than %d work units", batch,
+                mla::kMaxUnits);
   mla::Workspace ws;
   const size_t need = mla::workspace_bytes(*h, batch, max_ctx, &ws, static_cast<char*>(workspace));
   if (workspace_bytes < need)
@@ -544,7 +554,7 @@ mla_status_t mla_set_option(mla_handle_t hh, int32_t option, int64_t value) {
       h->n_ev_recorded = 0;
       return MLA_OK;
     case MLA_OPT_TEST_STALL:
-      if (value != 0 && value != 1) return fail(MLA_ERR_INVALID_ARG, "MLA_OPT_TEST_STALL = %lld is not 0 or 1", (long long)value);
+      if (value < 0 || value > 5) return fail(MLA_ERR_INVALID_ARG, "MLA_OPT_TEST_STALL = %lld is not in 0..5", (long long)value);
       h->test_stall = (int)value;
       return MLA_OK;
   }

@@ -18,9 +18,14 @@
 //   - all calls on one device share the array, across handles and streams: two calls in
 //     flight at the same time overwrite each other's scratch.  Callers order them (one
 //     stream, or events between streams);
-//   - the first call on a device looks up the array's device address
-//     (cudaGetSymbolAddress), which may load the module on that device; make that first
-//     call before any stream capture begins.  Later calls only read a cached pointer.
+//   - the first call in a CUDA context looks up the array's device address
+//     (cudaGetSymbolAddress), which may load the module in that context; make that first
+//     call before any stream capture begins.  The address is cached together with the
+//     context it belongs to (a device reset, or another context made current, gives a new
+//     context and so a new lookup, which must also happen outside stream capture).  Later
+//     calls in the same context only read the cached pointer.
+#include <cuda.h>
+
 #include <mutex>
 #include <cstdio>
 
@@ -34,19 +39,47 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
 
+// One cached lookup per device: the context it was made in and the array's address there.
+struct ScratchEntry {
+  CUcontext ctx;
+  void* ptr;
+};
 std::mutex g_lookup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
-// Device address of the array on `device` (which the caller has made current).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry-point query (the library does not link
+// libcuda directly).
+cudaError_t current_context(CUcontext* ctx) {
+  static CtxGetCurrentFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return cudaErrorNotSupported;
+    fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  }
+  return fn(ctx) == CUDA_SUCCESS && *ctx ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of the array on `device` (which the caller has made current), looked up
+// again whenever the current context is not the one the cached address was taken in.
 cudaError_t scratch_on(int device, void** ptr) {
   std::lock_guard<std::mutex> lock(g_lookup_mutex);
-  if (!g_scratch_ptr[device]) {
+  CUcontext ctx = nullptr;
+  cudaError_t e = cudaFree(nullptr);      // make sure the runtime's context exists and is current
+  if (e != cudaSuccess) return e;
+  if ((e = current_context(&ctx)) != cudaSuccess) return e;
+  ScratchEntry& ent = g_scratch[device];
+  if (!ent.ptr || ent.ctx != ctx) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_fixed_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[device] = p;
+    if ((e = cudaGetSymbolAddress(&p, g_fixed_scratch)) != cudaSuccess) return e;
+    ent.ctx = ctx;
+    ent.ptr = p;
   }
-  *ptr = g_scratch_ptr[device];
+  *ptr = ent.ptr;
   return cudaSuccess;
 }
 

@@ -105,10 +105,13 @@ struct Bars {                               // mbarriers (8 bytes each) and flag
   uint64_t pdone[2];                        // P . C of a tile in P slot b done     (MMA commit)
   uint64_t ofinal;                          // single phase: the last P . C landed  (MMA commit)
   uint64_t qfull;                           // single phase: the absorbed query landed (producer, tx)
-  uint64_t recvfull[kSlots];                // peer's partial scores arrived        (1 + 16 KB tx)
+  uint64_t recvfull[kSlots][4];             // peer's partial scores of one lane quarter (32 heads) arrived
+                                            //   (1 arrival + 4 KB tx, armed by the receiving warp)
   uint64_t drain[2];                        // every MMA of the QK^T / P . C issuer done
   uint32_t tmem_base;
   int abort;
+  int peer_sent[8];                         // written by the peer: partial-score copies its group warp w sent here
+  int consumed[8];                          // copies group warp w of this CTA received and read
 };
 static_assert(sizeof(Bars) <= 1024, "barrier block");
 
@@ -191,7 +194,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                  const __grid_constant__ CUtensorMap tmap_o,
                  const int32_t* __restrict__ ctx_len, int n_h,
                  const int32_t* __restrict__ block_table, int bt_stride, int num_pages, float scale_log2,
-                 float out_scale, Workspace ws, unsigned* check) {
+                 float out_scale, int stall, Workspace ws, unsigned* check) {
   constexpr bool kFp8 = kMode != kModeBf16;            // e4m3 codes, converted in shared memory
   constexpr bool kBlock = kMode == kModeFp8Block;
   extern __shared__ uint8_t smem_raw[];
@@ -222,7 +225,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       mbar_init(smem_u32(&bars->pfull[i]), 4);
     }
     mbar_init(smem_u32(&bars->efin), 8);
-    for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&bars->recvfull[i]), 1);
+    for (int i = 0; i < kSlots; ++i)
+      for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bars->recvfull[i][q]), 1);
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->pdone[i]), 1);
     mbar_init(smem_u32(&bars->ofinal), 1);
     mbar_init(smem_u32(&bars->qfull), 1);
@@ -274,6 +278,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   // swizzle, staged in the still unused receive slots; RoPE half: straight into its 64-byte
   // swizzled operand slot; heads past n_h read as zeros), then the first tiles of the empty ring
   const int n_pre = min(n_tiles, kStages);
+  // a test of the bounded waits (stall == 2): CTA 0 of unit 0 never loads its tile 1
+  const int withheld = (stall == 2 && unit_idx == 0 && rank == 0 && n_tiles > 1) ? 1 : -1;
   if (warp == kWarpProducer && lane == 0) {
     const uint32_t qf = smem_u32(&bars->qfull);
     mbar_arrive_expect_tx(qf, (uint32_t)(4 * kMaxHeads * 128 + kQpeBytes));
@@ -282,7 +288,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     int pages[kStages];
 #pragma unroll
     for (int j = 0; j < kStages; ++j) pages[j] = j < n_pre ? bt_row[j] : 0;
-    for (int j = 0; j < n_pre; ++j) issue_tile(j, pages[j]);
+    for (int j = 0; j < n_pre; ++j)
+      if (j != withheld) issue_tile(j, pages[j]);
     for (int j = kStages; j < min(n_tiles, 2 * kStages); ++j) {    // the next user of each stage, into L2
       const int pg = bt_row[j];
       if (pg >= 0 && pg < num_pages) {
@@ -308,6 +315,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   if (warp < 8) {
     const int q4 = warp & 3, half = warp >> 2;
     const int h = q4 * 32 + lane;
+    // this warp's receive quarter of its group's tiles 0..3 (tile j lands in slot j % 4); later
+    // tiles are armed four tiles ahead, as each slot is consumed
+    if (lane == 0)
+      for (int jj = half; jj < min(n_tiles, kSlots); jj += 2)
+        mbar_arrive_expect_tx(smem_u32(&bars->recvfull[jj][q4]), 32 * 128);
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
     if (__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->qfull), 0, abort_flag))) {
 #pragma unroll
@@ -357,7 +369,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       // drain: every load issued has landed before the CTA may exit
       for (int j = max(0, issued - kStages); j < issued; ++j) {
         volatile int never = 0;
-        mbar_wait(smem_u32(&bars->full[j % kStages]), (j / kStages) & 1, &never);
+        if (j != withheld) mbar_wait(smem_u32(&bars->full[j % kStages]), (j / kStages) & 1, &never);
       }
     }
   } else if (warp == kWarpMma) {
@@ -511,7 +523,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const float2 sc2 = make_float2(scale_log2, scale_log2), zero2 = make_float2(0.0f, 0.0f);
     float m_g = -INFINITY, l_g = 0.0f;        // this group's sum, relative to 2^m_g
     bool ok = true;
-    int armed = 0;
+    int sent = 0, consumed = 0;               // this warp's partial-score copies sent / received (in tile order)
     // waits are made warp-uniform: tcgen05.ld / st below are .sync.aligned
     auto wait_cta = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, abort_flag));
@@ -522,9 +534,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     for (int j = g; j < n_tiles; j += 2) {
       const int k = j >> 1, slot = j & (kSlots - 1);
       const int valid = min(kPage, t_end - (unit.page_begin + j) * kPage);
-      // this group waited for slot j % 4's previous phase (tile j - 4) itself
-      if (lane == 0 && q4 == 0) mbar_arrive_expect_tx(smem_u32(&bars->recvfull[slot]), (uint32_t)kSlotBytes);
-      armed = j + 1;
       if (!wait_cta(&bars->sfull[g], k & 1)) { ok = false; break; }
       tc_fence_after();
       // x2[i] = scores 2i, 2i + 1 in the log2 domain, as pairs for the packed fp32 ops
@@ -545,13 +554,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       }
       {
         // fp16 copy for the peer, staged in this CTA's own receive slot (j + 2) % 4 and moved
-        // by one 4 KB bulk copy per warp into the peer's slot j % 4.  The staging rows last
-        // held tile j - 2 for this same warp, which has consumed them; the peer refills them
-        // with tile j + 2 only after its group g has finished tile j, which needed every copy
-        // of this tile, so after the copies have read them.  The peer's slot j % 4 needs no
-        // "free" handshake either: this CTA sends tile j after its group g finished tile
-        // j - 2, which needed the peer's tile j - 2 copies, sent after the peer's group g
-        // finished tile j - 4, the last user of the slot.
+        // by one 4 KB bulk copy per warp into the peer's slot j % 4, completing on the peer's
+        // barrier of that slot and lane quarter.  The staging rows last held tile j - 2 for
+        // this same warp, which has consumed them; the peer refills them with tile j + 2 only
+        // after its group g has finished tile j, which needed every copy of this tile, so
+        // after the copies have read them.  The peer's slot j % 4 needs no "free" handshake
+        // either: this CTA sends tile j after its group g finished tile j - 2, which needed
+        // the peer's tile j - 2 copies, sent after the peer's group g finished tile j - 4,
+        // the last user of the slot -- and re-armed the slot's quarter for tile j there, so
+        // every copy lands in an armed phase.
         uint8_t* stg = smem + kOffRecv + ((j + 2) & (kSlots - 1)) * kSlotBytes;
 #pragma unroll
         for (int qq = 0; qq < 8; ++qq)
@@ -560,15 +571,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                          f16x2_sat(x2[4 * qq + 2].x, x2[4 * qq + 2].y), f16x2_sat(x2[4 * qq + 3].x, x2[4 * qq + 3].y));
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          const uint32_t peer_bar = map_to_rank(smem_u32(&bars->recvfull[slot]), peer);
+        // (a test of the bounded waits, stall == 3: CTA 1 of unit 0 withholds warp 4's copy of tile 1)
+        const bool withhold = stall == 3 && unit_idx == 0 && rank == 1 && j == 1 && q4 == 0;
+        if (lane == 0 && !withhold) {
+          const uint32_t peer_bar = map_to_rank(smem_u32(&bars->recvfull[slot][q4]), peer);
           asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                        ::"r"(recv_peer + slot * kSlotBytes + q4 * 32 * 128), "r"(smem_u32(stg + q4 * 32 * 128)),
                        "r"(32 * 128), "r"(peer_bar) : "memory");
-          bulk_commit_group();
         }
+        ++sent;                               // (a withheld copy counts: its receiver then waits out its limit at exit)
       }
-      if (!wait_cluster(&bars->recvfull[slot], (j >> 2) & 1)) { ok = false; break; }
+      if (!wait_cluster(&bars->recvfull[slot][q4], (j >> 2) & 1)) { ok = false; break; }
+      ++consumed;
       {
         // x = x_own + x_peer
         const uint4* rp = reinterpret_cast<const uint4*>(smem + kOffRecv + slot * kSlotBytes + h * 128);
@@ -580,6 +594,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
           for (int kk = 0; kk < 4; ++kk) x2[4 * qq + kk] = __fadd2_rn(x2[4 * qq + kk], f16x2_to_f32(ww[kk]));
         }
       }
+      // the quarter is read: arm it for tile j + 4, which the peer sends only after this warp has
+      // sent tile j + 2, later in this loop
+      if (lane == 0 && j + kSlots < n_tiles)
+        mbar_arrive_expect_tx(smem_u32(&bars->recvfull[slot][q4]), 32 * 128);
       if (valid < kPage) {
         // a partial last page: rows past the context hold stale data; zero this CTA's latent
         // rows there so P = 0 meets finite values in P . C
@@ -661,8 +679,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->pfull[g]));
     }
-    if (lane == 0) bulk_wait_all();           // this warp's copies have landed before the CTA may exit
     if (!ok) fail_timeout(bars, check);
+    // tell the peer how many copies this warp sent into it (read after the first cluster barrier below)
+    if (lane == 0) {
+      const uint32_t dst = map_to_rank(smem_u32(&bars->peer_sent[warp]), peer);
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst), "r"(sent) : "memory");
+    }
     // ---- epilogue: reconcile the two groups' sums; group g writes latent columns
     // [128 g, 128 g + 128) of this CTA's half of every head
     // (ofinal is a single-phase barrier: a parity wait on pdone here could be two phases behind)
@@ -722,16 +744,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       if (live && unit.part >= 0 && rank == 0 && g == 0)
         ws.part_lse[(size_t)unit.part * n_h + h] = (m_fin + log2f(l_sum)) * 0.69314718055994531f;
     }
-    // a timed-out CTA still lets in-flight partial-score copies from the peer land
-    if (!ok && lane == 0 && q4 == 0 && armed > 0) {
-      volatile int never = 0;
-      mbar_wait<true>(smem_u32(&bars->recvfull[(armed - 1) & (kSlots - 1)]), ((armed - 1) >> 2) & 1, &never);
-    }
-    // and every copy this warp sent has landed in the peer before the cluster may exit (after a
-    // timeout the peer need not have waited for it)
-    if (lane == 0) bulk_wait_all();
+    bars->consumed[warp] = consumed;
   }
   tc_fence_before();
+  __syncthreads();
+  // Every copy either CTA will ever send has been issued and its count published.  A copy
+  // completes only on its receiver's barrier, so each receiving warp waits there for every copy
+  // the peer sent it but it did not consume (none in normal operation; after a timeout, the ones
+  // in flight) before the cluster may exit and its shared memory be reused.
+  cluster_sync();
+  if (warp < 8 && lane == 0) {
+    const int g = warp >> 2, q4 = warp & 3;
+    volatile int never = 0;
+    const int n_sent = bars->peer_sent[warp];
+    for (int c = bars->consumed[warp]; c < n_sent; ++c) {
+      const int j = g + 2 * c;
+      mbar_wait<true>(smem_u32(&bars->recvfull[j & (kSlots - 1)][q4]), (j >> 2) & 1, &never);
+    }
+  }
   __syncthreads();
   cluster_sync();
   if (warp == kWarpMma) tmem_dealloc(tmem, 512);
@@ -870,7 +900,8 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch,
   return launch_pdl(decode_tc_kernel<kMode>, dim3(2 * ws.max_units), dim3(kMode != kModeBf16 ? kThreadsFp8 : kThreads),
                     kSmemBytes, st, map, map_rope, map_scale, map_q, map_qpe, map_o,
                     ctx_len,
-                    h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, ws, h.check_word);
+                    h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, h.test_stall, ws,
+                    h.check_word);
 }
 }  // namespace
 

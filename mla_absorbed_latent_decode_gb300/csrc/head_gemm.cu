@@ -111,7 +111,7 @@ q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     griddep_wait();                        // the queries may come from the previous kernel
     griddep_launch_dependents();
     const uint32_t qf = smem_u32(&bars->full[0]);
-    if (!stall) {                          // (a test of the bounded waits withholds the copy)
+    if (stall != 1) {                      // (a test of the bounded waits, stall == 1, withholds the copy)
       mbar_arrive_expect_tx(qf, 2u * kBox);
       load_rows(a_st, &tm_q, 0, h, n0, qf);
       load_rows(a_st + kBox, &tm_q, 64, h, n0, qf);

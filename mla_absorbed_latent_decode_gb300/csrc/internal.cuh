@@ -82,7 +82,9 @@ cudaError_t prepare_weight_maps(Handle& h);
 // TMA descriptors of a cache in h.tmap / h.tmap_rope (64- and 32-column boxes of one page).
 cudaError_t cache_maps(const Handle& h, const void* cache, int num_pages);
 
-// Workspace sizing and carving (host).
+// Workspace sizing and carving (host).  The unit bound sizes the decode grid (two CTAs a unit).
+constexpr long long kMaxUnits = 1LL << 28;
+long long decode_unit_bound(const Handle& h, int batch, int max_ctx);
 size_t workspace_bytes(const Handle& h, int batch, int max_ctx, Workspace* carve, char* base);
 
 // The calling thread's message for mla_last_error (kept in api.cu).

@@ -103,7 +103,8 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
                  const __grid_constant__ CUtensorMap tm_wuv, const __nv_bfloat16* __restrict__ cache,
                  const int32_t* __restrict__ ctx_len, int n_h, int max_ctx, const int32_t* __restrict__ block_table,
                  int bt_stride, int num_pages, int lpad, int n_items, __nv_bfloat16* __restrict__ kn,
-                 __nv_bfloat16* __restrict__ vv, __nv_bfloat16* __restrict__ kr, int* sched, unsigned* check) {
+                 __nv_bfloat16* __restrict__ vv, __nv_bfloat16* __restrict__ kr, int* sched, int stall,
+                 unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -158,7 +159,10 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
           if (it.ok0) tma_load_2d(st, &tm_cache, 64 * kc, it.p0 * kPage, fb);
           if (it.ok1) tma_load_2d(st + kPageBox, &tm_cache, 64 * kc, it.p1 * kPage, fb);
           tma_load_2d(st + 2 * kPageBox, &tm_wuk, 64 * kc, kDn * it.h, fb);
-          tma_load_2d(st + 2 * kPageBox + kBox, &tm_wuv, 64 * kc, kDv * it.h, fb);
+          // (a test of the bounded waits, stall == 4: CTA 0 never loads the W_UV box of its first
+          // chunk, so that stage's barrier, armed for every byte, cannot complete)
+          if (!(stall == 4 && blockIdx.x == 0 && c == 0))
+            tma_load_2d(st + 2 * kPageBox + kBox, &tm_wuv, 64 * kc, kDv * it.h, fb);
         }
       }
       if (!ok && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
@@ -373,7 +377,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     const int32_t* __restrict__ ctx_len, int n_h, int max_ctx, const int32_t* __restrict__ block_table,
                     int bt_stride, int num_pages, const float2* __restrict__ rope_cs, int max_position,
                     float scale_log2, int lpad, int nqb, int n_items, int* sched, __nv_bfloat16* __restrict__ out,
-                    unsigned* check) {
+                    int stall, unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -467,7 +471,11 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           mbar_arrive_expect_tx(fb, 3 * kBox);
           tma_load_2d(st, &tm_kn, 0, kv_row0 + kTile * j, fb);
           tma_load_2d(st + kBox, &tm_kn, 64, kv_row0 + kTile * j, fb);
-          tma_load_2d(st + 2 * kBox, &tm_kr, 0, it.b * lpad + kTile * j, fb);
+          // (a test of the bounded waits, stall == 5: the CTA that takes the item of sequence 0, head
+          // 0, first query block never loads the RoPE-key box of its first key tile, so that tile's
+          // barrier, armed for every byte, cannot complete)
+          if (!(stall == 5 && it.b == 0 && it.h == 0 && it.r0 == 0 && j == 0))
+            tma_load_2d(st + 2 * kBox, &tm_kr, 0, it.b * lpad + kTile * j, fb);
         }
         if (!ok) break;
       }
@@ -847,7 +855,8 @@ cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_star
   e = launch_pdl(expand_tc_kernel, dim3(min(n_items, h.num_sms)), dim3(kExThreads), kExSmem, st,
                  *reinterpret_cast<const CUtensorMap*>(h.tmap), *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk),
                  *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv), static_cast<const __nv_bfloat16*>(cache), ctx_len,
-                 n_h, max_ctx, block_table, bt_stride, num_pages, lpad, n_items, kn, vv, kr, sched, h.check_word);
+                 n_h, max_ctx, block_table, bt_stride, num_pages, lpad, n_items, kn, vv, kr, sched, h.test_stall,
+                 h.check_word);
   if (e != cudaSuccess) return e;
   if (between && (e = cudaEventRecord(between, st)) != cudaSuccess) return e;   // profiling: splits the two kernels
   const float scale_log2 = h.scale * 1.4426950408889634f;
@@ -855,7 +864,7 @@ cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_star
   return launch_pdl(prefill_attn_kernel, dim3(min(n_att, h.num_sms)), dim3(kAtThreads), kAtSmem, st,
                     tm_q, tm_kn, tm_v, tm_kr, q_start, q_len, total_q, max_q, ctx_len, n_h, max_ctx, block_table,
                     bt_stride, num_pages, (const float2*)h.rope_cs, h.cfg.max_position, scale_log2, lpad, nqb, n_att,
-                    sched, static_cast<__nv_bfloat16*>(out), h.check_word);
+                    sched, static_cast<__nv_bfloat16*>(out), h.test_stall, h.check_word);
 }
 
 }  // namespace mla

@@ -148,7 +148,7 @@ def rescale_targets(n_rows, n_pairs, tile, visible, seed, plateau=16.0, jump=9.0
 def force_decode_rescale(wl, seed=3, jump=None):
     """Rewrite the latent part of every sequence's rows (of at least 3 pages) so that each head
     rescales at a tile of its own (:func:`rescale_targets` with 64-token tiles, the decode
-    kernel's tile).  An e4m3 cache moves scores by up to ~0.3 (log2 units), so its jump is 10
+    kernel's tile; n_h <= d_c / 4 keeps the rows of moderate size).  An e4m3 cache moves scores by up to ~0.3 (log2 units), so its jump is 10
     instead of 9.  Returns {sequence: g per head} for the sequences rewritten."""
     if jump is None:
         jump = 9.0 if wl.cache_dtype == W.CACHE_BF16 else 10.0
@@ -180,7 +180,7 @@ PREFILL_KEY_TILE = 128    # keys per tile of the prefill attention kernel
 def force_prefill_rescale(wl, seed=5):
     """Same for a prefill workload: every (query, head) pair of every sequence whose chunk sees at
     least three key tiles rescales at a key tile of its own (128-key tiles).  The chunk's
-    q_len * n_h pairs must not exceed d_c.  Returns {sequence: g per pair}."""
+    q_len * n_h pairs must not exceed d_c / 4.  Returns {sequence: g per pair}."""
     p = wl.extra["prefill"]
     q = mla_ref.bf16_to_f64(p["q"])
     w_uk = mla_ref.bf16_to_f64(wl.w_uk)
@@ -192,7 +192,8 @@ def force_prefill_rescale(wl, seed=5):
         pos0 = L - n
         if n == 0 or pos0 + 1 < 2 * PREFILL_KEY_TILE + 1:
             continue
-        assert n * wl.n_h <= wl.d_c, "too many (query, head) pairs to prescribe every score"
+        # few pairs against d_c unknowns keep the system well conditioned (rows of moderate size)
+        assert n * wl.n_h <= wl.d_c // 4, "too many (query, head) pairs to prescribe every score"
         qa = np.concatenate([mla_ref.absorb_query(q[a + i], w_uk, pos0 + i, wl.rope_base) for i in range(n)])
         visible = np.repeat(pos0 + 1 + np.arange(n), wl.n_h)
         rows = mla_ref.bf16_to_f64(wl.rows[starts[b]:starts[b + 1]])

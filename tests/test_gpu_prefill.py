@@ -136,7 +136,7 @@ def test_prefill_argument_errors():
     s.close()
 
 
-@pytest.mark.parametrize("n_h,ctx,ql", [(16, [700, 1100, 64], [8, 4, 64]), (5, [900, 300], [100, 40])])
+@pytest.mark.parametrize("n_h,ctx,ql", [(16, [700, 1100, 64], [8, 4, 64]), (5, [900, 300], [25, 12])])
 def test_prefill_forced_rescale_matches_the_oracle(n_h, ctx, ql):
     """Every (query, head) pair of the long chunks has a score plateau and then, in a key tile
     j >= 1 of its own, a key more than the rescale step above it, so the prefill's running row

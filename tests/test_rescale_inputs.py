@@ -31,13 +31,16 @@ def test_decode_inputs_force_a_rescale_per_head(n_h, dtype):
             assert x[h].max() == at                       # the jump is the row's maximum
             parities.add(int(g[h]) % 2)
     assert parities == {0, 1}
+    assert np.max(np.abs(vals)) < 128.0                   # rows stay of moderate size (a well-posed problem)
 
 
-def test_prefill_inputs_force_a_rescale_per_pair():
-    wl = W.make_prefill("rescale_pf", 93, 16, [700, 1100, 64], [8, 4, 64])
+@pytest.mark.parametrize("n_h,ctx,ql", [(16, [700, 1100, 64], [8, 4, 64]), (5, [900, 300], [25, 12])])
+def test_prefill_inputs_force_a_rescale_per_pair(n_h, ctx, ql):
+    wl = W.make_prefill("rescale_pf", 95 + n_h, n_h, ctx, ql)
     forced = force_prefill_rescale(wl)
     assert sorted(forced) == [0, 1]
     vals = oracle_values(wl, oracle_stored(wl))
+    assert np.max(np.abs(vals)) < 128.0
     p = wl.extra["prefill"]
     starts = np.concatenate([[0], np.cumsum(wl.ctx_len.astype(np.int64))])
     scale = mla_ref.default_scale(wl.d_nope, wl.d_rope) * LOG2E

@@ -10,7 +10,8 @@ import torch
 from mla_absorbed_latent_decode_gb300 import binding as B
 from mla_absorbed_latent_decode_gb300 import workloads as W
 from mla_absorbed_latent_decode_gb300.runner import DecodeSession, bf16_tensor
-from tests.mla_cases import BF16_TOL, FP8_TOL, bf16_out_to_f64, compare
+from tests.mla_cases import (BF16_TOL, FP8_TOL, bf16_out_to_f64, compare, oracle_decode_paged, oracle_stored,
+                             oracle_values)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,4 +62,49 @@ def test_fixed_scratch_rejects_a_batch_beyond_its_size():
     assert "MLA_ERR_WORKSPACE" in str(ei.value) and "fixed" in str(ei.value)
     torch.cuda.synchronize()
     assert not torch.any(out.view(torch.int16) != 0)      # nothing was enqueued
+    s.close()
+
+
+def test_fixed_scratch_matches_the_oracle():
+    """The scratch-array path against the fp64 oracle itself (not only against mla_decode)."""
+    wl = W.make_decode("fixed_oracle", 301, 128, RAGGED + [4096])
+    s = DecodeSession(wl)
+    s.append_rows()
+    out = torch.full_like(s.out, float("nan"))
+    for _ in range(2):
+        s.mla.decode_fixed_scratch(s.q, s.ctx_len, wl.max_ctx, s.block_table, s.cache, wl.num_pages, out, s.stream)
+        assert s.status() == 0
+        got = bf16_out_to_f64(out)
+        ref = oracle_decode_paged(wl, oracle_values(wl, oracle_stored(wl)))
+        rel, err, scale = compare(got, ref, BF16_TOL)
+        assert rel <= BF16_TOL, (rel, err, scale)
+    s.close()
+
+
+def test_fixed_scratch_limit_is_the_workspace_size():
+    """The largest batch the array takes is the one whose mla_decode_workspace_size fits in it: at
+    128 heads and max_ctx 4096 that batch is accepted and one more sequence is rejected (short
+    contexts, so only the sizing differs from a full step)."""
+    max_ctx = 4096
+    wl = W.make_decode("fixed_edge", 302, 128, [10] * 40)
+    s = DecodeSession(wl, max_position=max_ctx)
+    sizes = {b: s.mla.decode_workspace_size(b, max_ctx) for b in range(1, 41)}
+    fit = max(b for b, n in sizes.items() if n <= B.MLA_FIXED_SCRATCH_BYTES)
+    assert fit < 40 and sizes[fit + 1] > B.MLA_FIXED_SCRATCH_BYTES
+    bt = torch.full((wl.B, (max_ctx + 63) // 64), -1, dtype=torch.int32, device=s.device)
+    bt[:, :1] = s.block_table[:, :1]
+    s.append_rows()
+    for batch, ok in ((fit, True), (fit + 1, False)):
+        out = torch.zeros((batch, wl.n_h, wl.d_v), dtype=torch.bfloat16, device=s.device)
+        args = (s.q[:batch], s.ctx_len[:batch], max_ctx, bt[:batch], s.cache, wl.num_pages, out, s.stream)
+        if ok:
+            s.mla.decode_fixed_scratch(*args)
+            assert s.status() == 0
+            ref = bf16_out_to_f64(s.decode()[:batch].clone())
+            got = bf16_out_to_f64(out)
+            assert compare(got, ref, BF16_TOL)[0] <= BF16_TOL
+        else:
+            with pytest.raises(B.MlaError) as ei:
+                s.mla.decode_fixed_scratch(*args)
+            assert ei.value.status == B.MLA_ERR_WORKSPACE
     s.close()
