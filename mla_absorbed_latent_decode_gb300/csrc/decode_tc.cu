@@ -194,7 +194,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                  const __grid_constant__ CUtensorMap tmap_o,
                  const int32_t* __restrict__ ctx_len, int n_h,
                  const int32_t* __restrict__ block_table, int bt_stride, int num_pages, float scale_log2,
-                 float out_scale, int stall, Workspace ws, unsigned* check) {
+                 float out_scale, int stall, const uint8_t* __restrict__ w_next, size_t w_next_bytes, Workspace ws,
+                 unsigned* check) {
   constexpr bool kFp8 = kMode != kModeBf16;            // e4m3 codes, converted in shared memory
   constexpr bool kBlock = kMode == kModeFp8Block;
   extern __shared__ uint8_t smem_raw[];
@@ -245,8 +246,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   __syncthreads();
   griddep_wait();                           // plan, absorbed queries and cache rows are inputs
   griddep_launch_dependents();
-  if (unit_idx >= ws.counters[0]) return;   // both CTAs of the cluster leave together
+  // (the unit record is read together with the unit count: the grid never exceeds the workspace's units)
+  const int n_units = ws.counters[0];
   const Unit unit = ws.units[unit_idx];
+  if (unit_idx >= n_units) return;         // both CTAs of the cluster leave together
   const int b = unit.b;
   const int n_tiles = unit.page_end - unit.page_begin;
 
@@ -265,6 +268,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     constexpr uint32_t kTx = kBlock ? 2 * kChunkBytes + kRopeBytes + kScaleBytes
                                     : (kFp8 ? 2 * kChunkBytes + kRopeBytes / 2 : 4 * kChunkBytes + kRopeBytes);
     mbar_arrive_expect_tx(full, kTx);
+    // (an evict-first L2 policy on these once-read rows was measured 4 us slower per step)
     for (int c = 0; c < 4; ++c)            // FP8: each code box into the upper half of its chunk slot
       tma_load_2d(stage0 + s * kStageBytes + c * kChunkBytes + (kFp8 ? kChunkBytes / 2 : 0), &tmap,
                   (int)(rank * 256 + c * 64), page * kPage, full);
@@ -281,23 +285,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   // a test of the bounded waits (stall == 2): CTA 0 of unit 0 never loads its tile 1
   const int withheld = (stall == 2 && unit_idx == 0 && rank == 0 && n_tiles > 1) ? 1 : -1;
   if (warp == kWarpProducer && lane == 0) {
+    // tile 0 first, then the query, then the rest of the ring: every CTA of the grid requests its
+    // ring at once, and the first QK^T needs only tile 0 and the query
+    int pages[kStages];
+#pragma unroll
+    for (int j = 0; j < kStages; ++j) pages[j] = j < n_pre ? bt_row[j] : 0;
+    if (withheld != 0) issue_tile(0, pages[0]);
     const uint32_t qf = smem_u32(&bars->qfull);
     mbar_arrive_expect_tx(qf, (uint32_t)(4 * kMaxHeads * 128 + kQpeBytes));
     for (int c = 0; c < 4; ++c) tma_load_3d(sbase + kOffRecv + c * kMaxHeads * 128, &tmap_q, (int)(rank * 256 + c * 64), 0, b, qf);
     tma_load_3d(sbase + kOffQpe, &tmap_qpe, (int)(kDc + rank * 32), 0, b, qf);
-    int pages[kStages];
-#pragma unroll
-    for (int j = 0; j < kStages; ++j) pages[j] = j < n_pre ? bt_row[j] : 0;
-    for (int j = 0; j < n_pre; ++j)
+    for (int j = 1; j < n_pre; ++j)
       if (j != withheld) issue_tile(j, pages[j]);
-    for (int j = kStages; j < min(n_tiles, 2 * kStages); ++j) {    // the next user of each stage, into L2
-      const int pg = bt_row[j];
-      if (pg >= 0 && pg < num_pages) {
-        for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tmap, (int)(rank * 256 + c * 64), pg * kPage);
-        tma_prefetch_2d(&tmap_rope, (int)((kBlock ? 0 : kDc) + rank * 32), pg * kPage);
-        if (kBlock) tma_prefetch_2d(&tmap_scale, kDc, pg * kPage);
-      }
-    }
   }
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
@@ -347,6 +346,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      // the next user of each stage into L2, once tile 0 has landed (out of the start-up burst)
+      if (n_tiles > kStages && mbar_wait(smem_u32(&bars->full[0]), 0, abort_flag)) {
+        for (int j = kStages; j < min(n_tiles, 2 * kStages); ++j) {
+          const int pg = bt_row[j];
+          if (pg >= 0 && pg < num_pages) {
+            for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tmap, (int)(rank * 256 + c * 64), pg * kPage);
+            tma_prefetch_2d(&tmap_rope, (int)((kBlock ? 0 : kDc) + rank * 32), pg * kPage);
+            if (kBlock) tma_prefetch_2d(&tmap_scale, kDc, pg * kPage);
+          }
+        }
+      }
       int issued = n_pre;
       for (int j = n_pre; j < n_tiles; ++j) {
         const int s = j % kStages;
@@ -365,6 +375,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         }
         issue_tile(j, page);
         issued = j + 1;
+      }
+      // the value up-projection's weights (the next kernel) into L2 while the last tiles are
+      // consumed: this CTA's share of them, 16 KB per request
+      if (w_next) {
+        const size_t n_cta = 2 * (size_t)__ldcg(&ws.counters[0]), me = 2 * (size_t)unit_idx + rank;
+        const size_t lo = (w_next_bytes * me / n_cta) & ~(size_t)15, hi = (w_next_bytes * (me + 1) / n_cta) & ~(size_t)15;
+        for (size_t off = lo; off < hi; off += 16384)
+          bulk_prefetch_l2(w_next + off, (uint32_t)min((size_t)16384, hi - off));
       }
       // drain: every load issued has landed before the CTA may exit
       for (int j = max(0, issued - kStages); j < issued; ++j) {
@@ -738,7 +756,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
           for (int bx = 0; bx < 2; ++bx)
             tma_store_3d(&tmap_o, smem_u32(ob + bx * 4096), (int)(rank * 256 + 128 * g + 64 * bx), 32 * q4, b);
           bulk_commit_group();
-          bulk_wait_all();                    // written (and the staging read) before the CTA may exit
+          bulk_wait_read();                   // the staging read before the CTA may exit (the writes
+                                              // complete with the grid)
         }
       }
       if (live && unit.part >= 0 && rank == 0 && g == 0)
@@ -900,7 +919,8 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch,
   return launch_pdl(decode_tc_kernel<kMode>, dim3(2 * ws.max_units), dim3(kMode != kModeBf16 ? kThreadsFp8 : kThreads),
                     kSmemBytes, st, map, map_rope, map_scale, map_q, map_qpe, map_o,
                     ctx_len,
-                    h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, h.test_stall, ws,
+                    h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, h.test_stall,
+                    reinterpret_cast<const uint8_t*>(h.w_uv), sizeof(__nv_bfloat16) * (size_t)h.cfg.n_h * kDv * kDc, ws,
                     h.check_word);
 }
 }  // namespace

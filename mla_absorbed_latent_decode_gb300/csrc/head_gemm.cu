@@ -38,7 +38,9 @@ constexpr int kBox = 128 * 128;                        // one 64-column x 128-ro
 // query absorption: one CTA per (head, tile of 128 sequences); sequences are the M rows
 constexpr int kQaM = 128;
 constexpr int kQaSmem = 8 * kBox + 2 * kBox + 1024 + 1024;
-// value up-projection: one CTA per (head, tile of up to 64 sequences); the 128 value rows are M
+// value up-projection: one CTA per (head, tile of up to 64 sequences); the 128 value rows are M.
+// The tile (the MMA's N) is 64, 32 or 16 sequences, chosen at launch so that small batches
+// still spread over many SMs.
 constexpr int kUpN = 64;
 constexpr int kUpSmem = 8 * kBox + 8 * kUpN * 128 + 1024 + 1024;
 
@@ -211,15 +213,17 @@ q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 512);
-  if (tid == 0) bulk_wait_all();
+  if (tid == 0) bulk_wait_read();          // the staging read before the CTA exits (the writes complete with the grid)
 }
 
 // out^T[h] = W_UV[h] . o_lat[:, h]^T for the sequences n0 .. n0 + n_pad of this CTA, after
 // merging split sequences' partials of head h into o_lat by log-sum-exp (zero latent for an
-// invalid sequence or one with a bad page id; unsplit sequences already hold theirs).
-__global__ void __launch_bounds__(kThreads, 1)
+// invalid sequence or one with a bad page id; unsplit sequences already hold theirs).  Eight
+// warps take the merge; warps 0-3 (one per 32 TMEM lanes) run the epilogue.
+constexpr int kUpThreads = 256;
+__global__ void __launch_bounds__(kUpThreads, 1)
 up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_o, int B, int n_h,
-                  int n_pad, Workspace ws, __nv_bfloat16* __restrict__ out, unsigned* check) {
+                  int n_pad, int n_tile, Workspace ws, __nv_bfloat16* __restrict__ out, unsigned* check) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int2 plan_s[kUpN];
   const uint32_t raw = smem_u32(smem_raw);
@@ -228,8 +232,8 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
   GemmBars* bars = reinterpret_cast<GemmBars*>(smem + 8 * kBox + 8 * kUpN * 128);
   volatile int* abort_flag = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x, n0 = blockIdx.z * kUpN;
-  const int n_here = min(n_pad, kUpN);                 // the TMA box height (rows past B arrive as zeros)
+  const int h = blockIdx.x, n0 = blockIdx.z * n_tile;
+  const int n_here = min(n_pad, n_tile);               // the TMA box height (rows past B arrive as zeros)
   const uint32_t b_bytes = (uint32_t)n_here * 128;
   if (tid == 0) {
     for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars->full[i]), 1);
@@ -251,16 +255,22 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
   griddep_wait();                          // the plan and latent sums come from earlier kernels
   griddep_launch_dependents();
   // merge pass: one warp per split, invalid or bad-page sequence of this tile.  The plan
-  // entries of the tile are loaded together first (one per thread); a split sequence's
-  // partial slots are its unit indices first_unit .. first_unit + nsplit - 1.
-  const int n_seq = min(B - n0, kUpN);
-  if (tid < n_seq) {
-    const SeqPlan sp = ws.seqs[n0 + tid];
-    plan_s[tid] = make_int2(sp.first_unit, ws.bad[n0 + tid] ? 0 : sp.nsplit);
-  }
+  // entries of the tile are loaded together first (one per thread), before the dependency wait:
+  // the plan comes from the query-absorption launch, two launches back and complete when this
+  // grid starts; the bad-page flags, written by the decode, after it.  A split sequence's
+  // partial slots are its unit indices first_unit .. first_unit + nsplit - 1.  Lane k holds
+  // split k's weight (32 splits at a time, one load each, all in flight together); the
+  // partials are then requested four splits at a time before any is used, so a merge costs a
+  // few L2 round trips instead of one per split.
+  const int n_seq = min(B - n0, n_tile);
+  int2 sp = make_int2(0, 0);
+  if (tid < n_seq) sp = __ldcg(reinterpret_cast<const int2*>(ws.seqs) + n0 + tid);
+  griddep_wait();                          // the latent sums and bad-page flags of the decode
+  griddep_launch_dependents();
+  if (tid < n_seq) plan_s[tid] = make_int2(sp.x, ws.bad[n0 + tid] ? 0 : sp.y);
   __syncthreads();
   bool wrote = false;
-  for (int j = warp; j < n_seq; j += kThreads / 32) {
+  for (int j = warp; j < n_seq; j += kUpThreads / 32) {
     const int b = n0 + j;
     const int first = plan_s[j].x, nsplit = plan_s[j].y;
     if (nsplit == 1) continue;
@@ -271,23 +281,39 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
       dst[1] = make_uint4(0, 0, 0, 0);
       continue;
     }
+    const float* lse = ws.part_lse + (size_t)first * n_h + h;
     float m = -INFINITY;
-    for (int k = 0; k < nsplit; ++k) m = fmaxf(m, ws.part_lse[(size_t)(first + k) * n_h + h]);
+    for (int k0 = 0; k0 < nsplit; k0 += 32)
+      if (k0 + lane < nsplit) m = fmaxf(m, __ldcg(lse + (size_t)(k0 + lane) * n_h));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float acc[16], den = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-    for (int k = 0; k < nsplit; ++k) {
-      const int part = first + k;
-      const float w = expf(ws.part_lse[(size_t)part * n_h + h] - m);
-      den += w;
-      const float4* src = reinterpret_cast<const float4*>(ws.part_o + ((size_t)part * n_h + h) * kDc) + 4 * lane;
+    const float4* src0 = reinterpret_cast<const float4*>(ws.part_o + ((size_t)first * n_h + h) * kDc) + 4 * lane;
+    const size_t slot4 = (size_t)n_h * kDc / 4;                 // one partial slot, in float4
+    for (int k0 = 0; k0 < nsplit; k0 += 32) {
+      const float w_lane = k0 + lane < nsplit ? expf(__ldcg(lse + (size_t)(k0 + lane) * n_h) - m) : 0.0f;
+      const int kn = min(32, nsplit - k0);
+      for (int k1 = 0; k1 < kn; k1 += 4) {
+        float4 v[4][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 v = src[i];
-        acc[4 * i] = fmaf(w, v.x, acc[4 * i]);
-        acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
-        acc[4 * i + 2] = fmaf(w, v.z, acc[4 * i + 2]);
-        acc[4 * i + 3] = fmaf(w, v.w, acc[4 * i + 3]);
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            v[u][i] = k1 + u < kn ? __ldcg(src0 + (size_t)(k0 + k1 + u) * slot4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float w = __shfl_sync(0xffffffffu, w_lane, (k1 + u) & 31);
+          den += k1 + u < kn ? w : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[4 * i] = fmaf(w, v[u][i].x, acc[4 * i]);
+            acc[4 * i + 1] = fmaf(w, v[u][i].y, acc[4 * i + 1]);
+            acc[4 * i + 2] = fmaf(w, v[u][i].z, acc[4 * i + 2]);
+            acc[4 * i + 3] = fmaf(w, v[u][i].w, acc[4 * i + 3]);
+          }
+        }
       }
     }
     const float inv = 1.0f / den;
@@ -332,10 +358,10 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
   // epilogue: thread = value row v (TMEM lane) holding up to 64 sequences; transposed through
   // shared memory (the weight region is free now) into [sequence][128 v] bf16 rows, then
   // written with 16-byte stores, one 256-byte row per sequence
-  const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   __nv_bfloat16* tile = reinterpret_cast<__nv_bfloat16*>(smem);     // [64][128]
   const int v = 32 * warp + lane;
-  if (ok) {
+  if (ok && warp < 4) {
     for (int c0 = 0; c0 < n_here; c0 += 32) {
       uint32_t r[32];
       tmem_ld32(lane_addr + c0, r);
@@ -346,7 +372,7 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
   }
   __syncthreads();
   if (ok) {
-    for (int i = tid; i < n_seq * (kDv / 8); i += kThreads) {
+    for (int i = tid; i < n_seq * (kDv / 8); i += kUpThreads) {
       const int j = i / (kDv / 8), c = i % (kDv / 8);
       reinterpret_cast<uint4*>(out + ((size_t)(n0 + j) * n_h + h) * kDv)[c] =
           reinterpret_cast<const uint4*>(tile + j * kDv)[c];
@@ -436,12 +462,15 @@ cudaError_t launch_combine_uv(const Handle& h, int batch, const Workspace& ws, _
     attr = true;
   }
   const int n_pad = ((batch + 15) / 16) * 16;
+  // the largest tile of 64 / 32 / 16 sequences that still gives half the SMs a CTA (else 16)
+  int n_tile = kUpN;
+  while (n_tile > 16 && (long long)h.cfg.n_h * ((batch + n_tile - 1) / n_tile) < h.num_sms / 2) n_tile /= 2;
   alignas(64) CUtensorMap to;
-  cudaError_t e = rows_map(ws.o_lat, batch, h.cfg.n_h, kDc, min(n_pad, kUpN), &to);
+  cudaError_t e = rows_map(ws.o_lat, batch, h.cfg.n_h, kDc, min(n_pad, n_tile), &to);
   if (e != cudaSuccess) return e;
-  dim3 grid(h.cfg.n_h, 1, (batch + kUpN - 1) / kUpN);
-  return launch_pdl(up_project_kernel, grid, dim3(kThreads), kUpSmem, st,
-                    *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv), to, batch, h.cfg.n_h, n_pad, ws, out,
+  dim3 grid(h.cfg.n_h, 1, (batch + n_tile - 1) / n_tile);
+  return launch_pdl(up_project_kernel, grid, dim3(kUpThreads), kUpSmem, st,
+                    *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv), to, batch, h.cfg.n_h, n_pad, n_tile, ws, out,
                     h.check_word);
 }
 

@@ -37,6 +37,7 @@ struct SeqPlan {
   int32_t first_unit;  // first unit of the sequence (units of a sequence are consecutive)
   int32_t nsplit;      // 0: invalid sequence (output zeroed), 1: unsplit, >1: split
 };
+static_assert(sizeof(SeqPlan) == 8, "plan entries are read as int2");
 
 // Device-side views of the workspace (all regions 256-byte aligned).
 struct Workspace {
