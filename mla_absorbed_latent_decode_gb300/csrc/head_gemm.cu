@@ -252,8 +252,6 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
       tma_load_2d(a_st + i * kBox, &tm_w, 64 * i, 128 * h, smem_u32(&bars->full[i]));
     }
   }
-  griddep_wait();                          // the plan and latent sums come from earlier kernels
-  griddep_launch_dependents();
   // merge pass: one warp per split, invalid or bad-page sequence of this tile.  The plan
   // entries of the tile are loaded together first (one per thread), before the dependency wait:
   // the plan comes from the query-absorption launch, two launches back and complete when this
