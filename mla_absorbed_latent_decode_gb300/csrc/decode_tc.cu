@@ -377,8 +377,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         issued = j + 1;
       }
       // the value up-projection's weights (the next kernel) into L2 while the last tiles are
-      // consumed: this CTA's share of them, 16 KB per request
-      if (w_next) {
+      // consumed: this CTA's share of them, 16 KB per request.  (bf16 cache only: with an FP8
+      // cache the extra code in this register-bound variant measured 14 us slower per step)
+      if (kMode == kModeBf16 && w_next) {
         const size_t n_cta = 2 * (size_t)__ldcg(&ws.counters[0]), me = 2 * (size_t)unit_idx + rank;
         const size_t lo = (w_next_bytes * me / n_cta) & ~(size_t)15, hi = (w_next_bytes * (me + 1) / n_cta) & ~(size_t)15;
         for (size_t off = lo; off < hi; off += 16384)
