@@ -255,20 +255,25 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
   // merge pass: one warp per split, invalid or bad-page sequence of this tile.  The plan
   // entries of the tile are loaded together first (one per thread), before the dependency wait:
   // the plan comes from the query-absorption launch, two launches back and complete when this
-  // grid starts; the bad-page flags, written by the decode, after it.  A split sequence's
-  // partial slots are its unit indices first_unit .. first_unit + nsplit - 1.  Lane k holds
-  // split k's weight (32 splits at a time, one load each, all in flight together); the
-  // partials are then requested four splits at a time before any is used, so a merge costs a
-  // few L2 round trips instead of one per split.
+  // grid starts; the bad-page flags, written by the decode, after it.  A tile without a split or
+  // invalid sequence loads its latent rows at once (a bad-page sequence's rows are then zeroed in
+  // shared memory).  A split sequence's partial slots are its unit indices first_unit ..
+  // first_unit + nsplit - 1; lane k holds split k's log-sum-exp (32 splits per load, one load
+  // each), and the partials are requested eight splits at a time, the first batch together with
+  // the log-sum-exps, merged with a running maximum: one or two L2 round trips per merge.
   const int n_seq = min(B - n0, n_tile);
   int2 sp = make_int2(0, 0);
   if (tid < n_seq) sp = __ldcg(reinterpret_cast<const int2*>(ws.seqs) + n0 + tid);
   griddep_wait();                          // the latent sums and bad-page flags of the decode
   griddep_launch_dependents();
-  if (tid < n_seq) plan_s[tid] = make_int2(sp.x, ws.bad[n0 + tid] ? 0 : sp.y);
-  __syncthreads();
+  const bool early = __syncthreads_and(tid >= n_seq || sp.y == 1) != 0;
+  if (early && tid == 0)
+    for (int i = 0; i < 8; ++i) load_rows(b_st + i * b_bytes, &tm_o, 64 * i, h, n0, smem_u32(&bars->full[i]));
+  const int bad = tid < n_seq ? ws.bad[n0 + tid] : 0;
+  if (tid < n_seq) plan_s[tid] = make_int2(sp.x, bad ? 0 : sp.y);
+  const bool any_bad = __syncthreads_or(bad) != 0;
   bool wrote = false;
-  for (int j = warp; j < n_seq; j += kUpThreads / 32) {
+  for (int j = warp; j < n_seq && !early; j += kUpThreads / 32) {
     const int b = n0 + j;
     const int first = plan_s[j].x, nsplit = plan_s[j].y;
     if (nsplit == 1) continue;
@@ -280,30 +285,38 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
       continue;
     }
     const float* lse = ws.part_lse + (size_t)first * n_h + h;
-    float m = -INFINITY;
-    for (int k0 = 0; k0 < nsplit; k0 += 32)
-      if (k0 + lane < nsplit) m = fmaxf(m, __ldcg(lse + (size_t)(k0 + lane) * n_h));
-#pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float acc[16], den = 0.0f;
+    float acc[16], den = 0.0f, m = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
     const float4* src0 = reinterpret_cast<const float4*>(ws.part_o + ((size_t)first * n_h + h) * kDc) + 4 * lane;
     const size_t slot4 = (size_t)n_h * kDc / 4;                 // one partial slot, in float4
     for (int k0 = 0; k0 < nsplit; k0 += 32) {
-      const float w_lane = k0 + lane < nsplit ? expf(__ldcg(lse + (size_t)(k0 + lane) * n_h) - m) : 0.0f;
       const int kn = min(32, nsplit - k0);
-      for (int k1 = 0; k1 < kn; k1 += 4) {
-        float4 v[4][4];
+      const float l_lane = lane < kn ? __ldcg(lse + (size_t)(k0 + lane) * n_h) : -INFINITY;
+      for (int k1 = 0; k1 < kn; k1 += 8) {
+        float4 v[8][4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 8; ++u)
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             v[u][i] = k1 + u < kn ? __ldcg(src0 + (size_t)(k0 + k1 + u) * slot4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        float lb[8], mb = m;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float w = __shfl_sync(0xffffffffu, w_lane, (k1 + u) & 31);
-          den += k1 + u < kn ? w : 0.0f;
+        for (int u = 0; u < 8; ++u) {
+          lb[u] = __shfl_sync(0xffffffffu, l_lane, (k1 + u) & 31);
+          if (k1 + u < kn) mb = fmaxf(mb, lb[u]);
+        }
+        if (mb > m) {                        // the running maximum grows: rescale what is summed
+          const float sc = expf(m - mb);       // 0 on the first batch (m = -inf)
+          den *= sc;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[i] *= sc;
+          m = mb;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float w = k1 + u < kn ? expf(lb[u] - m) : 0.0f;
+          den += w;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             acc[4 * i] = fmaf(w, v[u][i].x, acc[4 * i]);
@@ -321,13 +334,25 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
+  if (early && any_bad) {
+    // rows of bad-page sequences, loaded before the flags were read, become zeros in the tile
+    bool landed = true;
+    for (int i = 0; i < 8; ++i) landed = mbar_wait(smem_u32(&bars->full[i]), 0, abort_flag) && landed;
+    if (!landed && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+    for (int x = tid; x < n_seq * 8 * 8; x += kUpThreads) {   // (sequence, box, 16-byte piece)
+      const int j = x >> 6, i = (x >> 3) & 7, q = x & 7;
+      if (plan_s[j].y == 0) *reinterpret_cast<uint4*>(smem + 8 * kBox + i * b_bytes + j * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
   if (wrote) fence_proxy_async_global();       // these rows are read below by TMA (async proxy)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) load_rows(b_st + i * b_bytes, &tm_o, 64 * i, h, n0, smem_u32(&bars->full[i]));
+    if (!early)
+      for (int i = 0; i < 8; ++i) load_rows(b_st + i * b_bytes, &tm_o, 64 * i, h, n0, smem_u32(&bars->full[i]));
     const uint32_t idesc = idesc_bf16_f32(128, n_here, false, false);
     const uint64_t a0 = sdesc_sw128(a_st, 16, 1024), b0 = sdesc_sw128(b_st, 16, 1024);
     bool ok = true;

@@ -149,6 +149,27 @@ def test_bad_lengths_and_pages_zero_only_their_sequence():
     s.close()
 
 
+def test_bad_page_in_a_tile_without_splits_zeroes_only_its_sequence():
+    """With one unit per sequence the up-projection loads the latent rows before it reads the
+    bad-page flags; a bad sequence's rows must still come out as zeros."""
+    wl = W.make_decode("badpage1", 77, 16, [100, 200, 300, 64])
+    s = DecodeSession(wl, splits=1)
+    s.append_rows()
+    good = bf16_out_to_f64(s.decode())
+    assert s.status() == 0
+    ref = oracle_decode_paged(wl, oracle_values(wl, oracle_stored(wl)))
+    rel, err, scale = compare(good, ref, BF16_TOL)
+    assert rel <= BF16_TOL, (rel, err, scale)
+    bt = s.block_table.clone()
+    bt[1, 2] = wl.num_pages + 5
+    s.mla.decode(s.q, s.ctx_len, wl.max_ctx, bt, s.cache, wl.num_pages, s.workspace, s.out)
+    out = bf16_out_to_f64(s.out)
+    assert s.status() == B.MLA_CHECK_PAGE_ID
+    assert np.all(out[1] == 0)
+    assert np.array_equal(out[0], good[0]) and np.array_equal(out[2:], good[2:])
+    s.close()
+
+
 def test_decode_host_argument_errors():
     wl = W.make_decode("args", 81, 16, [10, 20])
     s = DecodeSession(wl)
