@@ -557,6 +557,10 @@ mla_status_t mla_set_option(mla_handle_t hh, int32_t option, int64_t value) {
       if (value < 0 || value > 5) return fail(MLA_ERR_INVALID_ARG, "MLA_OPT_TEST_STALL = %lld is not in 0..5", (long long)value);
       h->test_stall = (int)value;
       return MLA_OK;
+    case MLA_OPT_FP8_MMA:
+      if (value < 0 || value > 1) return fail(MLA_ERR_INVALID_ARG, "MLA_OPT_FP8_MMA = %lld is not 0 or 1", (long long)value);
+      h->fp8_mma = (int)value;
+      return MLA_OK;
   }
   return fail(MLA_ERR_INVALID_ARG, "mla_set_option: unknown option %d", option);
 }

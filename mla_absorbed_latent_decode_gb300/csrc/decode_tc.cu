@@ -63,25 +63,47 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 4;                 // cache tiles in flight per CTA
+constexpr int kStagesMax = 4;              // cache tiles in flight per CTA (3 with FP8 MMAs)
 constexpr int kChunkBytes = kPage * 128;   // one 64-token x 64-column bf16 box (SW128): 8 KB
 constexpr int kRopeBytes = kPage * 64;     // one 64-token x 32-column bf16 box of the RoPE key (SW64): 4 KB
 constexpr int kScaleBytes = kPage * 16;   // per-block FP8 cache: the 4 fp32 block scales of 64 tokens: 1 KB
-constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes + kScaleBytes;
 constexpr int kQpeBytes = kMaxHeads * 64;              // 128 heads x 32 bf16 of the RoPE query, SW64 K-major
 constexpr int kSlots = 4;                              // partial-score receive slots
 constexpr int kSlotBytes = kMaxHeads * kPage * 2;      // 128 x 64 fp16 = 16 KB
-constexpr int kOffStages = 0;
-constexpr int kOffQpe = kOffStages + kStages * kStageBytes;
-constexpr int kOffRecv = kOffQpe + kQpeBytes;
-constexpr int kOffBars = kOffRecv + kSlots * kSlotBytes;
-constexpr int kOffXchg = kOffBars + 1024;             // running maxima / final sums of the two tile groups
-constexpr int kXchgBytes = 3 * 2 * kMaxHeads * 4;
-constexpr int kSmemBytes = kOffXchg + kXchgBytes + 1024;   // + alignment slack
+constexpr int kXchgBytes = 3 * 2 * kMaxHeads * 4;      // running maxima / final sums of the two tile groups
 constexpr int kThreads = 352;                          // 2 tile groups of 4 warps, producer, 2 MMA warps
 constexpr int kThreadsFp8 = 512;                       // + 5 FP8 conversion warps (4 for the per-block format)
-// cache modes of the kernel: bf16 rows, e4m3 rows with one tensor scale, per-block e4m3 rows
-constexpr int kModeBf16 = 0, kModeFp8 = 1, kModeFp8Block = 2;
+// cache modes of the kernel: bf16 rows, e4m3 rows with one tensor scale (converted to bf16 in shared
+// memory, or used as they are by FP8 MMAs), per-block e4m3 rows
+constexpr int kModeBf16 = 0, kModeFp8 = 1, kModeFp8Block = 2, kModeFp8Mma = 3;
+// FP8 MMAs (kind::f8f6f4): the latent codes are the B operand of QK^T as stored; P . C reads P in
+// e4m3 and a copy of the tile's latent codes transposed to token-contiguous rows (every operand
+// K-major in shared memory)
+constexpr int kCodeBox = kPage * 128;        // 64 tokens x 128 e4m3 codes, 128-byte swizzle: 8 KB
+constexpr int kCtBytes = 256 * kPage;        // 256 latent columns x 64 token codes, 64-byte swizzle: 16 KB
+constexpr int kQ8Bytes = kMaxHeads * 256;    // e4m3 latent query: two boxes of 128 heads x 128 codes (SW128)
+constexpr int kP8Bytes = kMaxHeads * kPage;  // e4m3 P of one tile: 128 heads x 64 codes (SW64): 8 KB
+
+// Shared-memory layout of a kernel mode (offsets from the 1024-byte aligned base).
+template <int kMode>
+struct Smem {
+  static constexpr bool kMma8 = kMode == kModeFp8Mma;
+  static constexpr int kStages = kMma8 ? 3 : 4;
+  // a stage: the bf16 latent chunks (or two code boxes), the RoPE key in bf16, per-block scales
+  static constexpr int kStage = kMma8 ? 2 * kCodeBox + kRopeBytes : 4 * kChunkBytes + kRopeBytes + kScaleBytes;
+  static constexpr int kRopeOff = kMma8 ? 2 * kCodeBox : 4 * kChunkBytes;   // RoPE box inside a stage
+  static constexpr int kOffCt = kStages * kStage;                           // two transposed-tile buffers
+  static constexpr int kOffQ8 = kOffCt + (kMma8 ? 2 * kCtBytes : 0);
+  static constexpr int kOffQpe = kOffQ8 + (kMma8 ? kQ8Bytes : 0);
+  static constexpr int kOffRecv = kOffQpe + kQpeBytes;
+  static constexpr int kOffP8 = kOffRecv + kSlots * kSlotBytes;              // two e4m3 P slots
+  static constexpr int kOffBars = kOffP8 + (kMma8 ? 2 * kP8Bytes : 0);
+  static constexpr int kOffXchg = kOffBars + 1024;
+  static constexpr int kBytes = kOffXchg + kXchgBytes + 1024;                // + alignment slack
+  static_assert(kBytes <= 232448, "the largest dynamic shared memory a CTA may opt into (227 KB)");
+  static_assert(kOffQ8 >= 8 * 2 * 4096, "the epilogue stages its output in the first 64 KB");
+  static_assert(kOffCt % 1024 == 0 && kOffQ8 % 1024 == 0 && kOffP8 % 1024 == 0 && kStage % 1024 == 0, "atoms");
+};
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;                            // QK^T issuer (allocates TMEM)
 constexpr int kWarpPv = 10;                            // P . C issuer
@@ -94,9 +116,12 @@ constexpr uint32_t kTmS = 384;             // 64 columns of fp32 partial scores
 constexpr uint32_t kTmP = 448;             // P slot b (64 bf16 per lane) at kTmP + 32 b
 
 struct Bars {                               // mbarriers (8 bytes each) and flags
-  uint64_t full[kStages];                   // TMA tile landed                      (producer, tx)
-  uint64_t conv[kStages];                   // FP8 cache: tile converted to bf16    (5 or 4 conversion warps)
-  uint64_t empty[kStages];                  // tile consumed by P . C               (MMA commit)
+  uint64_t full[kStagesMax];                // TMA tile landed                      (producer, tx)
+  uint64_t conv[kStagesMax];                // FP8 cache: tile converted to bf16    (5 or 4 conversion warps;
+                                            //   FP8 MMAs: the RoPE key converted, 1 warp)
+  uint64_t empty[kStagesMax];               // tile consumed by P . C               (MMA commit; FP8 MMAs:
+                                            //   QK^T done (MMA commit) and the tile transposed (4 warps))
+  uint64_t tready[2];                       // FP8 MMAs: tile j transposed into buffer j % 2 (4 warps)
   uint64_t sfull[2];                        // S_r(j) in TMEM, tile group j % 2     (MMA commit)
   uint64_t sfree[2];                        // S_r(j) loaded by its tile group      (4 warps)
   uint64_t mready[2];                       // a group's running max published     (4 warps)
@@ -127,6 +152,17 @@ __device__ __forceinline__ uint32_t f16x2_sat(float lo, float hi) {
 }
 __device__ __forceinline__ float2 f16x2_to_f32(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+__device__ __forceinline__ float2 bf16x2_to_f32(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// four values -> e4m3 codes (round to nearest even, saturating at +-448), the first in the low byte
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  unsigned short lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
 // three-input maximum (one instruction on sm_100 and later)
@@ -196,29 +232,33 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                  const int32_t* __restrict__ block_table, int bt_stride, int num_pages, float scale_log2,
                  float out_scale, int stall, const uint8_t* __restrict__ w_next, size_t w_next_bytes, Workspace ws,
                  unsigned* check) {
-  constexpr bool kFp8 = kMode != kModeBf16;            // e4m3 codes, converted in shared memory
+  constexpr bool kFp8 = kMode != kModeBf16;            // e4m3 codes (converted in shared memory, or FP8 MMAs)
   constexpr bool kBlock = kMode == kModeFp8Block;
+  using L = Smem<kMode>;
+  constexpr bool kMma8 = L::kMma8;
+  constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base: swizzle atoms and TMA destinations need it
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(smem);
-  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::kOffBars);
   volatile int* abort_flag = &bars->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int unit_idx = blockIdx.x >> 1;
-  const uint32_t stage0 = sbase + kOffStages;
+  const uint32_t stage0 = sbase;            // the ring starts the layout
 
   // barriers and descriptor prefetch need nothing from the earlier kernels of the step
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
-      mbar_init(smem_u32(&bars->empty[s]), 1);
-      mbar_init(smem_u32(&bars->conv[s]), kBlock ? 4 : 5);
+      mbar_init(smem_u32(&bars->empty[s]), kMma8 ? 5 : 1);
+      mbar_init(smem_u32(&bars->conv[s]), kMma8 ? 1 : (kBlock ? 4 : 5));
     }
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->tready[i]), 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->sfull[i]), 1);
       mbar_init(smem_u32(&bars->sfree[i]), 4);
@@ -265,18 +305,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       page = 0;
     }
     const uint32_t full = smem_u32(&bars->full[s]);
-    constexpr uint32_t kTx = kBlock ? 2 * kChunkBytes + kRopeBytes + kScaleBytes
-                                    : (kFp8 ? 2 * kChunkBytes + kRopeBytes / 2 : 4 * kChunkBytes + kRopeBytes);
+    const uint32_t st = stage0 + s * L::kStage;
+    constexpr uint32_t kTx = kMma8 ? 2 * kCodeBox + kRopeBytes / 2
+                             : kBlock ? 2 * kChunkBytes + kRopeBytes + kScaleBytes
+                                      : (kFp8 ? 2 * kChunkBytes + kRopeBytes / 2 : 4 * kChunkBytes + kRopeBytes);
     mbar_arrive_expect_tx(full, kTx);
     // (an evict-first L2 policy on these once-read rows was measured 4 us slower per step)
-    for (int c = 0; c < 4; ++c)            // FP8: each code box into the upper half of its chunk slot
-      tma_load_2d(stage0 + s * kStageBytes + c * kChunkBytes + (kFp8 ? kChunkBytes / 2 : 0), &tmap,
-                  (int)(rank * 256 + c * 64), page * kPage, full);
+    if constexpr (kMma8) {                 // FP8 MMAs: two boxes of 128 codes, 128-byte swizzled, as stored
+      for (int c = 0; c < 2; ++c) tma_load_2d(st + c * kCodeBox, &tmap, (int)(rank * 256 + c * 128), page * kPage, full);
+    } else {
+      for (int c = 0; c < 4; ++c)          // FP8: each code box into the upper half of its chunk slot
+        tma_load_2d(st + c * kChunkBytes + (kFp8 ? kChunkBytes / 2 : 0), &tmap, (int)(rank * 256 + c * 64),
+                    page * kPage, full);
+    }
     // RoPE key: bf16 (its own map over the rows' last 128 bytes for the per-block format) or codes
-    tma_load_2d(stage0 + s * kStageBytes + 4 * kChunkBytes + (kMode == kModeFp8 ? kRopeBytes / 2 : 0), &tmap_rope,
+    tma_load_2d(st + L::kRopeOff + ((kMode == kModeFp8 || kMma8) ? kRopeBytes / 2 : 0), &tmap_rope,
                 (int)((kBlock ? 0 : kDc) + rank * 32), page * kPage, full);
     if (kBlock)                            // the 4 block scales of every token of the page
-      tma_load_2d(stage0 + s * kStageBytes + 4 * kChunkBytes + kRopeBytes, &tmap_scale, kDc, page * kPage, full);
+      tma_load_2d(st + 4 * kChunkBytes + kRopeBytes, &tmap_scale, kDc, page * kPage, full);
   };
   // the absorbed query of this CTA (latent half: 4 boxes of 64 columns x 128 heads, 128-byte
   // swizzle, staged in the still unused receive slots; RoPE half: straight into its 64-byte
@@ -293,8 +339,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     if (withheld != 0) issue_tile(0, pages[0]);
     const uint32_t qf = smem_u32(&bars->qfull);
     mbar_arrive_expect_tx(qf, (uint32_t)(4 * kMaxHeads * 128 + kQpeBytes));
-    for (int c = 0; c < 4; ++c) tma_load_3d(sbase + kOffRecv + c * kMaxHeads * 128, &tmap_q, (int)(rank * 256 + c * 64), 0, b, qf);
-    tma_load_3d(sbase + kOffQpe, &tmap_qpe, (int)(kDc + rank * 32), 0, b, qf);
+    for (int c = 0; c < 4; ++c)
+      tma_load_3d(sbase + L::kOffRecv + c * kMaxHeads * 128, &tmap_q, (int)(rank * 256 + c * 64), 0, b, qf);
+    tma_load_3d(sbase + L::kOffQpe, &tmap_qpe, (int)(kDc + rank * 32), 0, b, qf);
     for (int j = 1; j < n_pre; ++j)
       if (j != withheld) issue_tile(j, pages[j]);
   }
@@ -302,15 +349,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
     tmem_relinquish();
   }
-  const int L = ctx_len[b];
-  const int t_end = min(unit.page_end * kPage, L);
+  const int t_end = min(unit.page_end * kPage, ctx_len[b]);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
   // ---- latent half of the query: shared memory -> TMEM (A operand of QK^T).  Warp w moves heads
-  // 32 (w % 4) .. + 31, latent columns 128 (w / 4) .. + 127 of this CTA's 256.
+  // 32 (w % 4) .. + 31, latent columns 128 (w / 4) .. + 127 of this CTA's 256.  With FP8 MMAs the
+  // latent half is quantised instead: one e4m3 scale per head and CTA, s = max |q| / 448 over the
+  // CTA's 256 latent values, codes q / s into two 128-byte-swizzled boxes (box w / 4), and the RoPE
+  // half divided by s in place, so that QK^T sums s-scaled units (times s in the score scale).
+  float qscale = scale_log2;                // per-thread factor of the scores: scale (x s with FP8 MMAs)
   if (warp < 8) {
     const int q4 = warp & 3, half = warp >> 2;
     const int h = q4 * 32 + lane;
@@ -320,10 +370,61 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       for (int jj = half; jj < min(n_tiles, kSlots); jj += 2)
         mbar_arrive_expect_tx(smem_u32(&bars->recvfull[jj][q4]), 32 * 128);
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
-    if (__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->qfull), 0, abort_flag))) {
+    const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->qfull), 0, abort_flag));
+    if (!landed) fail_timeout(bars, check);
+    if constexpr (kMma8) {
+      uint32_t r[2][32];
+      float amax = 0.0f;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const uint8_t* row = smem + L::kOffRecv + (2 * half + part) * kMaxHeads * 128 + h * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 x = *reinterpret_cast<const uint4*>(row + ((k ^ (h & 7)) * 16));
+          r[part][4 * k] = x.x; r[part][4 * k + 1] = x.y; r[part][4 * k + 2] = x.z; r[part][4 * k + 3] = x.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float2 v = bf16x2_to_f32(r[part][k]);
+          amax = fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y)));
+        }
+      }
+      float* amax_x = reinterpret_cast<float*>(smem + L::kOffXchg) + 2 * kMaxHeads;   // [half][head]
+      amax_x[half * kMaxHeads + h] = amax;
+      named_barrier(1, 256);                // the two halves of every head's amax are out
+      amax = fmaxf(amax_x[h], amax_x[kMaxHeads + h]);
+      const float sq = amax > 0.0f ? amax * (1.0f / 448.0f) : 1.0f, inv = 1.0f / sq;
+      qscale = scale_log2 * sq;
+      uint8_t* q8row = smem + L::kOffQ8 + half * (kQ8Bytes / 2) + h * 128;
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {        // 16 codes = 8 words of this part
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 v0 = bf16x2_to_f32(r[part][8 * c + 2 * i]), v1 = bf16x2_to_f32(r[part][8 * c + 2 * i + 1]);
+            w[i] = e4m3x4(v0.x * inv, v0.y * inv, v1.x * inv, v1.y * inv);
+          }
+          const int chunk = 4 * part + c;
+          *reinterpret_cast<uint4*>(q8row + ((chunk ^ (h & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      if (half == 0) {                       // the RoPE half, 32 bf16 of the head, divided by s in place
+        uint8_t* pe = smem + L::kOffQpe + h * 64;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4* p4 = reinterpret_cast<uint4*>(pe + ((c ^ ((h >> 1) & 3)) * 16));
+          uint4 x = *p4;
+          const float2 a = bf16x2_to_f32(x.x), bq = bf16x2_to_f32(x.y), cq = bf16x2_to_f32(x.z), d = bf16x2_to_f32(x.w);
+          *p4 = make_uint4(bf16x2_bits(a.x * inv, a.y * inv), bf16x2_bits(bq.x * inv, bq.y * inv),
+                           bf16x2_bits(cq.x * inv, cq.y * inv), bf16x2_bits(d.x * inv, d.y * inv));
+        }
+      }
+      fence_proxy_async_smem();              // generic writes before the tensor core reads them
+    } else if (landed) {
 #pragma unroll
       for (int part = 0; part < 2; ++part) {      // box 2 half + part: 64 columns = 32 TMEM columns
-        const uint8_t* row = smem + kOffRecv + (2 * half + part) * kMaxHeads * 128 + h * 128;
+        const uint8_t* row = smem + L::kOffRecv + (2 * half + part) * kMaxHeads * 128 + h * 128;
         uint32_t r[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -333,8 +434,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         tmem_st32(lane_addr + kTmQ + 64 * half + 32 * part, r);
       }
       tmem_st_wait();
-    } else {
-      fail_timeout(bars, check);
     }
     fence_proxy_async_smem();    // these reads come before the copies that later reuse the slots
   }
@@ -346,29 +445,26 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      auto prefetch_tile = [&](int pg) {     // a tile's boxes into L2 (no shared memory, no completion)
+        if (pg >= 0 && pg < num_pages) {
+          if constexpr (kMma8) {
+            for (int c = 0; c < 2; ++c) tma_prefetch_2d(&tmap, (int)(rank * 256 + c * 128), pg * kPage);
+          } else {
+            for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tmap, (int)(rank * 256 + c * 64), pg * kPage);
+          }
+          tma_prefetch_2d(&tmap_rope, (int)((kBlock ? 0 : kDc) + rank * 32), pg * kPage);
+          if (kBlock) tma_prefetch_2d(&tmap_scale, kDc, pg * kPage);
+        }
+      };
       // the next user of each stage into L2, once tile 0 has landed (out of the start-up burst)
       if (n_tiles > kStages && mbar_wait(smem_u32(&bars->full[0]), 0, abort_flag)) {
-        for (int j = kStages; j < min(n_tiles, 2 * kStages); ++j) {
-          const int pg = bt_row[j];
-          if (pg >= 0 && pg < num_pages) {
-            for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tmap, (int)(rank * 256 + c * 64), pg * kPage);
-            tma_prefetch_2d(&tmap_rope, (int)((kBlock ? 0 : kDc) + rank * 32), pg * kPage);
-            if (kBlock) tma_prefetch_2d(&tmap_scale, kDc, pg * kPage);
-          }
-        }
+        for (int j = kStages; j < min(n_tiles, 2 * kStages); ++j) prefetch_tile(bt_row[j]);
       }
       int issued = n_pre;
       for (int j = n_pre; j < n_tiles; ++j) {
         const int s = j % kStages;
         const int page = bt_row[j];
-        if (j + kStages < n_tiles) {         // the tile that will refill this stage next, into L2
-          const int pg = bt_row[j + kStages];
-          if (pg >= 0 && pg < num_pages) {
-            for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tmap, (int)(rank * 256 + c * 64), pg * kPage);
-            tma_prefetch_2d(&tmap_rope, (int)((kBlock ? 0 : kDc) + rank * 32), pg * kPage);
-            if (kBlock) tma_prefetch_2d(&tmap_scale, kDc, pg * kPage);
-          }
-        }
+        if (j + kStages < n_tiles) prefetch_tile(bt_row[j + kStages]);   // the stage's next tile, into L2
         if (!mbar_wait(smem_u32(&bars->empty[s]), ((j / kStages) & 1) ^ 1, abort_flag)) {
           fail_timeout(bars, check);
           break;
@@ -395,7 +491,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // ------------------------------------------------------------ QK^T issuer
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 64, false, false);
-      const uint64_t qpe_desc = sdesc_sw64(sbase + kOffQpe, 16, 512);
+      const uint32_t idesc_qk8 = idesc_e4m3_f32(128, 64);
+      const uint64_t qpe_desc = sdesc_sw64(sbase + L::kOffQpe, 16, 512);
+      const uint64_t q8_desc = sdesc_sw128(sbase + L::kOffQ8, 16, 1024);
       bool ok = true;
       for (int j = 0; j < n_tiles; ++j) {
         const int s = j % kStages;
@@ -406,17 +504,25 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
           break;
         }
         tc_fence_after();
-        const uint32_t st = stage0 + s * kStageBytes;
-        const uint64_t lat_desc = sdesc_sw128(st, 16, 1024), rope_desc = sdesc_sw64(st + 4 * kChunkBytes, 16, 512);
+        const uint32_t st = stage0 + s * L::kStage;
+        const uint64_t lat_desc = sdesc_sw128(st, 16, 1024), rope_desc = sdesc_sw64(st + L::kRopeOff, 16, 512);
         const uint32_t d = tmem + kTmS;
+        if constexpr (kMma8) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k)         // latent chunk k / 4, 32-byte step k % 4 inside the 128-byte row
-          mma_ts(d, tmem + kTmQ + 8 * k, lat_desc + (uint64_t)((((k >> 2) * kChunkBytes) + (k & 3) * 32) >> 4),
-                 idesc_qk, k > 0);
+          for (int k = 0; k < 8; ++k)        // code box k / 4, 32-code step k % 4 inside the 128-byte row
+            mma8_ss(d, q8_desc + (uint64_t)((((k >> 2) * (kQ8Bytes / 2)) + (k & 3) * 32) >> 4),
+                    lat_desc + (uint64_t)((((k >> 2) * kCodeBox) + (k & 3) * 32) >> 4), idesc_qk8, k > 0);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k)       // latent chunk k / 4, 32-byte step k % 4 inside the 128-byte row
+            mma_ts(d, tmem + kTmQ + 8 * k, lat_desc + (uint64_t)((((k >> 2) * kChunkBytes) + (k & 3) * 32) >> 4),
+                   idesc_qk, k > 0);
+        }
 #pragma unroll
         for (int k = 0; k < 2; ++k)
           mma_ss(d, qpe_desc + (uint64_t)(2 * k), rope_desc + (uint64_t)(2 * k), idesc_qk, 1);
         mma_commit(smem_u32(&bars->sfull[j & 1]));
+        if constexpr (kMma8) mma_commit(smem_u32(&bars->empty[s]));   // QK^T's share of releasing the stage
       }
       if (!ok) fail_timeout(bars, check);
       mma_commit(smem_u32(&bars->drain[0]));   // arrives once every MMA issued above has finished
@@ -429,17 +535,32 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // TMEM: P slots and O, against the score buffer).
     if (lane == 0) {
       const uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
+      const uint32_t idesc_pv8 = idesc_e4m3_f32(128, 256);
       bool ok = true;
       for (int jj = 0; jj < n_tiles; ++jj) {
         const int s = jj % kStages, bb = jj & 1;
-        if (!mbar_wait(smem_u32(&bars->pfull[bb]), (jj >> 1) & 1, abort_flag)) { ok = false; break; }
+        // P(jj) written; with FP8 MMAs also tile jj transposed into buffer jj % 2
+        if (!mbar_wait(smem_u32(&bars->pfull[bb]), (jj >> 1) & 1, abort_flag) ||
+            (kMma8 && !mbar_wait(smem_u32(&bars->tready[bb]), (jj >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const uint64_t c_desc = sdesc_sw128(stage0 + s * kStageBytes, kChunkBytes, 1024);
+        if constexpr (kMma8) {               // e4m3 P (K-major, 64-byte rows) . transposed codes (K-major)
+          const uint64_t p_desc = sdesc_sw64(sbase + L::kOffP8 + bb * kP8Bytes, 16, 512);
+          const uint64_t ct_desc = sdesc_sw64(sbase + L::kOffCt + bb * kCtBytes, 16, 512);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + kTmO, tmem + kTmP + 32 * bb + 8 * k, c_desc + (uint64_t)(128 * k), idesc_pv,
-                 (jj > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bars->empty[s]));
+          for (int k = 0; k < 2; ++k)        // 32 tokens per step: 32 bytes along both operands' rows
+            mma8_ss(tmem + kTmO, p_desc + (uint64_t)(2 * k), ct_desc + (uint64_t)(2 * k), idesc_pv8,
+                    (jj > 0 || k > 0) ? 1u : 0u);
+        } else {
+          const uint64_t c_desc = sdesc_sw128(stage0 + s * L::kStage, kChunkBytes, 1024);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + kTmO, tmem + kTmP + 32 * bb + 8 * k, c_desc + (uint64_t)(128 * k), idesc_pv,
+                   (jj > 0 || k > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bars->empty[s]));
+        }
         mma_commit(smem_u32(&bars->pdone[bb]));
         if (jj == n_tiles - 1) mma_commit(smem_u32(&bars->ofinal));
       }
@@ -458,13 +579,77 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     if constexpr (kFp8) {
       const int c = warp - kWarpConv;         // 0..3 latent chunk, 4 RoPE box (codes with one tensor scale)
       bool ok = true;
-      for (int t = 0; t < n_tiles && !(kBlock && c == 4); ++t) {
+      if (kMma8 && c < 4) {
+        // FP8 MMAs: warp 11 + c transposes latent columns [64 c, 64 c + 64) of every tile into the
+        // buffer of the tile's parity: row n = latent column, 64 token codes, 64-byte swizzle
+        // (16-byte chunk k of row n at k ^ ((n >> 1) & 3)), token codes past the context zeroed.
+        // Lane = (token group tg = lane & 3: tokens 16 tg .. + 15; column group cg = lane >> 2:
+        // columns 8 cg .. + 7 of the warp's 64); 4 x 4 byte blocks are transposed with byte permutes.
+        const int tg = lane & 3, cg = lane >> 2;
+        const int box = c >> 1, chunk = 4 * (c & 1) + (cg >> 1), off8 = (cg & 1) * 8;
+        for (int t = 0; t < n_tiles; ++t) {
+          const int s = t % kStages, bb = t & 1;
+          // the tile has landed, and buffer bb's last reader, P . C of tile t - 2, has finished
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (t / kStages) & 1, abort_flag)) ||
+              (t >= 2 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->pdone[bb]), ((t - 2) >> 1) & 1, abort_flag)))) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src = smem + s * L::kStage + box * kCodeBox;
+          uint32_t a[16][2];                  // a[r]: the 8 codes of token 16 tg + r
+#pragma unroll
+          for (int r = 0; r < 16; ++r) {
+            const int tok = 16 * tg + r;
+            const uint2 v = *reinterpret_cast<const uint2*>(src + tok * 128 + ((chunk ^ (tok & 7)) * 16) + off8);
+            a[r][0] = v.x;
+            a[r][1] = v.y;
+          }
+          uint32_t o[8][4];                   // o[col][i]: the codes of tokens 16 tg + 4 i .. + 3 in column col
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const uint32_t t0 = __byte_perm(a[4 * i][k], a[4 * i + 1][k], 0x5140);
+              const uint32_t t1 = __byte_perm(a[4 * i][k], a[4 * i + 1][k], 0x7362);
+              const uint32_t t2 = __byte_perm(a[4 * i + 2][k], a[4 * i + 3][k], 0x5140);
+              const uint32_t t3 = __byte_perm(a[4 * i + 2][k], a[4 * i + 3][k], 0x7362);
+              o[4 * k][i] = __byte_perm(t0, t2, 0x5410);
+              o[4 * k + 1][i] = __byte_perm(t0, t2, 0x7632);
+              o[4 * k + 2][i] = __byte_perm(t1, t3, 0x5410);
+              o[4 * k + 3][i] = __byte_perm(t1, t3, 0x7632);
+            }
+          const int valid = min(kPage, t_end - (unit.page_begin + t) * kPage);
+          if (valid < kPage) {                // a partial last page: codes of rows past the context become 0
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int nv = min(4, max(0, valid - (16 * tg + 4 * i)));
+              const uint32_t keep = nv >= 4 ? 0xFFFFFFFFu : ((1u << (8 * nv)) - 1u);
+#pragma unroll
+              for (int col = 0; col < 8; ++col) o[col][i] &= keep;
+            }
+          }
+          uint8_t* dst = smem + L::kOffCt + bb * kCtBytes;
+#pragma unroll
+          for (int col = 0; col < 8; ++col) {
+            const int n = 64 * c + 8 * cg + col;
+            *reinterpret_cast<uint4*>(dst + n * 64 + ((tg ^ ((n >> 1) & 3)) * 16)) =
+                make_uint4(o[col][0], o[col][1], o[col][2], o[col][3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&bars->tready[bb]));
+            mbar_arrive(smem_u32(&bars->empty[s]));   // this warp is done with the stage's codes
+          }
+        }
+      }
+      for (int t = 0; t < n_tiles && !(kBlock && c == 4) && !(kMma8 && c < 4); ++t) {
         const int s = t % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (t / kStages) & 1, abort_flag))) {
           ok = false;
           break;
         }
-        uint8_t* st = smem + kOffStages + s * kStageBytes;
+        uint8_t* st = smem + s * L::kStage;
         if (c < 4 && kBlock) {
           // as below, each value times its token's scale for this chunk's block of 128 latent
           // values (block 2 rank + c / 2; the page's scales sit after the RoPE box, 16 bytes a token)
@@ -505,7 +690,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         } else {
           // lane = (row 16 k + lane / 2, 16 codes 16 (lane % 2) ..) for k = 0..3
           const int p = lane & 1;
-          uint8_t* box = st + 4 * kChunkBytes;
+          uint8_t* box = st + L::kRopeOff;
           uint4 v[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -536,10 +721,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const int g = warp >> 2, q4 = warp & 3;
     const int h = q4 * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
-    const uint32_t recv_peer = map_to_rank(sbase + kOffRecv, peer);
-    float* m_pub = reinterpret_cast<float*>(smem + kOffXchg);    // [group][head]: running max after its last tile
+    const uint32_t recv_peer = map_to_rank(sbase + L::kOffRecv, peer);
+    float* m_pub = reinterpret_cast<float*>(smem + L::kOffXchg);    // [group][head]: running max after its last tile
     float* fin_x = m_pub + 2 * kMaxHeads;                         // [group][2][head]: final (max, sum)
-    const float2 sc2 = make_float2(scale_log2, scale_log2), zero2 = make_float2(0.0f, 0.0f);
+    const float2 sc2 = make_float2(qscale, qscale), zero2 = make_float2(0.0f, 0.0f);
     float m_g = -INFINITY, l_g = 0.0f;        // this group's sum, relative to 2^m_g
     bool ok = true;
     int sent = 0, consumed = 0;               // this warp's partial-score copies sent / received (in tile order)
@@ -582,7 +767,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         // the peer's tile j - 2 copies, sent after the peer's group g finished tile j - 4,
         // the last user of the slot -- and re-armed the slot's quarter for tile j there, so
         // every copy lands in an armed phase.
-        uint8_t* stg = smem + kOffRecv + ((j + 2) & (kSlots - 1)) * kSlotBytes;
+        uint8_t* stg = smem + L::kOffRecv + ((j + 2) & (kSlots - 1)) * kSlotBytes;
 #pragma unroll
         for (int qq = 0; qq < 8; ++qq)
           *reinterpret_cast<uint4*>(stg + h * 128 + ((qq ^ (h & 7)) * 16)) =
@@ -604,7 +789,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       ++consumed;
       {
         // x = x_own + x_peer
-        const uint4* rp = reinterpret_cast<const uint4*>(smem + kOffRecv + slot * kSlotBytes + h * 128);
+        const uint4* rp = reinterpret_cast<const uint4*>(smem + L::kOffRecv + slot * kSlotBytes + h * 128);
 #pragma unroll
         for (int qq = 0; qq < 8; ++qq) {
           const uint4 v = rp[qq ^ (h & 7)];
@@ -619,14 +804,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         mbar_arrive_expect_tx(smem_u32(&bars->recvfull[slot][q4]), 32 * 128);
       if (valid < kPage) {
         // a partial last page: rows past the context hold stale data; zero this CTA's latent
-        // rows there so P = 0 meets finite values in P . C
-        uint8_t* st = smem + kOffStages + (j % kStages) * kStageBytes;
-        const int rows = kPage - valid;
-        for (int i = h; i < 4 * rows * 8; i += 128) {
-          const int cc = i / (rows * 8), rr = valid + (i / 8) % rows, kk = i % 8;
-          *reinterpret_cast<uint4*>(st + cc * kChunkBytes + rr * 128 + kk * 16) = make_uint4(0, 0, 0, 0);
+        // rows there so P = 0 meets finite values in P . C (with FP8 MMAs the transposing warps
+        // zero those tokens' codes in the copy P . C reads)
+        if constexpr (!kMma8) {
+          uint8_t* st = smem + (j % kStages) * L::kStage;
+          for (int rr = valid + (h >> 3); rr < kPage; rr += 16)     // 16 rows x 8 16-byte pieces per pass
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+              *reinterpret_cast<uint4*>(st + cc * kChunkBytes + rr * 128 + (h & 7) * 16) = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           if (2 * i >= valid) x2[i].x = -INFINITY;
@@ -686,15 +873,31 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         const float2 d = __fadd2_rn(x2[i], negm2);
         const float2 p = make_float2(ex2_approx(d.x), ex2_approx(d.y));
         ps[i & 3] = __fadd2_rn(ps[i & 3], p);
-        pk[i] = bf16x2_bits(p.x, p.y);
+        if constexpr (kMma8) x2[i] = p;       // packed to e4m3 below
+        else pk[i] = bf16x2_bits(p.x, p.y);
       }
       {
         const float2 s2 = __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3]));
         l_g += s2.x + s2.y;
       }
-      tmem_st32(lane_addr + kTmP + 32 * g, pk);
-      tmem_st_wait();
-      tc_fence_before();
+      if constexpr (kMma8) {
+        // P(j) as e4m3 codes (P <= 2^8 < 448) into this thread's row of P slot g (64-byte rows,
+        // 16-byte chunk c at c ^ ((h >> 1) & 3)); its last reader, P . C of tile j - 2, is done
+        uint8_t* prow = smem + L::kOffP8 + g * kP8Bytes + h * 64;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            w[q] = e4m3x4(x2[8 * c + 2 * q].x, x2[8 * c + 2 * q].y, x2[8 * c + 2 * q + 1].x, x2[8 * c + 2 * q + 1].y);
+          *reinterpret_cast<uint4*>(prow + ((c ^ ((h >> 1) & 3)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();            // generic writes before the tensor core reads them
+      } else {
+        tmem_st32(lane_addr + kTmP + 32 * g, pk);
+        tmem_st_wait();
+        tc_fence_before();
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->pfull[g]));
     }
@@ -725,7 +928,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       const bool live = h < n_h;
       // a whole sequence: bf16 rows staged in the (now idle) ring, this warp's 32 heads x 2 boxes
       // of 64 columns, 128-byte swizzled, and written by TMA stores (heads past n_h are clipped)
-      uint8_t* ob = smem + kOffStages + (g * 4 + q4) * 2 * 4096;
+      uint8_t* ob = smem + (g * 4 + q4) * 2 * 4096;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         const int c0 = 128 * g + 32 * cc;
@@ -817,8 +1020,10 @@ cudaError_t make_cache_tensor_map(const void* cache, int num_pages, int width, C
 }
 
 // Tensor map of an e4m3 cache [num_pages * 64 rows][576 bytes]: boxes of `width` bytes x 64
-// rows, no swizzle (the kernel converts them into swizzled bf16 chunks).
+// rows, no swizzle (the kernel converts them into swizzled bf16 chunks), or, for 128-byte boxes,
+// 128-byte swizzled (FP8 MMA operands as they land).
 cudaError_t make_cache_tensor_map_fp8(const void* cache, int num_pages, int width, CUtensorMap* map) {
+  // 128-byte boxes are MMA operands as loaded (128-byte swizzle); narrower ones are converted first
   auto enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)num_pages * kPage};
@@ -826,7 +1031,7 @@ cudaError_t make_cache_tensor_map_fp8(const void* cache, int num_pages, int widt
   const cuuint32_t box[2] = {(cuuint32_t)width, (cuuint32_t)kPage};
   const cuuint32_t elem[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims, strides, box, elem,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, width == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -902,13 +1107,13 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch,
   static bool attr = false;
   if (!attr) {
     cudaError_t e =
-        cudaFuncSetAttribute(decode_tc_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(decode_tc_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<kMode>::kBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   // an FP8 cache with one tensor scale holds codes of value / fp8_scale: the scale multiplies
   // every score and the output (the per-block format's values are scaled when converted)
-  const float cache_scale = kMode == kModeFp8 ? h.cfg.fp8_scale : 1.0f;
+  const float cache_scale = (kMode == kModeFp8 || kMode == kModeFp8Mma) ? h.cfg.fp8_scale : 1.0f;
   const float scale_log2 = h.scale * cache_scale * 1.4426950408889634f;
   // the absorbed query [B][n_h][576] as (column, head, sequence): 64- and 32-column boxes of 128 heads
   alignas(64) CUtensorMap map_q, map_qpe;
@@ -918,7 +1123,7 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch,
   if (e == cudaSuccess) e = make_latent_out_tensor_map(ws.o_lat, batch, h.cfg.n_h, &map_o);
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_tc_kernel<kMode>, dim3(2 * ws.max_units), dim3(kMode != kModeBf16 ? kThreadsFp8 : kThreads),
-                    kSmemBytes, st, map, map_rope, map_scale, map_q, map_qpe, map_o,
+                    Smem<kMode>::kBytes, st, map, map_rope, map_scale, map_q, map_qpe, map_o,
                     ctx_len,
                     h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, h.test_stall,
                     reinterpret_cast<const uint8_t*>(h.w_uv), sizeof(__nv_bfloat16) * (size_t)h.cfg.n_h * kDv * kDc, ws,
@@ -944,6 +1149,9 @@ cudaError_t cache_maps(const Handle& h, const void* cache, int num_pages) {
       if (e == cudaSuccess)
         e = fp8 ? make_cache_tensor_map_fp8(cache, num_pages, 32, mr) : make_cache_tensor_map(cache, num_pages, 32, mr);
       if (e == cudaSuccess) *ms = *m;      // unused by these formats; any valid map
+      CUtensorMap* m8 = reinterpret_cast<CUtensorMap*>(hm.tmap8);
+      if (e == cudaSuccess) e = fp8 ? make_cache_tensor_map_fp8(cache, num_pages, 128, m8) : cudaSuccess;
+      if (e == cudaSuccess && !fp8) *m8 = *m;
     }
     if (e != cudaSuccess) return e;
     hm.tmap_cache = cache;
@@ -953,7 +1161,7 @@ cudaError_t cache_maps(const Handle& h, const void* cache, int num_pages) {
 }
 
 // Decode-kernel dispatch: the tensor-core kernel, with in-shared-memory e4m3 -> bf16
-// conversion for an FP8 cache.
+// conversion for an FP8 cache, or (per-tensor scale, MLA_OPT_FP8_MMA) FP8 tensor-core MMAs.
 cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table,
                           int bt_stride, const void* cache, int num_pages, const Workspace& ws, cudaStream_t st) {
   cudaError_t e = cache_maps(h, cache, num_pages);
@@ -963,6 +1171,9 @@ cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch, co
   const CUtensorMap& map_scale = *reinterpret_cast<const CUtensorMap*>(h.tmap_scale);
   switch (h.cfg.cache_dtype) {
     case MLA_CACHE_FP8_E4M3:
+      if (h.fp8_mma)
+        return launch_decode_tc<kModeFp8Mma>(h, ctx_len, batch, block_table, bt_stride, num_pages,
+                                             *reinterpret_cast<const CUtensorMap*>(h.tmap8), map_rope, map_scale, ws, st);
       return launch_decode_tc<kModeFp8>(h, ctx_len, batch, block_table, bt_stride, num_pages, map, map_rope,
                                         map_scale, ws, st);
     case MLA_CACHE_FP8_E4M3_BLOCK:

@@ -66,12 +66,14 @@ struct Handle {
   int force_splits;         // MLA_OPT_SPLITS
   int profile;              // MLA_OPT_PROFILE
   int test_stall;           // MLA_OPT_TEST_STALL
+  int fp8_mma;              // MLA_OPT_FP8_MMA
   cudaEvent_t ev[8];
   int n_ev_recorded;
   int prof_prefill;         // the last profiled call was mla_prefill (else mla_decode)
   alignas(64) unsigned char tmap[128];   // TMA descriptor (CUtensorMap) of the last cache seen
   alignas(64) unsigned char tmap_rope[128];  // same cache, RoPE-key columns (32-column boxes)
   alignas(64) unsigned char tmap_scale[128]; // per-block FP8 cache: the rows' scale bytes
+  alignas(64) unsigned char tmap8[128];      // per-tensor FP8 cache: 128-code boxes, 128-byte swizzle (FP8 MMAs)
   alignas(64) unsigned char tmap_wuk[128];  // TMA descriptors of the handle's weight copies
   alignas(64) unsigned char tmap_wuv[128];
   const void* tmap_cache;

@@ -17,8 +17,8 @@ from tests.mla_cases import (bf16_out_to_f64, compare, gpu_rows, oracle_decode, 
 pytestmark = pytest.mark.gpu
 
 
-def _check(wl, check_codes=True):
-    s = DecodeSession(wl)
+def _check(wl, check_codes=True, fp8_mma=False):
+    s = DecodeSession(wl, fp8_mma=fp8_mma)
     s.prefill()
     rows, seq, pos = s.step_inputs()
     s.append_step(rows, seq, pos)                       # the decode token's own row, as in a step
@@ -62,3 +62,11 @@ def test_named_config(name):
     wl = W.NAMED[name]()
     rel, err, scale = _check(wl)
     assert rel <= tolerance(wl), (name, rel, err, scale)
+
+
+def test_fp8_config_with_fp8_mma():
+    """The V3 B=128 x 4096 per-tensor FP8 configuration with both contractions on FP8 tensor cores
+    (MLA_OPT_FP8_MMA): e4m3 query (one scale per head and half) and e4m3 P."""
+    wl = W.NAMED["v3_b128_s4096_fp8"]()
+    rel, err, scale = _check(wl, fp8_mma=True)
+    assert rel <= tolerance(wl), (rel, err, scale)
