@@ -385,13 +385,13 @@ mla_status_t mla_get_status(mla_handle_t h, mla_stream_t stream, uint32_t* devic
                                box of the expansion kernel's first CTA; 5: one key box of the
                                attention kernel (sequence 0, head 0, first query block).  0 (the default): off.  A CUDA
                                graph keeps the value it was captured with. */
-#define MLA_OPT_FP8_MMA 4   /* per-tensor FP8 cache (MLA_CACHE_FP8_E4M3): value 1 runs the decode's
+#define MLA_OPT_FP8_MMA 4   /* per-tensor FP8 cache (MLA_CACHE_FP8_E4M3): value 1 (the default) runs the decode's
                                contractions on FP8 tensor cores ("G5 MLA KV 访存建模设计规格" use case 1,
                                the FP8 latent cache): QK^T reads the cached e4m3 codes as
                                they are, against the absorbed query quantised to e4m3 with one scale per
                                head (max |q| / 448 over each half of the latent columns; the RoPE part
                                stays bf16), and P . C reads P in e4m3 (P <= 2^8) against a transposed
-                               copy of the tile's codes.  Value 0 (the default): the codes are
+                               copy of the tile's codes (the default).  Value 0: the codes are
                                converted to bf16 in shared memory and both contractions run in bf16.
                                The two differ by the e4m3 rounding of q and P (within the FP8
                                tolerance of the tests).  No effect on other caches. */

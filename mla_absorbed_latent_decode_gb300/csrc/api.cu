@@ -193,6 +193,7 @@ mla_status_t mla_create(const mla_config_t* cfg, const void* w_uk, const void* w
   h->device = dev;
   h->num_sms = sms;
   h->num_pairs = sms / 2;
+  h->fp8_mma = 1;                           // MLA_OPT_FP8_MMA default
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   auto cleanup = [&](mla_status_t err) { mla_destroy(reinterpret_cast<mla_handle_t>(h)); return err; };

@@ -73,6 +73,7 @@ constexpr int kSlotBytes = kMaxHeads * kPage * 2;      // 128 x 64 fp16 = 16 KB
 constexpr int kXchgBytes = 3 * 2 * kMaxHeads * 4;      // running maxima / final sums of the two tile groups
 constexpr int kThreads = 352;                          // 2 tile groups of 4 warps, producer, 2 MMA warps
 constexpr int kThreadsFp8 = 512;                       // + 5 FP8 conversion warps (4 for the per-block format)
+constexpr int kThreadsFp8Mma = 512;                    // + 4 warps transposing tiles, 1 converting the RoPE key
 // cache modes of the kernel: bf16 rows, e4m3 rows with one tensor scale (converted to bf16 in shared
 // memory, or used as they are by FP8 MMAs), per-block e4m3 rows
 constexpr int kModeBf16 = 0, kModeFp8 = 1, kModeFp8Block = 2, kModeFp8Mma = 3;
@@ -90,8 +91,11 @@ struct Smem {
   static constexpr bool kMma8 = kMode == kModeFp8Mma;
   static constexpr int kStages = kMma8 ? 3 : 4;
   // a stage: the bf16 latent chunks (or two code boxes), the RoPE key in bf16, per-block scales
-  static constexpr int kStage = kMma8 ? 2 * kCodeBox + kRopeBytes : 4 * kChunkBytes + kRopeBytes + kScaleBytes;
+  // (FP8 MMAs: two code boxes, the RoPE key in bf16, then its 2 KB of codes, converted out of place)
+  static constexpr int kStage = kMma8 ? 2 * kCodeBox + kRopeBytes + kRopeBytes / 2
+                                      : 4 * kChunkBytes + kRopeBytes + kScaleBytes;
   static constexpr int kRopeOff = kMma8 ? 2 * kCodeBox : 4 * kChunkBytes;   // RoPE box inside a stage
+  static constexpr int kRopeCodeOff = kMma8 ? 2 * kCodeBox + kRopeBytes : kRopeOff + kRopeBytes / 2;
   static constexpr int kOffCt = kStages * kStage;                           // two transposed-tile buffers
   static constexpr int kOffQ8 = kOffCt + (kMma8 ? 2 * kCtBytes : 0);
   static constexpr int kOffQpe = kOffQ8 + (kMma8 ? kQ8Bytes : 0);
@@ -223,7 +227,8 @@ __device__ __forceinline__ uint2 e4m3x4_scaled_to_bf16x4(uint32_t w, float scale
 // format brings each page's block scales in a 1 KB box and its RoPE key already in bf16: four
 // warps convert the latent boxes, each value times its token's block scale.
 template <int kMode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMode != kModeBf16 ? kThreadsFp8 : kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1)
+__launch_bounds__(kMode == kModeFp8Mma ? kThreadsFp8Mma : kMode != kModeBf16 ? kThreadsFp8 : kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_rope,
                  const __grid_constant__ CUtensorMap tmap_scale,
                  const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_qpe,
@@ -319,7 +324,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                     page * kPage, full);
     }
     // RoPE key: bf16 (its own map over the rows' last 128 bytes for the per-block format) or codes
-    tma_load_2d(st + L::kRopeOff + ((kMode == kModeFp8 || kMma8) ? kRopeBytes / 2 : 0), &tmap_rope,
+    tma_load_2d(kMma8 ? st + L::kRopeCodeOff : st + L::kRopeOff + (kMode == kModeFp8 ? kRopeBytes / 2 : 0), &tmap_rope,
                 (int)((kBlock ? 0 : kDc) + rank * 32), page * kPage, full);
     if (kBlock)                            // the 4 block scales of every token of the page
       tma_load_2d(st + 4 * kChunkBytes + kRopeBytes, &tmap_scale, kDc, page * kPage, full);
@@ -373,7 +378,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->qfull), 0, abort_flag));
     if (!landed) fail_timeout(bars, check);
     if constexpr (kMma8) {
-      uint32_t r[2][32];
+      // two passes over the staged bf16 query (it stays in the receive slots until the exchange
+      // starts): the head's maximum magnitude, then the codes
       float amax = 0.0f;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
@@ -381,12 +387,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint4 x = *reinterpret_cast<const uint4*>(row + ((k ^ (h & 7)) * 16));
-          r[part][4 * k] = x.x; r[part][4 * k + 1] = x.y; r[part][4 * k + 2] = x.z; r[part][4 * k + 3] = x.w;
-        }
+          const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float2 v = bf16x2_to_f32(r[part][k]);
-          amax = fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y)));
+          for (int i = 0; i < 4; ++i) {
+            const float2 v = bf16x2_to_f32(w4[i]);
+            amax = fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y)));
+          }
         }
       }
       float* amax_x = reinterpret_cast<float*>(smem + L::kOffXchg) + 2 * kMaxHeads;   // [half][head]
@@ -397,18 +403,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       qscale = scale_log2 * sq;
       uint8_t* q8row = smem + L::kOffQ8 + half * (kQ8Bytes / 2) + h * 128;
 #pragma unroll
-      for (int part = 0; part < 2; ++part)
+      for (int part = 0; part < 2; ++part) {
+        const uint8_t* row = smem + L::kOffRecv + (2 * half + part) * kMaxHeads * 128 + h * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {        // 16 codes = 8 words of this part
+        for (int c = 0; c < 4; ++c) {        // 16 codes = 8 bf16 pairs (two 16-byte pieces of the row)
+          const uint4 x0 = *reinterpret_cast<const uint4*>(row + (((2 * c) ^ (h & 7)) * 16));
+          const uint4 x1 = *reinterpret_cast<const uint4*>(row + (((2 * c + 1) ^ (h & 7)) * 16));
+          const uint32_t w8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
           uint32_t w[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float2 v0 = bf16x2_to_f32(r[part][8 * c + 2 * i]), v1 = bf16x2_to_f32(r[part][8 * c + 2 * i + 1]);
+            const float2 v0 = bf16x2_to_f32(w8[2 * i]), v1 = bf16x2_to_f32(w8[2 * i + 1]);
             w[i] = e4m3x4(v0.x * inv, v0.y * inv, v1.x * inv, v1.y * inv);
           }
           const int chunk = 4 * part + c;
           *reinterpret_cast<uint4*>(q8row + ((chunk ^ (h & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+      }
       if (half == 0) {                       // the RoPE half, 32 bf16 of the head, divided by s in place
         uint8_t* pe = smem + L::kOffQpe + h * 64;
 #pragma unroll
@@ -585,8 +596,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         // (16-byte chunk k of row n at k ^ ((n >> 1) & 3)), token codes past the context zeroed.
         // Lane = (token group tg = lane & 3: tokens 16 tg .. + 15; column group cg = lane >> 2:
         // columns 8 cg .. + 7 of the warp's 64); 4 x 4 byte blocks are transposed with byte permutes.
+        // Bank-conflict-free order: step r reads token 16 tg + (r ^ 2 tg) (the four token groups then
+        // sit on rows of different swizzle phase), and odd column groups write their columns in
+        // pairs swapped (the two column groups of a store phase then fill both halves of the bank
+        // line); the byte permute and the selects below undo both orders.
         const int tg = lane & 3, cg = lane >> 2;
         const int box = c >> 1, chunk = 4 * (c & 1) + (cg >> 1), off8 = (cg & 1) * 8;
+        const int xr = tg << 1;
+        const uint32_t bsel = (tg & 1) ? 0x1032u : 0x3210u;   // token k ^ 2 (tg & 1) -> byte k of a block
+        const bool bswap = (tg >> 1) != 0;                       // block i holds tokens 4 (i ^ (tg >> 1)) ..
+        const bool cswap = (cg & 1) != 0;
         for (int t = 0; t < n_tiles; ++t) {
           const int s = t % kStages, bb = t & 1;
           // the tile has landed, and buffer bb's last reader, P . C of tile t - 2, has finished
@@ -596,15 +615,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             break;
           }
           const uint8_t* src = smem + s * L::kStage + box * kCodeBox;
-          uint32_t a[16][2];                  // a[r]: the 8 codes of token 16 tg + r
+          uint32_t a[16][2];                  // a[r]: the 8 codes of token 16 tg + (r ^ 2 tg)
 #pragma unroll
           for (int r = 0; r < 16; ++r) {
-            const int tok = 16 * tg + r;
+            const int tok = 16 * tg + (r ^ xr);
             const uint2 v = *reinterpret_cast<const uint2*>(src + tok * 128 + ((chunk ^ (tok & 7)) * 16) + off8);
             a[r][0] = v.x;
             a[r][1] = v.y;
           }
-          uint32_t o[8][4];                   // o[col][i]: the codes of tokens 16 tg + 4 i .. + 3 in column col
+          uint32_t o[8][4];                   // o[col][i] byte k: token 16 tg + 4 (i ^ (tg >> 1)) + (k ^ 2 (tg & 1))
 #pragma unroll
           for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -619,21 +638,25 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
               o[4 * k + 3][i] = __byte_perm(t1, t3, 0x7632);
             }
           const int valid = min(kPage, t_end - (unit.page_begin + t) * kPage);
-          if (valid < kPage) {                // a partial last page: codes of rows past the context become 0
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int nv = min(4, max(0, valid - (16 * tg + 4 * i)));
-              const uint32_t keep = nv >= 4 ? 0xFFFFFFFFu : ((1u << (8 * nv)) - 1u);
-#pragma unroll
-              for (int col = 0; col < 8; ++col) o[col][i] &= keep;
-            }
-          }
           uint8_t* dst = smem + L::kOffCt + bb * kCtBytes;
 #pragma unroll
           for (int col = 0; col < 8; ++col) {
-            const int n = 64 * c + 8 * cg + col;
-            *reinterpret_cast<uint4*>(dst + n * 64 + ((tg ^ ((n >> 1) & 3)) * 16)) =
-                make_uint4(o[col][0], o[col][1], o[col][2], o[col][3]);
+            const int n = 64 * c + 8 * cg + (col ^ (cswap ? 1 : 0));   // the column this lane writes now
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {     // block i of the output: tokens 16 tg + 4 i .. + 3 in order
+              const uint32_t x0 = cswap ? o[col ^ 1][i] : o[col][i];
+              const uint32_t x1 = cswap ? o[col ^ 1][i ^ 1] : o[col][i ^ 1];
+              w[i] = __byte_perm(bswap ? x1 : x0, 0u, bsel);
+            }
+            if (valid < kPage) {              // a partial last page: codes of rows past the context become 0
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int nv = min(4, max(0, valid - (16 * tg + 4 * i)));
+                w[i] &= nv >= 4 ? 0xFFFFFFFFu : ((1u << (8 * nv)) - 1u);
+              }
+            }
+            *reinterpret_cast<uint4*>(dst + n * 64 + ((tg ^ ((n >> 1) & 3)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -688,13 +711,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             *reinterpret_cast<uint4*>(box + r * 128 + (((2 * p + 1) ^ (r & 7)) * 16)) = make_uint4(d.x, d.y, e.x, e.y);
           }
         } else {
-          // lane = (row 16 k + lane / 2, 16 codes 16 (lane % 2) ..) for k = 0..3
+          // lane = (row 16 k + lane / 2, 16 codes 16 (lane % 2) ..) for k = 0..3; the codes sit in
+          // the upper half of the box (or, with FP8 MMAs, in their own landing area)
           const int p = lane & 1;
           uint8_t* box = st + L::kRopeOff;
+          const uint8_t* codes = st + L::kRopeCodeOff;
           uint4 v[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            v[k] = *reinterpret_cast<const uint4*>(box + kRopeBytes / 2 + (16 * k + (lane >> 1)) * 32 + p * 16);
+            v[k] = *reinterpret_cast<const uint4*>(codes + (16 * k + (lane >> 1)) * 32 + p * 16);
           __syncwarp();
 #pragma unroll
           for (int k = 0; k < 4; ++k) {       // 64-byte rows, 64-byte swizzle
@@ -863,18 +888,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         l_g *= ex2_approx(m_g - m_new);       // 0 while this group has no sum yet
         m_g = m_new;
       }
-      uint32_t pk[32];
+      uint32_t pk[32];                        // P as bf16 pairs, or (FP8 MMAs) 16 words of 4 e4m3 codes
       float2 ps[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) ps[i] = zero2;
       const float2 negm2 = make_float2(-m_new, -m_new);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float2 d = __fadd2_rn(x2[i], negm2);
-        const float2 p = make_float2(ex2_approx(d.x), ex2_approx(d.y));
-        ps[i & 3] = __fadd2_rn(ps[i & 3], p);
-        if constexpr (kMma8) x2[i] = p;       // packed to e4m3 below
-        else pk[i] = bf16x2_bits(p.x, p.y);
+      for (int i = 0; i < 32; i += 2) {
+        const float2 d0 = __fadd2_rn(x2[i], negm2), d1 = __fadd2_rn(x2[i + 1], negm2);
+        const float2 p0 = make_float2(ex2_approx(d0.x), ex2_approx(d0.y));
+        const float2 p1 = make_float2(ex2_approx(d1.x), ex2_approx(d1.y));
+        ps[i & 3] = __fadd2_rn(ps[i & 3], p0);
+        ps[(i + 1) & 3] = __fadd2_rn(ps[(i + 1) & 3], p1);
+        if constexpr (kMma8) {
+          pk[i >> 1] = e4m3x4(p0.x, p0.y, p1.x, p1.y);
+        } else {
+          pk[i] = bf16x2_bits(p0.x, p0.y);
+          pk[i + 1] = bf16x2_bits(p1.x, p1.y);
+        }
       }
       {
         const float2 s2 = __fadd2_rn(__fadd2_rn(ps[0], ps[1]), __fadd2_rn(ps[2], ps[3]));
@@ -885,13 +916,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         // 16-byte chunk c at c ^ ((h >> 1) & 3)); its last reader, P . C of tile j - 2, is done
         uint8_t* prow = smem + L::kOffP8 + g * kP8Bytes + h * 64;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            w[q] = e4m3x4(x2[8 * c + 2 * q].x, x2[8 * c + 2 * q].y, x2[8 * c + 2 * q + 1].x, x2[8 * c + 2 * q + 1].y);
-          *reinterpret_cast<uint4*>(prow + ((c ^ ((h >> 1) & 3)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+        for (int c = 0; c < 4; ++c)            // 16 tokens per 16-byte chunk
+          *reinterpret_cast<uint4*>(prow + ((c ^ ((h >> 1) & 3)) * 16)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         fence_proxy_async_smem();            // generic writes before the tensor core reads them
       } else {
         tmem_st32(lane_addr + kTmP + 32 * g, pk);
@@ -1122,7 +1149,8 @@ cudaError_t launch_decode_tc(const Handle& h, const int32_t* ctx_len, int batch,
   if (e == cudaSuccess) e = make_query_tensor_map(ws.q_abs, batch, h.cfg.n_h, 32, &map_qpe);
   if (e == cudaSuccess) e = make_latent_out_tensor_map(ws.o_lat, batch, h.cfg.n_h, &map_o);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_tc_kernel<kMode>, dim3(2 * ws.max_units), dim3(kMode != kModeBf16 ? kThreadsFp8 : kThreads),
+  const int threads = kMode == kModeFp8Mma ? kThreadsFp8Mma : kMode != kModeBf16 ? kThreadsFp8 : kThreads;
+  return launch_pdl(decode_tc_kernel<kMode>, dim3(2 * ws.max_units), dim3(threads),
                     Smem<kMode>::kBytes, st, map, map_rope, map_scale, map_q, map_qpe, map_o,
                     ctx_len,
                     h.cfg.n_h, block_table, bt_stride, num_pages, scale_log2, cache_scale, h.test_stall,

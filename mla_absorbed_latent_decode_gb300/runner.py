@@ -23,7 +23,7 @@ def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
 
 class DecodeSession:
     def __init__(self, wl: Workload, device: str = "cuda", max_position: int | None = None,
-                 splits: int = 0, stream=None, fp8_mma: bool = False):
+                 splits: int = 0, stream=None, fp8_mma: bool | None = None):
         self.wl = wl
         self.device = torch.device(device)
         self.stream = stream
@@ -36,8 +36,8 @@ class DecodeSession:
         self.mla = B.Mla(self.config, self.w_uk, self.w_uv, stream)
         if splits:
             self.mla.set_option(B.MLA_OPT_SPLITS, splits)
-        if fp8_mma:
-            self.mla.set_option(B.MLA_OPT_FP8_MMA, 1)
+        if fp8_mma is not None:                 # None: the library's default (FP8 MMAs)
+            self.mla.set_option(B.MLA_OPT_FP8_MMA, int(fp8_mma))
         row_bytes = ROW_BYTES[wl.cache_dtype]
         self.cache = torch.full((wl.num_pages, wl.page_size, row_bytes), SENTINEL, dtype=torch.uint8,
                                 device=self.device)

@@ -17,7 +17,7 @@ from tests.mla_cases import (bf16_out_to_f64, compare, gpu_rows, oracle_decode, 
 pytestmark = pytest.mark.gpu
 
 
-def _check(wl, check_codes=True, fp8_mma=False):
+def _check(wl, check_codes=True, fp8_mma=None):
     s = DecodeSession(wl, fp8_mma=fp8_mma)
     s.prefill()
     rows, seq, pos = s.step_inputs()
@@ -64,9 +64,10 @@ def test_named_config(name):
     assert rel <= tolerance(wl), (name, rel, err, scale)
 
 
-def test_fp8_config_with_fp8_mma():
-    """The V3 B=128 x 4096 per-tensor FP8 configuration with both contractions on FP8 tensor cores
-    (MLA_OPT_FP8_MMA): e4m3 query (one scale per head and half) and e4m3 P."""
+def test_fp8_config_with_bf16_conversion():
+    """The V3 B=128 x 4096 per-tensor FP8 configuration on the other FP8 path (MLA_OPT_FP8_MMA = 0:
+    codes converted to bf16 in shared memory, bf16 contractions); the default, FP8 MMAs, is
+    test_named_config's."""
     wl = W.NAMED["v3_b128_s4096_fp8"]()
-    rel, err, scale = _check(wl, fp8_mma=True)
+    rel, err, scale = _check(wl, fp8_mma=False)
     assert rel <= tolerance(wl), (rel, err, scale)

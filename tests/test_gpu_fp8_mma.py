@@ -61,6 +61,18 @@ def test_fp8_mma_forced_rescale(n_h):
     s.close()
 
 
+@pytest.mark.parametrize("n_h", [16, 128])
+def test_conversion_path_matches_oracle_ragged(n_h):
+    """The other FP8 path (MLA_OPT_FP8_MMA = 0: codes converted to bf16 in shared memory)."""
+    wl = W.make_decode("fp8conv", 63 + n_h, n_h, RAGGED, cache_dtype=W.CACHE_FP8)
+    s, out, flags = _run(wl, fp8_mma=False)
+    assert flags == 0
+    ref = oracle_decode_paged(wl, oracle_values(wl, oracle_stored(wl)))
+    rel, err, scale = compare(out, ref, FP8_TOL)
+    assert rel <= FP8_TOL, (rel, err, scale)
+    s.close()
+
+
 def test_fp8_mma_and_conversion_paths_agree():
     """The two FP8 paths differ only by the e4m3 rounding of the query and of P."""
     wl = W.make_decode("fp8mmaab", 97, 128, [3000, 64, 257], cache_dtype=W.CACHE_FP8)
