@@ -173,8 +173,8 @@ mla_status_t mla_kv_append(mla_handle_t h, const void* rows, const int32_t* seq,
  * hidden state to the [d_c | d_rope] row; the kv norm is the identity here), each value the
  * bf16 rounding of an fp32 sum, is then stored exactly as mla_kv_append stores a row (same
  * slot, rotation, encoding and device checks): the bytes equal those of mla_project into a
- * rows buffer followed by mla_kv_append.  A per-block FP8 cache is MLA_ERR_UNSUPPORTED here
- * (its block scales need a whole row; use mla_project + mla_kv_append).
+ * rows buffer followed by mla_kv_append, for every cache format (with the per-block FP8
+ * cache a CTA projects whole rows, since a block's scale needs all 128 of its values).
  *
  *   x            device [n][hidden] bf16, 16-byte aligned.
  *   hidden       a positive multiple of 256.

@@ -285,8 +285,6 @@ mla_status_t mla_kv_project_append(mla_handle_t hh, const void* x, int32_t hidde
                 bt_rows, bt_stride, num_pages);
   if (!aligned(x, 16) || !aligned(w_dkv, 16) || !aligned(cache, 16))
     return fail(MLA_ERR_INVALID_ARG, "mla_kv_project_append: x, w_dkv and cache must be 16-byte aligned");
-  if (h->cfg.cache_dtype == MLA_CACHE_FP8_E4M3_BLOCK)
-    return fail(MLA_ERR_UNSUPPORTED, "mla_kv_project_append: the per-block FP8 cache is written by mla_kv_append only");
   cudaError_t e = mla::launch_kv_project_append(*h, static_cast<const __nv_bfloat16*>(x), n, hidden,
                                                 static_cast<const __nv_bfloat16*>(w_dkv), seq, pos, block_table,
                                                 bt_rows, bt_stride, cache, num_pages,

@@ -20,8 +20,6 @@
 namespace mla {
 namespace {
 
-enum AppendMode { kBf16 = 0, kFp8Tensor = 1, kFp8Block = 2 };
-
 template <int kMode>
 __global__ void __launch_bounds__(256) kv_append_kernel(
     const __nv_bfloat16* __restrict__ rows, const int32_t* __restrict__ seq,
@@ -44,66 +42,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     if (lane == 0) atomicOr(check, kCheckPageId);
     return;
   }
-  constexpr int kRowBytes = kMode == kBf16 ? kRow * 2 : kMode == kFp8Tensor ? kRow : kDc + 16 + 2 * kDr;
+  constexpr int kRowBytes = cache_row_bytes<kMode>();
   const uint4* src = reinterpret_cast<const uint4*>(rows + (size_t)warp * kRow);
   uint8_t* dst = cache + ((size_t)page * kPage + (p % kPage)) * (size_t)kRowBytes;
-
-  // latent: values [16 lane, 16 lane + 16)
-  const uint4 a = src[2 * lane];
-  const uint4 b = src[2 * lane + 1];
-  if (kMode == kBf16) {
-    reinterpret_cast<uint4*>(dst)[2 * lane] = a;
-    reinterpret_cast<uint4*>(dst)[2 * lane + 1] = b;
-  } else {
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    float scale = fp8_scale;
-    if (kMode == kFp8Block) {               // this lane's block: 128 values on lanes 8 k .. 8 k + 7
-      float m = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-#pragma unroll
-      for (int off = 4; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      scale = __fdiv_rn(m, 448.0f);
-      if ((lane & 7) == 0) reinterpret_cast<float*>(dst + kDc)[lane >> 3] = scale;
-    }
-    uint32_t o[4];
-    if (kMode == kFp8Block && !(scale > 0.0f)) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = 0u;   // an all-zero block: zero codes
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        o[i] = pack_e4m3x4(__fdiv_rn(bf16_lo(w[2 * i]), scale), __fdiv_rn(bf16_hi(w[2 * i]), scale),
-                           __fdiv_rn(bf16_lo(w[2 * i + 1]), scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), scale));
-    }
-    reinterpret_cast<uint4*>(dst)[lane] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-
-  // RoPE key: lanes 0..3 own values [16 lane, 16 lane + 16) = pairs [8 lane, 8 lane + 8)
-  if (lane < 4) {
-    const uint4 ra = src[kDc / 8 + 2 * lane];
-    const uint4 rb = src[kDc / 8 + 2 * lane + 1];
-    const uint32_t w[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
-    const float2* cs = rope_cs + (size_t)p * (kDr / 2) + 8 * lane;
-    float r[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) rope_pair(bf16_lo(w[i]), bf16_hi(w[i]), cs[i], &r[2 * i], &r[2 * i + 1]);
-    if (kMode != kFp8Tensor) {             // bf16, after the latent (and, per-block, the 16 scale bytes)
-      uint32_t o[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = pack_bf16(r[2 * i], r[2 * i + 1]);
-      uint4* d = reinterpret_cast<uint4*>(dst + (kMode == kBf16 ? kDc * 2 : kDc + 16));
-      d[2 * lane] = make_uint4(o[0], o[1], o[2], o[3]);
-      d[2 * lane + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-    } else {
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        o[i] = pack_e4m3x4(__fdiv_rn(r[4 * i], fp8_scale), __fdiv_rn(r[4 * i + 1], fp8_scale),
-                           __fdiv_rn(r[4 * i + 2], fp8_scale), __fdiv_rn(r[4 * i + 3], fp8_scale));
-      reinterpret_cast<uint4*>(dst + kDc)[lane] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
+  write_cache_row<kMode>(src, dst, p, lane, rope_cs, fp8_scale);
 }
 
 }  // namespace

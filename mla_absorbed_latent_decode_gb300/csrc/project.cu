@@ -1,8 +1,8 @@
 // project.cu -- the input and output projections around the absorbed decode, on the device:
 //
 //   kv rows   [c_kv | k_r] = x . W_DKV^T, then written into the paged cache exactly as
-//             mla_kv_append writes rows (latent copied or e4m3-encoded, RoPE key rotated at the
-//             token's position) -- "DeepSeek-V2-Lite 真实权重执行审计" §3.1: kv_a_proj_with_mqa
+//             mla_kv_append writes rows (latent copied or e4m3-encoded, per tensor or per block of
+//             128 values, RoPE key rotated at the token's position) -- "DeepSeek-V2-Lite 真实权重执行审计" §3.1: kv_a_proj_with_mqa
 //             maps a hidden state to the 512 + 64 row; kv_norm is the identity here;
 //   queries   q = x . W_Q^T, per head [q_nope | q_pe] ("80 行 PyTorch 从零写 DeepSeek 的 MLA" §2);
 //   output    y = o . W_O^T over the heads' concatenated values.
@@ -124,6 +124,44 @@ __global__ void __launch_bounds__(kPThreads) kv_project_append_kernel(
   }
 }
 
+// Per-block FP8 cache: a block's scale needs all 128 of its values, so a CTA projects whole rows.
+// It computes the 576 features of its kPTok rows in 36 passes of 16 (project_pair, as above, each
+// bf16-rounded into a shared-memory row), then one warp per row writes it as mla_kv_append does.
+__global__ void __launch_bounds__(kPThreads) kv_project_append_block_kernel(
+    const __nv_bfloat16* __restrict__ x, int n, int k, const __nv_bfloat16* __restrict__ w,
+    const int32_t* __restrict__ seq, const int32_t* __restrict__ pos, const int32_t* __restrict__ block_table,
+    int bt_rows, int bt_stride, uint8_t* __restrict__ cache, int num_pages, const float2* __restrict__ rope_cs,
+    int max_position, unsigned* check) {
+  __shared__ __align__(16) uint32_t rows_s[kPTok][kRow / 2];      // bf16 pairs of the CTA's rows
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kPTok, mt = min(kPTok, n - m0);
+  sm100::griddep_wait();
+  sm100::griddep_launch_dependents();
+  for (int f0 = 0; f0 < kRow; f0 += kPFeat) {
+    const int f = f0 + 2 * warp;
+    float acc[kPTok][2];
+    project_pair(x, m0, mt, w, k, f, lane, acc);
+#pragma unroll
+    for (int t = 0; t < kPTok; ++t)
+      if (t < mt && lane == t) rows_s[t][f / 2] = pack_bf16(acc[t][0], acc[t][1]);
+  }
+  __syncthreads();
+  for (int t = warp; t < mt; t += kPThreads / 32) {
+    const int s = seq[m0 + t], p = pos[m0 + t];
+    if (s < 0 || s >= bt_rows || p < 0 || p >= max_position || p / kPage >= bt_stride) {
+      if (lane == 0) atomicOr(check, kCheckAppend);
+      continue;
+    }
+    const int page = block_table[(size_t)s * bt_stride + p / kPage];
+    if (page < 0 || page >= num_pages) {
+      if (lane == 0) atomicOr(check, kCheckPageId);
+      continue;
+    }
+    uint8_t* dst = cache + ((size_t)page * kPage + (p % kPage)) * (size_t)cache_row_bytes<kFp8Block>();
+    write_cache_row<kFp8Block>(reinterpret_cast<const uint4*>(rows_s[t]), dst, p, lane, rope_cs, 0.0f);
+  }
+}
+
 // RMSNorm of a row (Zhang & Sennrich 2019): y = x / sqrt(mean(x^2) + eps) * w, the sum of squares
 // in fp32 (each lane over its 8-value chunks, then a shuffle tree), y = bf16((x * inv) * w).
 // One warp per row; a lane reads its chunks in both passes and writes only them, so y may be x.
@@ -179,6 +217,10 @@ cudaError_t launch_kv_project_append(const Handle& h, const __nv_bfloat16* x, in
                                      const __nv_bfloat16* w, const int32_t* seq, const int32_t* pos,
                                      const int32_t* block_table, int bt_rows, int bt_stride, void* cache,
                                      int num_pages, cudaStream_t st) {
+  if (h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3_BLOCK)
+    return launch_pdl(kv_project_append_block_kernel, dim3((n + kPTok - 1) / kPTok), dim3(kPThreads), 0, st, x, n, k,
+                      w, seq, pos, block_table, bt_rows, bt_stride, static_cast<uint8_t*>(cache), num_pages,
+                      (const float2*)h.rope_cs, h.cfg.max_position, h.check_word);
   const dim3 grid(kRow / kPFeat, (n + kPTok - 1) / kPTok);
   if (h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3)
     return launch_pdl(kv_project_append_kernel<true>, grid, dim3(kPThreads), 0, st, x, n, k, w, seq, pos,

@@ -95,12 +95,6 @@ def test_calls_without_the_format_refuse_it():
     wl = W.make_decode("blk_refuse", 46, 16, [10], cache_dtype=W.CACHE_FP8_BLOCK)
     s = DecodeSession(wl)
     dev = s.device
-    x = torch.zeros((1, 256), dtype=torch.bfloat16, device=dev)
-    w = torch.zeros((576, 256), dtype=torch.bfloat16, device=dev)
-    i = torch.zeros(1, dtype=torch.int32, device=dev)
-    with pytest.raises(B.MlaError) as e:
-        s.mla.kv_project_append(x, w, i, i, s.block_table, s.cache, wl.num_pages)
-    assert e.value.status == B.MLA_ERR_UNSUPPORTED
     with pytest.raises(B.MlaError) as e:
         s.mla.expand_kv(s.cache, wl.num_pages, torch.empty(16, dtype=torch.uint8, device=dev))
     assert e.value.status == B.MLA_ERR_UNSUPPORTED

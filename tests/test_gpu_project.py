@@ -45,18 +45,19 @@ def test_project_matches_float64(m, k, n_out):
     mla.close()
 
 
-@pytest.mark.parametrize("fp8", [False, True])
-def test_kv_project_append_writes_the_bytes_of_project_then_append(fp8):
-    rng = np.random.default_rng(11 + fp8)
+@pytest.mark.parametrize("cache", [W.CACHE_BF16, W.CACHE_FP8, W.CACHE_FP8_BLOCK])
+def test_kv_project_append_writes_the_bytes_of_project_then_append(cache):
+    rng = np.random.default_rng(11 + cache)
     n, hidden, num_pages, bt_stride = 70, 2048, 12, 4
     xb, wb = _bits(rng, (n, hidden), 1.0), _bits(rng, (576, hidden), 0.02)
-    mla = _handle(cache_dtype=W.CACHE_FP8 if fp8 else W.CACHE_BF16, fp8_scale=0.01 if fp8 else 0.0)
+    fp8 = cache == W.CACHE_FP8
+    mla = _handle(cache_dtype=cache, fp8_scale=0.01 if fp8 else 0.0)
     bt = torch.from_numpy(rng.permutation(num_pages)[:3 * bt_stride].astype(np.int32).reshape(3, bt_stride)).cuda()
     slots = rng.choice(3 * bt_stride * 64, size=n, replace=False)
     seq_np, pos_np = (slots // (bt_stride * 64)).astype(np.int32), (slots % (bt_stride * 64)).astype(np.int32)
     seq_np[5] = 3                                                   # outside the block table: skipped, flagged
     seq, pos = torch.from_numpy(seq_np).cuda(), torch.from_numpy(pos_np).cuda()
-    row_bytes = 576 * (1 if fp8 else 2)
+    row_bytes = W.ROW_BYTES[cache]
     fused = torch.full((num_pages, 64, row_bytes), SENTINEL, dtype=torch.uint8, device="cuda")
     split = fused.clone()
     x, w = bf16_tensor(xb, "cuda"), bf16_tensor(wb, "cuda")
