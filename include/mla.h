@@ -281,7 +281,9 @@ mla_status_t mla_prefill_workspace_size(mla_handle_t h, int32_t batch, int32_t m
  *   total_q      rows of q and out (>= 1).
  *   max_q        host bound on q_len, 1 <= max_q <= max_ctx (sets the grid).
  *   ctx_len, batch, max_ctx, block_table, bt_stride, num_pages: as in mla_decode.
- *   cache        device, a bf16 cache (an FP8 cache is MLA_ERR_UNSUPPORTED), 128-byte aligned.
+ *   cache        device, the handle's cache format, 128-byte aligned (an FP8 cache's values are
+ *                decoded -- codes times the tensor scale, or times their block's scale -- as the
+ *                expansion loads them).
  *   workspace    device, >= mla_prefill_workspace_size bytes, 256-byte aligned; overwritten.
  *   out          device [total_q][n_h][d_v] bf16, 32-byte aligned: row q_start[b] + i is the
  *                output of query i of sequence b; other rows are not written.

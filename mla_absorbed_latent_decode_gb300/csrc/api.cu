@@ -412,8 +412,6 @@ mla_status_t mla_prefill(mla_handle_t hh, const void* q, const int32_t* q_start,
   g_last_error.clear();
   Handle* h = reinterpret_cast<Handle*>(hh);
   if (!h) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: handle is NULL");
-  if (h->cfg.cache_dtype != MLA_CACHE_BF16)
-    return fail(MLA_ERR_UNSUPPORTED, "mla_prefill: only a bf16 cache is supported");
   if (batch <= 0) return fail(MLA_ERR_INVALID_ARG, "mla_prefill: batch = %d must be positive", batch);
   if (max_ctx <= 0 || max_ctx > h->cfg.max_position)
     return fail(MLA_ERR_INVALID_ARG, "mla_prefill: max_ctx = %d must be in [1, max_position=%d]", max_ctx,

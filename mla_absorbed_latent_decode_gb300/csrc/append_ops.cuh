@@ -1,7 +1,7 @@
-// append_ops.cuh -- the per-value operations of a cache write, shared by mla_kv_append and the
-// fused projection + append: bf16 unpacking and packing, e4m3 encoding (nearest even,
-// saturating), and the RoPE rotation of one interleaved pair with every product and sum
-// rounded to fp32.
+// append_ops.cuh -- the per-value operations of a cache write and read, shared by mla_kv_append,
+// the fused projection + append and the kernels that read an FP8 cache: bf16 unpacking and
+// packing, e4m3 encoding (nearest even, saturating) and exact decoding, the RoPE rotation of one
+// interleaved pair with every product and sum rounded to fp32, and the row write itself.
 #pragma once
 
 #include <cstdint>
@@ -31,6 +31,34 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 __device__ __forceinline__ void rope_pair(float x0, float x1, float2 cs, float* o0, float* o1) {
   *o0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
   *o1 = __fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y));
+}
+
+// FP8 cache: e4m3 -> bf16, exact, in integer and fp32 arithmetic (no conversion instruction):
+// the code's 7 magnitude bits placed at bit 20 of a float32, its sign at bit 31, make that
+// value times 2^-120 (a normal e4m3 keeps its exponent and mantissa fields; a subnormal one
+// becomes a float32 subnormal), so one multiply by 2^120 (denormals kept) gives the value; it
+// has at most 4 significant bits, so the upper 16 bits of the float32 are its bf16.  Code k of
+// the word is moved to bits 24..31, shifted arithmetically by 4 (the sign lands on bits 28..31)
+// and masked.  Output: bf16 of codes (0, 1) and (2, 3), low half first.
+__device__ __forceinline__ float e4m3_at_top_to_f32(uint32_t t) {
+  const uint32_t bits = (uint32_t)((int32_t)t >> 4) & 0x87F00000u;
+  float f;
+  asm("mul.rn.f32 %0, %1, 0f7B800000;" : "=f"(f) : "f"(__uint_as_float(bits)));   // x 2^120
+  return f;
+}
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
+  const float f0 = e4m3_at_top_to_f32(w << 24), f1 = e4m3_at_top_to_f32(w << 16);
+  const float f2 = e4m3_at_top_to_f32(w << 8), f3 = e4m3_at_top_to_f32(w);
+  return make_uint2(__byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632),
+                    __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632));
+}
+
+// Per-block FP8 cache: the exact values of four codes times their block scale, each product
+// rounded to fp32 and then to bf16 (nearest even); low half first, as above.
+__device__ __forceinline__ uint2 e4m3x4_scaled_to_bf16x4(uint32_t w, float scale) {
+  const float f0 = e4m3_at_top_to_f32(w << 24) * scale, f1 = e4m3_at_top_to_f32(w << 16) * scale;
+  const float f2 = e4m3_at_top_to_f32(w << 8) * scale, f3 = e4m3_at_top_to_f32(w) * scale;
+  return make_uint2(pack_bf16(f0, f1), pack_bf16(f2, f3));
 }
 
 // cache formats of a row write: bf16, e4m3 with one tensor scale, per-block e4m3 (656 bytes)

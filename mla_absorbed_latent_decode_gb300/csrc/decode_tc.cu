@@ -55,6 +55,7 @@
 
 #include <cuda_fp16.h>
 
+#include "append_ops.cuh"
 #include "internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -190,34 +191,6 @@ __device__ __forceinline__ float max64(const float2 (&x2)[32]) {
 
 __device__ __forceinline__ void fail_timeout(Bars* bars, unsigned* check) {
   if (atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
-}
-
-// FP8 cache: e4m3 -> bf16, exact, in integer and fp32 arithmetic (no conversion instruction):
-// the code's 7 magnitude bits placed at bit 20 of a float32, its sign at bit 31, make that
-// value times 2^-120 (a normal e4m3 keeps its exponent and mantissa fields; a subnormal one
-// becomes a float32 subnormal), so one multiply by 2^120 (denormals kept) gives the value; it
-// has at most 4 significant bits, so the upper 16 bits of the float32 are its bf16.  Code k of
-// the word is moved to bits 24..31, shifted arithmetically by 4 (the sign lands on bits 28..31)
-// and masked.  Output: bf16 of codes (0, 1) and (2, 3), low half first.
-__device__ __forceinline__ float e4m3_at_top_to_f32(uint32_t t) {
-  const uint32_t bits = (uint32_t)((int32_t)t >> 4) & 0x87F00000u;
-  float f;
-  asm("mul.rn.f32 %0, %1, 0f7B800000;" : "=f"(f) : "f"(__uint_as_float(bits)));   // x 2^120
-  return f;
-}
-__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
-  const float f0 = e4m3_at_top_to_f32(w << 24), f1 = e4m3_at_top_to_f32(w << 16);
-  const float f2 = e4m3_at_top_to_f32(w << 8), f3 = e4m3_at_top_to_f32(w);
-  return make_uint2(__byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632),
-                    __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632));
-}
-
-// Per-block FP8 cache: the exact values of four codes times their block scale, each product
-// rounded to fp32 and then to bf16 (nearest even); low half first, as above.
-__device__ __forceinline__ uint2 e4m3x4_scaled_to_bf16x4(uint32_t w, float scale) {
-  const float f0 = e4m3_at_top_to_f32(w << 24) * scale, f1 = e4m3_at_top_to_f32(w << 16) * scale;
-  const float f2 = e4m3_at_top_to_f32(w << 8) * scale, f3 = e4m3_at_top_to_f32(w) * scale;
-  return make_uint2(bf16x2_bits(f0, f1), bf16x2_bits(f2, f3));
 }
 
 // kMode != bf16: the cache holds e4m3 codes.  The producer TMA-loads each 64 x 64 code box into the

@@ -9,7 +9,8 @@
 //
 //   1. expand_tc_kernel: for every cached row t of a sequence and head h,
 //        K_nope[b][h][t] = W_UK[h] c_t,   V[b][h][t] = W_UV[h] c_t     (bf16),
-//      and the (already rotated) RoPE key K_r[b][t] copied once per token;
+//      and the (already rotated) RoPE key K_r[b][t] copied once per token (an FP8 cache's values
+//      decoded: codes times the tensor scale, or times their block's scale);
 //      item = (head, 128 tokens): D[128 tokens][256] = C[128][512] . [W_UK[h] ; W_UV[h]]^T,
 //      A = two cache pages by TMA, B = the head's weight rows, K-major, 4-stage ring;
 //      persistent CTAs, two TMEM accumulators (the epilogue of an item under the next's MMAs).
@@ -42,13 +43,30 @@ constexpr int kTile = 128;             // tokens of an expansion tile = keys of 
 constexpr int kQBlk = 128;             // queries of an attention CTA
 
 // ------------------------------------------------------------------ expansion
+// cache formats: bf16 rows; e4m3 rows with one tensor scale; per-block e4m3 rows (656 bytes: 512
+// codes, 4 fp32 block scales, 64 bf16 RoPE values).  With an FP8 cache each page's 64 x 64 code
+// box lands in the upper half of its bf16 box and one conversion warp per page turns it into the
+// bf16 operand in place (exact values; per block: times the token's block scale, rounded to bf16);
+// the tensor scale is applied in the epilogue, in fp32.
+constexpr int kExBf16 = 0, kExFp8 = 1, kExFp8Block = 2;
 constexpr int kExStages = 4;
-constexpr int kExStageBytes = 2 * kPageBox + 2 * kBox;      // two pages x 64 columns, W_UK and W_UV boxes
-constexpr int kExThreads = 192;                              // warps 0-3 epilogue, 4 producer, 5 MMA
-constexpr int kExSmem = kExStages * kExStageBytes + 1024 + 1024;
+constexpr int kExScaleBytes = kPage * 16;                    // per-block format: 64 tokens x 4 fp32 scales
+template <int kMode>
+__host__ __device__ constexpr int ex_stage_bytes() {                             // two pages x 64 columns, W_UK and W_UV boxes
+  return 2 * kPageBox + 2 * kBox + (kMode == kExFp8Block ? 2 * kExScaleBytes : 0);
+}
+template <int kMode>
+__host__ __device__ constexpr int ex_threads() {                                 // warps 0-3 epilogue, 4 producer, 5 MMA, 6-7 conversion
+  return kMode == kExBf16 ? 192 : 256;
+}
+template <int kMode>
+__host__ __device__ constexpr int ex_smem() {
+  return kExStages * ex_stage_bytes<kMode>() + 1024 + 1024;
+}
 
 struct ExBars {
   uint64_t full[kExStages];
+  uint64_t conv[kExStages];    // FP8 cache: both pages of the chunk converted (2 warps)
   uint64_t empty[kExStages];
   uint64_t acc_full[2];      // the MMAs of an item are done: its accumulator may be read
   uint64_t acc_empty[2];     // the epilogue has read the accumulator (4 warps arrive)
@@ -98,24 +116,30 @@ __device__ __forceinline__ ExItem ex_item(int idx, int n_h, int ntb, const int32
 // Persistent: CTA c takes items c, c + gridDim.x, ...; the K-chunk ring runs on across items and
 // the accumulator alternates between two 256-column TMEM halves, so the epilogue of one item
 // overlaps the loads and MMAs of the next.
-__global__ void __launch_bounds__(kExThreads, 1)
+template <int kMode>
+__global__ void __launch_bounds__(ex_threads<kMode>(), 1)
 expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_wuk,
-                 const __grid_constant__ CUtensorMap tm_wuv, const __nv_bfloat16* __restrict__ cache,
+                 const __grid_constant__ CUtensorMap tm_wuv, const __grid_constant__ CUtensorMap tm_scale,
+                 const uint8_t* __restrict__ cache, float cache_scale,
                  const int32_t* __restrict__ ctx_len, int n_h, int max_ctx, const int32_t* __restrict__ block_table,
                  int bt_stride, int num_pages, int lpad, int n_items, __nv_bfloat16* __restrict__ kn,
                  __nv_bfloat16* __restrict__ vv, __nv_bfloat16* __restrict__ kr, int* sched, int stall,
                  unsigned* check) {
+  constexpr bool kFp8 = kMode != kExBf16;
+  constexpr int kStageB = ex_stage_bytes<kMode>();
+  constexpr int kRowB = kMode == kExBf16 ? kRow * 2 : kMode == kExFp8 ? kRow : kDc + 16 + 2 * kDr;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(smem);
-  ExBars* bars = reinterpret_cast<ExBars*>(smem + kExStages * kExStageBytes);
+  ExBars* bars = reinterpret_cast<ExBars*>(smem + kExStages * kStageB);
   volatile int* abort_flag = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntb = lpad / kTile;
   if (tid == 0) {
     for (int i = 0; i < kExStages; ++i) {
       mbar_init(smem_u32(&bars->full[i]), 1);
+      mbar_init(smem_u32(&bars->conv[i]), 2);
       mbar_init(smem_u32(&bars->empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -141,23 +165,30 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       prefetch_tmap(&tm_cache);
+      if (kMode == kExFp8Block) prefetch_tmap(&tm_scale);
       int c = 0;                           // K chunks issued so far (ring position)
       bool ok = true;
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
         const ExItem it = ex_item(idx, n_h, ntb, ctx_len, max_ctx, block_table, bt_stride, num_pages);
         if (!it.valid) continue;
         if (it.h == 0 && (!it.ok0 || (it.t0 + kPage < it.L && !it.ok1))) atomicOr(check, kCheckPageId);
-        const uint32_t bytes = (it.ok0 ? kPageBox : 0) + (it.ok1 ? kPageBox : 0) + 2 * kBox;
+        constexpr uint32_t kPageTx = kMode == kExBf16 ? kPageBox : kPageBox / 2 + (kMode == kExFp8Block ? kExScaleBytes : 0);
+        const uint32_t bytes = (it.ok0 ? kPageTx : 0) + (it.ok1 ? kPageTx : 0) + 2 * kBox;
         for (int kc = 0; kc < kDc / 64; ++kc, ++c) {
           const int s = c % kExStages;
           if (c >= kExStages && !mbar_wait(smem_u32(&bars->empty[s]), ((c / kExStages) - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
-          const uint32_t st = sbase + s * kExStageBytes, fb = smem_u32(&bars->full[s]);
+          const uint32_t st = sbase + s * kStageB, fb = smem_u32(&bars->full[s]);
           mbar_arrive_expect_tx(fb, bytes);
-          if (it.ok0) tma_load_2d(st, &tm_cache, 64 * kc, it.p0 * kPage, fb);
-          if (it.ok1) tma_load_2d(st + kPageBox, &tm_cache, 64 * kc, it.p1 * kPage, fb);
+          // (an FP8 page's codes into the upper half of its bf16 box; per block, its scales after the weights)
+          if (it.ok0) tma_load_2d(st + (kFp8 ? kPageBox / 2 : 0), &tm_cache, 64 * kc, it.p0 * kPage, fb);
+          if (it.ok1) tma_load_2d(st + kPageBox + (kFp8 ? kPageBox / 2 : 0), &tm_cache, 64 * kc, it.p1 * kPage, fb);
+          if (kMode == kExFp8Block) {
+            if (it.ok0) tma_load_2d(st + 2 * kPageBox + 2 * kBox, &tm_scale, kDc, it.p0 * kPage, fb);
+            if (it.ok1) tma_load_2d(st + 2 * kPageBox + 2 * kBox + kExScaleBytes, &tm_scale, kDc, it.p1 * kPage, fb);
+          }
           tma_load_2d(st + 2 * kPageBox, &tm_wuk, 64 * kc, kDn * it.h, fb);
           // (a test of the bounded waits, stall == 4: CTA 0 never loads the W_UV box of its first
           // chunk, so that stage's barrier, armed for every byte, cannot complete)
@@ -187,9 +218,12 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
         tc_fence_after();
         for (int kc = 0; kc < kDc / 64; ++kc, ++c) {
           const int s = c % kExStages;
-          if (!mbar_wait(smem_u32(&bars->full[s]), (c / kExStages) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(kFp8 ? &bars->conv[s] : &bars->full[s]), (c / kExStages) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t st = sbase + s * kExStageBytes;
+          const uint32_t st = sbase + s * kStageB;
           const uint64_t ad = sdesc_sw128(st, 16, 1024), wd = sdesc_sw128(st + 2 * kPageBox, 16, 1024);
 #pragma unroll
           for (int k = 0; k < 4; ++k)        // 16 latent columns per MMA: 32-byte steps in the 128-byte row
@@ -204,6 +238,56 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
       mma_commit(smem_u32(&bars->drain));    // every issued MMA has finished ...
       volatile int never = 0;
       mbar_wait(smem_u32(&bars->drain), 0, &never);   // ... before the CTA frees its TMEM
+    }
+  } else if (warp >= 6) {
+    // ---------------------------------------------------------------- FP8 cache: codes -> bf16
+    // (launched only with an FP8 cache) warp 6 + q converts page q of every chunk: lane = (row
+    // 8 k + lane / 4, 16 codes 16 (lane % 4) ..) for k = 0..7; all of the box's codes are read
+    // into registers before any bf16 row is written (the rows overlap the codes)
+    if constexpr (kFp8) {
+      const int q = warp - 6, pw = lane & 3;
+      int c = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+        const ExItem it = ex_item(idx, n_h, ntb, ctx_len, max_ctx, block_table, bt_stride, num_pages);
+        if (!it.valid) continue;
+        const bool loaded = q == 0 ? it.ok0 : it.ok1;
+        for (int kc = 0; kc < kDc / 64; ++kc, ++c) {
+          const int s = c % kExStages;
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[s]), (c / kExStages) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          uint8_t* box = smem + s * kStageB + q * kPageBox;
+          if (loaded) {
+            uint4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              v[k] = *reinterpret_cast<const uint4*>(box + kPageBox / 2 + (8 * k + (lane >> 2)) * 64 + pw * 16);
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {       // 128-byte rows, 128-byte swizzle
+              const int r = 8 * k + (lane >> 2);
+              uint2 a, b, d, e;
+              if constexpr (kMode == kExFp8Block) {   // times the token's scale of block kc / 2
+                const float sc = reinterpret_cast<const float*>(smem + s * kStageB + 2 * kPageBox + 2 * kBox +
+                                                                q * kExScaleBytes)[r * 4 + (kc >> 1)];
+                a = e4m3x4_scaled_to_bf16x4(v[k].x, sc); b = e4m3x4_scaled_to_bf16x4(v[k].y, sc);
+                d = e4m3x4_scaled_to_bf16x4(v[k].z, sc); e = e4m3x4_scaled_to_bf16x4(v[k].w, sc);
+              } else {
+                a = e4m3x4_to_bf16x4(v[k].x); b = e4m3x4_to_bf16x4(v[k].y);
+                d = e4m3x4_to_bf16x4(v[k].z); e = e4m3x4_to_bf16x4(v[k].w);
+              }
+              *reinterpret_cast<uint4*>(box + r * 128 + (((2 * pw) ^ (r & 7)) * 16)) = make_uint4(a.x, a.y, b.x, b.y);
+              *reinterpret_cast<uint4*>(box + r * 128 + (((2 * pw + 1) ^ (r & 7)) * 16)) = make_uint4(d.x, d.y, e.x, e.y);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->conv[s]));
+        }
+      }
+      if (!ok && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
     }
   } else {
     // ---------------------------------------------------------------- epilogue: thread = token
@@ -232,7 +316,9 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
           uint32_t w[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            w[e] = row_ok ? bf16x2(__uint_as_float(x[16 * i + 2 * e]), __uint_as_float(x[16 * i + 2 * e + 1])) : 0u;
+            w[e] = row_ok ? bf16x2(__uint_as_float(x[16 * i + 2 * e]) * cache_scale,
+                                   __uint_as_float(x[16 * i + 2 * e + 1]) * cache_scale)
+                          : 0u;
           st_global_32B(d + 2 * i, w);
         }
       }
@@ -242,10 +328,22 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_cons
       if (it.h == 0) {                       // the RoPE key, shared by the heads, once per token
         uint4* d = reinterpret_cast<uint4*>(kr + ((size_t)it.b * lpad + t) * kDr);
         if (row_ok) {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              cache + ((size_t)(r < kPage ? it.p0 : it.p1) * kPage + (r & (kPage - 1))) * kRow + kDc);
+          const uint8_t* row = cache + ((size_t)(r < kPage ? it.p0 : it.p1) * kPage + (r & (kPage - 1))) * kRowB;
+          if constexpr (kMode == kExFp8) {    // 64 codes times the tensor scale
+            const uint4* src = reinterpret_cast<const uint4*>(row + kDc);
 #pragma unroll
-          for (int i = 0; i < kDr / 8; ++i) d[i] = src[i];
+            for (int i = 0; i < kDr / 16; ++i) {
+              const uint4 v = src[i];
+              const uint2 a = e4m3x4_scaled_to_bf16x4(v.x, cache_scale), b = e4m3x4_scaled_to_bf16x4(v.y, cache_scale);
+              const uint2 g = e4m3x4_scaled_to_bf16x4(v.z, cache_scale), f = e4m3x4_scaled_to_bf16x4(v.w, cache_scale);
+              d[2 * i] = make_uint4(a.x, a.y, b.x, b.y);
+              d[2 * i + 1] = make_uint4(g.x, g.y, f.x, f.y);
+            }
+          } else {                            // bf16 after the latent (per block: after its scales too)
+            const uint4* src = reinterpret_cast<const uint4*>(row + (kMode == kExBf16 ? kDc * 2 : kDc + 16));
+#pragma unroll
+            for (int i = 0; i < kDr / 8; ++i) d[i] = src[i];
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < kDr / 8; ++i) d[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -833,7 +931,13 @@ cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_star
                            cudaStream_t st, cudaEvent_t between) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(expand_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kExSmem);
+    cudaError_t e = cudaFuncSetAttribute(expand_tc_kernel<kExBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         ex_smem<kExBf16>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(expand_tc_kernel<kExFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, ex_smem<kExFp8>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(expand_tc_kernel<kExFp8Block>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               ex_smem<kExFp8Block>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtSmem);
     if (e != cudaSuccess) return e;
@@ -852,11 +956,24 @@ cudaError_t launch_prefill(const Handle& h, const void* q, const int32_t* q_star
   if ((e = rows_map_2d(vv, (long long)batch * n_h * lpad, kDv, &tm_v)) != cudaSuccess) return e;
   if ((e = rows_map_2d(kr, (long long)batch * lpad, kDr, &tm_kr)) != cudaSuccess) return e;
   const int n_items = n_h * (lpad / kTile) * batch;
-  e = launch_pdl(expand_tc_kernel, dim3(min(n_items, h.num_sms)), dim3(kExThreads), kExSmem, st,
-                 *reinterpret_cast<const CUtensorMap*>(h.tmap), *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk),
-                 *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv), static_cast<const __nv_bfloat16*>(cache), ctx_len,
-                 n_h, max_ctx, block_table, bt_stride, num_pages, lpad, n_items, kn, vv, kr, sched, h.test_stall,
-                 h.check_word);
+  const CUtensorMap& tm_cache = *reinterpret_cast<const CUtensorMap*>(h.tmap);
+  const CUtensorMap& tm_wuk = *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk);
+  const CUtensorMap& tm_wuv = *reinterpret_cast<const CUtensorMap*>(h.tmap_wuv);
+  const CUtensorMap& tm_scale = *reinterpret_cast<const CUtensorMap*>(h.tmap_scale);
+  const uint8_t* cache8 = static_cast<const uint8_t*>(cache);
+  const dim3 ex_grid(min(n_items, h.num_sms));
+  if (h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3)
+    e = launch_pdl(expand_tc_kernel<kExFp8>, ex_grid, dim3(ex_threads<kExFp8>()), ex_smem<kExFp8>(), st, tm_cache,
+                   tm_wuk, tm_wuv, tm_scale, cache8, h.cfg.fp8_scale, ctx_len, n_h, max_ctx, block_table, bt_stride,
+                   num_pages, lpad, n_items, kn, vv, kr, sched, h.test_stall, h.check_word);
+  else if (h.cfg.cache_dtype == MLA_CACHE_FP8_E4M3_BLOCK)
+    e = launch_pdl(expand_tc_kernel<kExFp8Block>, ex_grid, dim3(ex_threads<kExFp8Block>()), ex_smem<kExFp8Block>(), st,
+                   tm_cache, tm_wuk, tm_wuv, tm_scale, cache8, 1.0f, ctx_len, n_h, max_ctx, block_table, bt_stride,
+                   num_pages, lpad, n_items, kn, vv, kr, sched, h.test_stall, h.check_word);
+  else
+    e = launch_pdl(expand_tc_kernel<kExBf16>, ex_grid, dim3(ex_threads<kExBf16>()), ex_smem<kExBf16>(), st, tm_cache,
+                   tm_wuk, tm_wuv, tm_scale, cache8, 1.0f, ctx_len, n_h, max_ctx, block_table, bt_stride, num_pages,
+                   lpad, n_items, kn, vv, kr, sched, h.test_stall, h.check_word);
   if (e != cudaSuccess) return e;
   if (between && (e = cudaEventRecord(between, st)) != cudaSuccess) return e;   // profiling: splits the two kernels
   const float scale_log2 = h.scale * 1.4426950408889634f;

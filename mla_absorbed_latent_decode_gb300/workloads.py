@@ -171,12 +171,12 @@ def _finish_decode(rng, name, seed, n_h, ctx_len, cache_dtype, shuffle, spare_pa
 # the five named workloads
 # ---------------------------------------------------------------------------
 
-def make_prefill(name, seed, n_h, ctx_len, q_len=None, *, q_std=1.0) -> Workload:
+def make_prefill(name, seed, n_h, ctx_len, q_len=None, *, q_std=1.0, cache_dtype=CACHE_BF16) -> Workload:
     """Prefill inputs: a decode workload's cache rows, weights and paged layout (same draws as
     ``make_decode``), plus query rows for the last ``q_len[b]`` positions of every sequence
     (every position when ``q_len`` is None), packed [total_q][n_h][d_nope + d_rope] in
     sequence order and drawn from a second stream of the same seed."""
-    wl = make_decode(name, seed, n_h, ctx_len)
+    wl = make_decode(name, seed, n_h, ctx_len, cache_dtype=cache_dtype)
     ql = wl.ctx_len.copy() if q_len is None else np.asarray(q_len, np.int32)
     rng = np.random.default_rng([seed, 1])
     q = _normal_bf16(rng, (int(np.sum(ql.astype(np.int64))), n_h, D_NOPE + D_ROPE), q_std)

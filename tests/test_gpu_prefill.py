@@ -10,7 +10,8 @@ from mla_absorbed_latent_decode_gb300 import binding as B
 from mla_absorbed_latent_decode_gb300 import workloads as W
 from mla_absorbed_latent_decode_gb300.runner import DecodeSession, bf16_tensor
 from oracle import mla_ref
-from tests.mla_cases import BF16_TOL, bf16_out_to_f64, compare, force_prefill_rescale, oracle_stored, oracle_values
+from tests.mla_cases import (BF16_TOL, FP8_TOL, bf16_out_to_f64, compare, force_prefill_rescale, oracle_stored,
+                             oracle_values)
 
 pytestmark = pytest.mark.gpu
 
@@ -70,6 +71,31 @@ def test_prefill_matches_the_oracle(case):
             continue
         err = compare(out[a:a + n], ref, BF16_TOL)
         assert err[0] <= BF16_TOL, (b, err)
+    s.close()
+
+
+FP8_CASES = {
+    "chunks_and_whole_prompts_16h": (16, [1, 200, 515, 130], [1, 77, 515, 129]),
+    "whole_prompts_128h": (128, [130, 257], None),
+}
+
+
+@pytest.mark.parametrize("cache", [W.CACHE_FP8, W.CACHE_FP8_BLOCK])
+@pytest.mark.parametrize("case", sorted(FP8_CASES))
+def test_prefill_over_an_fp8_cache_matches_the_oracle(case, cache):
+    """An FP8 cache (one tensor scale, or the per-block format) against the oracle on its own
+    dequantised cache: the expansion decodes the codes exactly (times the tensor or block scale)."""
+    n_h, ctx, ql = FP8_CASES[case]
+    wl = W.make_prefill("prefill8_" + case, 73, n_h, ctx, ql, cache_dtype=cache)
+    s = DecodeSession(wl)
+    s.append_rows()
+    out = bf16_out_to_f64(_prefill(s, wl))
+    assert s.status() == 0
+    p = wl.extra["prefill"]
+    for b, ref in _oracle(wl).items():
+        a, n = int(p["q_start"][b]), int(p["q_len"][b])
+        err = compare(out[a:a + n], ref, FP8_TOL)
+        assert err[0] <= FP8_TOL, (b, err)
     s.close()
 
 
