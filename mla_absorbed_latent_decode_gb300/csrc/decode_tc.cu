@@ -251,6 +251,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     mbar_init(smem_u32(&bars->qfull), 1);
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->drain[i]), 1);
     bars->abort = 0;
+    // the first phase of every receive quarter (tiles 0..3) armed now, so that the cluster barrier
+    // below also publishes it; later tiles are armed four tiles ahead, as each slot is consumed.
+    // (A phase armed for a tile the unit does not have never completes and is never waited on.)
+    for (int i = 0; i < kSlots; ++i)
+      for (int q = 0; q < 4; ++q) mbar_arrive_expect_tx(smem_u32(&bars->recvfull[i][q]), 32 * 128);
     fence_mbar_init();
   }
   if (warp == kWarpProducer && lane == 0) {
@@ -262,6 +267,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     prefetch_tmap(&tmap_o);
   }
   __syncthreads();
+  // the peer's barriers are initialised (and its first receive phases armed) before any copy into
+  // this CTA: a cluster barrier, taken before the dependency wait so that it overlaps the previous
+  // kernel (taken after the query's arrival it cost ~1 us on every CTA's critical path)
+  cluster_sync();
   griddep_wait();                           // plan, absorbed queries and cache rows are inputs
   griddep_launch_dependents();
   // (the unit record is read together with the unit count: the grid never exceeds the workspace's units)
@@ -342,11 +351,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   if (warp < 8) {
     const int q4 = warp & 3, half = warp >> 2;
     const int h = q4 * 32 + lane;
-    // this warp's receive quarter of its group's tiles 0..3 (tile j lands in slot j % 4); later
-    // tiles are armed four tiles ahead, as each slot is consumed
-    if (lane == 0)
-      for (int jj = half; jj < min(n_tiles, kSlots); jj += 2)
-        mbar_arrive_expect_tx(smem_u32(&bars->recvfull[jj][q4]), 32 * 128);
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
     const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->qfull), 0, abort_flag));
     if (!landed) fail_timeout(bars, check);
@@ -423,7 +427,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();              // peer barriers initialised before any copy into this CTA
   tc_fence_after();
 
   if (warp == kWarpProducer) {
