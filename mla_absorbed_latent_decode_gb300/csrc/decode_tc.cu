@@ -141,6 +141,8 @@ struct Bars {                               // mbarriers (8 bytes each) and flag
   uint32_t tmem_base;
   int abort;
   int peer_sent[8];                         // written by the peer: partial-score copies its group warp w sent here
+  int peer_consumed[8];                     // written by the peer: copies its group warp w received from here
+  int sent[8];                              // copies group warp w of this CTA sent to the peer
   int consumed[8];                          // copies group warp w of this CTA received and read
 };
 static_assert(sizeof(Bars) <= 1024, "barrier block");
@@ -905,10 +907,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       if (lane == 0) mbar_arrive(smem_u32(&bars->pfull[g]));
     }
     if (!ok) fail_timeout(bars, check);
-    // tell the peer how many copies this warp sent into it (read after the first cluster barrier below)
+    // tell the peer how many copies this warp sent into it and received from it (read after the
+    // first cluster barrier below)
     if (lane == 0) {
-      const uint32_t dst = map_to_rank(smem_u32(&bars->peer_sent[warp]), peer);
-      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst), "r"(sent) : "memory");
+      const uint32_t dst_s = map_to_rank(smem_u32(&bars->peer_sent[warp]), peer);
+      const uint32_t dst_c = map_to_rank(smem_u32(&bars->peer_consumed[warp]), peer);
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst_s), "r"(sent) : "memory");
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst_c), "r"(consumed) : "memory");
+      bars->sent[warp] = sent;
+      bars->consumed[warp] = consumed;
     }
     // ---- epilogue: reconcile the two groups' sums; group g writes latent columns
     // [128 g, 128 g + 128) of this CTA's half of every head
@@ -962,34 +969,42 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         if (lane == 0 && 32 * q4 < n_h) {
           for (int bx = 0; bx < 2; ++bx)
             tma_store_3d(&tmap_o, smem_u32(ob + bx * 4096), (int)(rank * 256 + 128 * g + 64 * bx), 32 * q4, b);
-          bulk_commit_group();
-          bulk_wait_read();                   // the staging read before the CTA may exit (the writes
-                                              // complete with the grid)
+          bulk_commit_group();                // (its staging read is awaited at exit)
         }
       }
       if (live && unit.part >= 0 && rank == 0 && g == 0)
         ws.part_lse[(size_t)unit.part * n_h + h] = (m_fin + log2f(l_sum)) * 0.69314718055994531f;
     }
-    bars->consumed[warp] = consumed;
   }
   tc_fence_before();
   __syncthreads();
   // Every copy either CTA will ever send has been issued and its count published.  A copy
-  // completes only on its receiver's barrier, so each receiving warp waits there for every copy
-  // the peer sent it but it did not consume (none in normal operation; after a timeout, the ones
-  // in flight) before the cluster may exit and its shared memory be reused.
+  // completes only on its receiver's barrier, and its source is this CTA's shared memory.  When
+  // every copy sent either way was received (normal operation) none is in flight and the CTAs
+  // may exit after this barrier.  Otherwise (after a timeout) each receiving warp waits for the
+  // copies the peer sent it but it did not consume, and a second barrier keeps both CTAs, and so
+  // the copies' sources and destinations, alive until then.  Both CTAs decide alike: each holds
+  // the same four counts per warp pair.
   cluster_sync();
-  if (warp < 8 && lane == 0) {
-    const int g = warp >> 2, q4 = warp & 3;
-    volatile int never = 0;
-    const int n_sent = bars->peer_sent[warp];
-    for (int c = bars->consumed[warp]; c < n_sent; ++c) {
-      const int j = g + 2 * c;
-      mbar_wait<true>(smem_u32(&bars->recvfull[j & (kSlots - 1)][q4]), (j >> 2) & 1, &never);
+  bool all_received = true;
+#pragma unroll
+  for (int w = 0; w < 8; ++w)
+    all_received &= bars->consumed[w] == bars->peer_sent[w] && bars->peer_consumed[w] == bars->sent[w];
+  if (!all_received) {
+    if (warp < 8 && lane == 0) {
+      const int g = warp >> 2, q4 = warp & 3;
+      volatile int never = 0;
+      const int n_sent = bars->peer_sent[warp];
+      for (int c = bars->consumed[warp]; c < n_sent; ++c) {
+        const int j = g + 2 * c;
+        mbar_wait<true>(smem_u32(&bars->recvfull[j & (kSlots - 1)][q4]), (j >> 2) & 1, &never);
+      }
     }
+    __syncthreads();
+    cluster_sync();
   }
-  __syncthreads();
-  cluster_sync();
+  if (warp < 8 && lane == 0) bulk_wait_read();   // the output staging read before the CTA exits
+                                                 // (the writes complete with the grid)
   if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
