@@ -619,6 +619,9 @@ def run_ours(args):
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s (latent KV)", "ms_per_step": round(e2e, 5),
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "mode": E2E_MODE,
+                    "l2": (f"not flushed between pipelined steps (a flush would serialise the copies); each step "
+                           f"reads {wl.total_tokens * cache_bytes_per_token(wl) >> 20} MiB of cache, more than L2; "
+                           f"serial_ms_per_step flushes L2 before every step"),
                     "serial_ms_per_step": round(e2e_serial, 5)},
             "gpu_launches": args.steps * ((2 if layer else 1) + len(kernel_ms[0])),
             "clocks": clock_info,

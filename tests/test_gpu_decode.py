@@ -97,6 +97,21 @@ def test_plan_is_bit_exact(forced):
     s.close()
 
 
+@pytest.mark.parametrize("batch,splits", [(256, 0), (257, 0), (300, 3)])
+def test_large_batches_match_oracle(batch, splits):
+    """Batches of more sequences than SM pairs, short ragged contexts: the planner's page-count
+    arrays span several of its passes over the batch, and forced splits (three per sequence of
+    three pages or more) number hundreds of partial slots."""
+    lens = np.random.default_rng(batch).integers(1, 200, size=batch).tolist()
+    wl = W.make_decode("bigbatch", 400 + batch, 16, lens)
+    s, out, flags = _run(wl, splits=splits)
+    assert flags == 0
+    ref = oracle_decode_paged(wl, oracle_values(wl, oracle_stored(wl)))
+    rel, err, scale = compare(out, ref, BF16_TOL)
+    assert rel <= BF16_TOL, (rel, err, scale)
+    s.close()
+
+
 def test_split_count_does_not_change_the_result():
     wl = W.make_decode("split", 51, 128, [3000, 1500, 64, 1])
     outs = []
