@@ -135,6 +135,8 @@ struct Bars {                               // mbarriers (8 bytes each) and flag
   uint64_t pdone[2];                        // P . C of a tile in P slot b done     (MMA commit)
   uint64_t ofinal;                          // single phase: the last P . C landed  (MMA commit)
   uint64_t qfull;                           // single phase: the absorbed query landed (producer, tx)
+  uint64_t qfree;                           // FP8 MMAs, single phase: the peer has read its query out
+                                            //   of its receive slots (1 remote arrival)
   uint64_t recvfull[kSlots][4];             // peer's partial scores of one lane quarter (32 heads) arrived
                                             //   (1 arrival + 4 KB tx, armed by the receiving warp)
   uint64_t drain[2];                        // every MMA of the QK^T / P . C issuer done
@@ -251,6 +253,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->pdone[i]), 1);
     mbar_init(smem_u32(&bars->ofinal), 1);
     mbar_init(smem_u32(&bars->qfull), 1);
+    mbar_init(smem_u32(&bars->qfree), 1);
     for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->drain[i]), 1);
     bars->abort = 0;
     // the first phase of every receive quarter (tiles 0..3) armed now, so that the cluster barrier
@@ -314,9 +317,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       tma_load_2d(st + 4 * kChunkBytes + kRopeBytes, &tmap_scale, kDc, page * kPage, full);
   };
   // the absorbed query of this CTA (latent half: 4 boxes of 64 columns x 128 heads, 128-byte
-  // swizzle, staged in the still unused receive slots; RoPE half: straight into its 64-byte
-  // swizzled operand slot; heads past n_h read as zeros), then the first tiles of the empty ring
-  const int n_pre = min(n_tiles, kStages);
+  // swizzle; RoPE half: straight into its 64-byte swizzled operand slot; heads past n_h read as
+  // zeros), then the first tiles of the empty ring.  The latent boxes are staged where no copy
+  // can land before they are read.  The peer copies tile j's scores into receive slot j % 4 of
+  // this CTA; it sends tiles 2 and 3 only after it has received this CTA's copies of tiles 0 and
+  // 1, which leave after this CTA's query has been read, so boxes 2-3 wait in slots 2-3.  Boxes
+  // 0-1 wait in ring stage 3, whose tile is requested once they have been read.  With FP8 MMAs
+  // (three smaller stages) all four boxes wait in the receive slots, and the peer sends its first
+  // copies only after this CTA has signalled that it has read them (the qfree barrier).
+  constexpr bool kQStage3 = !kMma8;
+  static_assert(!kQStage3 || L::kStage >= 2 * kMaxHeads * 128, "query boxes 0-1 in one stage");
+  auto q_box = [&](int c) -> uint32_t {   // shared-memory offset of latent query box c
+    return (kQStage3 && c < 2) ? 3 * L::kStage + c * kMaxHeads * 128 : L::kOffRecv + c * kMaxHeads * 128;
+  };
+  const int n_pre = min(n_tiles, kQStage3 ? kStages - 1 : kStages);
   // a test of the bounded waits (stall == 2): CTA 0 of unit 0 never loads its tile 1
   const int withheld = (stall == 2 && unit_idx == 0 && rank == 0 && n_tiles > 1) ? 1 : -1;
   if (warp == kWarpProducer && lane == 0) {
@@ -329,7 +343,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const uint32_t qf = smem_u32(&bars->qfull);
     mbar_arrive_expect_tx(qf, (uint32_t)(4 * kMaxHeads * 128 + kQpeBytes));
     for (int c = 0; c < 4; ++c)
-      tma_load_3d(sbase + L::kOffRecv + c * kMaxHeads * 128, &tmap_q, (int)(rank * 256 + c * 64), 0, b, qf);
+      tma_load_3d(sbase + q_box(c), &tmap_q, (int)(rank * 256 + c * 64), 0, b, qf);
     tma_load_3d(sbase + L::kOffQpe, &tmap_qpe, (int)(kDc + rank * 32), 0, b, qf);
     for (int j = 1; j < n_pre; ++j)
       if (j != withheld) issue_tile(j, pages[j]);
@@ -362,7 +376,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       float amax = 0.0f;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
-        const uint8_t* row = smem + L::kOffRecv + (2 * half + part) * kMaxHeads * 128 + h * 128;
+        const uint8_t* row = smem + q_box(2 * half + part) + h * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint4 x = *reinterpret_cast<const uint4*>(row + ((k ^ (h & 7)) * 16));
@@ -383,7 +397,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       uint8_t* q8row = smem + L::kOffQ8 + half * (kQ8Bytes / 2) + h * 128;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
-        const uint8_t* row = smem + L::kOffRecv + (2 * half + part) * kMaxHeads * 128 + h * 128;
+        const uint8_t* row = smem + q_box(2 * half + part) + h * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {        // 16 codes = 8 bf16 pairs (two 16-byte pieces of the row)
           const uint4 x0 = *reinterpret_cast<const uint4*>(row + (((2 * c) ^ (h & 7)) * 16));
@@ -414,7 +428,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     } else if (landed) {
 #pragma unroll
       for (int part = 0; part < 2; ++part) {      // box 2 half + part: 64 columns = 32 TMEM columns
-        const uint8_t* row = smem + L::kOffRecv + (2 * half + part) * kMaxHeads * 128 + h * 128;
+        const uint8_t* row = smem + q_box(2 * half + part) + h * 128;
         uint32_t r[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -430,6 +444,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // FP8 MMAs: the query has left this CTA's receive slots, so the peer may now copy scores into
+  // them (its group warps wait for this before their first copy)
+  if (!kQStage3 && tid == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&bars->qfree), peer));
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ TMA producer
@@ -445,12 +462,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
           if (kBlock) tma_prefetch_2d(&tmap_scale, kDc, pg * kPage);
         }
       };
+      int issued = n_pre;
+      // the first tile of a stage that held query boxes, now that they have been read
+      for (; issued < min(n_tiles, kStages); ++issued) issue_tile(issued, bt_row[issued]);
       // the next user of each stage into L2, once tile 0 has landed (out of the start-up burst)
       if (n_tiles > kStages && mbar_wait(smem_u32(&bars->full[0]), 0, abort_flag)) {
         for (int j = kStages; j < min(n_tiles, 2 * kStages); ++j) prefetch_tile(bt_row[j]);
       }
-      int issued = n_pre;
-      for (int j = n_pre; j < n_tiles; ++j) {
+      for (int j = issued; j < n_tiles; ++j) {
         const int s = j % kStages;
         const int page = bt_row[j];
         if (j + kStages < n_tiles) prefetch_tile(bt_row[j + kStages]);   // the stage's next tile, into L2
@@ -742,6 +761,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
       const int k = j >> 1, slot = j & (kSlots - 1);
       const int valid = min(kPage, t_end - (unit.page_begin + j) * kPage);
       if (!wait_cta(&bars->sfull[g], k & 1)) { ok = false; break; }
+      // (FP8 MMAs) before this warp's first copy: the peer's query is out of the slots it lands in
+      if (!kQStage3 && k == 0 && !wait_cluster(&bars->qfree, 0)) { ok = false; break; }
       tc_fence_after();
       // x2[i] = scores 2i, 2i + 1 in the log2 domain, as pairs for the packed fp32 ops
       float2 x2[32];
