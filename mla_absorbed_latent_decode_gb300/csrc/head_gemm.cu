@@ -11,7 +11,7 @@
 // The query-absorption launch has one extra CTA that runs the split planner
 // (plan.cuh) while the GEMM CTAs wait for their weights.  Before the
 // up-projection, split sequences' partial latent sums are merged by log-sum-exp
-// into o_lat (a standard identity, not on the pages); invalid sequences, and
+// into the GEMM's operand tile (a standard identity, not on the pages); invalid sequences, and
 // sequences whose block table held a bad page id, get a zero latent, hence a zero
 // output.
 //
@@ -217,9 +217,10 @@ q_absorb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
 }
 
 // out^T[h] = W_UV[h] . o_lat[:, h]^T for the sequences n0 .. n0 + n_pad of this CTA, after
-// merging split sequences' partials of head h into o_lat by log-sum-exp (zero latent for an
-// invalid sequence or one with a bad page id; unsplit sequences already hold theirs).  Eight
-// warps take the merge; warps 0-3 (one per 32 TMEM lanes) run the epilogue.
+// merging split sequences' partials of head h by log-sum-exp straight into the operand tile in
+// shared memory (zero latent for an invalid sequence or one with a bad page id; unsplit
+// sequences' rows come from o_lat, written by the decode).  Eight warps take the merge; warps
+// 0-3 (one per 32 TMEM lanes) run the epilogue.
 constexpr int kUpThreads = 256;
 __global__ void __launch_bounds__(kUpThreads, 1)
 up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_o, int B, int n_h,
@@ -252,36 +253,50 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
       tma_load_2d(a_st + i * kBox, &tm_w, 64 * i, 128 * h, smem_u32(&bars->full[i]));
     }
   }
-  // merge pass: one warp per split, invalid or bad-page sequence of this tile.  The plan
-  // entries of the tile are loaded together first (one per thread), before the dependency wait:
-  // the plan comes from the query-absorption launch, two launches back and complete when this
-  // grid starts; the bad-page flags, written by the decode, after it.  A tile without a split or
-  // invalid sequence loads its latent rows at once (a bad-page sequence's rows are then zeroed in
-  // shared memory).  A split sequence's partial slots are its unit indices first_unit ..
-  // first_unit + nsplit - 1; lane k holds split k's log-sum-exp (32 splits per load, one load
-  // each), and the partials are requested eight splits at a time, the first batch together with
-  // the log-sum-exps, merged with a running maximum: one or two L2 round trips per merge.
+  // The latent rows of the tile's sequences (the B operand, 128-byte-swizzled boxes of 64
+  // columns) are requested by TMA right after the dependency wait, whatever the tile holds; the
+  // rows of split, invalid or bad-page sequences are then overwritten in shared memory, once the
+  // boxes have landed, by the merge pass: one warp per such sequence (zeros for an invalid or
+  // bad-page one).  The plan entries of the tile are loaded together first (one per thread),
+  // before the dependency wait: the plan comes from the query-absorption launch, two launches
+  // back and complete when this grid starts; the bad-page flags, written by the decode, after it.
+  // A split sequence's partial slots are its unit indices first_unit .. first_unit + nsplit - 1;
+  // lane k holds split k's log-sum-exp (32 splits per load, one load each), and the partials are
+  // requested eight splits at a time, the first batch together with the log-sum-exps, merged
+  // with a running maximum: one or two L2 round trips per merge.
   const int n_seq = min(B - n0, n_tile);
   int2 sp = make_int2(0, 0);
   if (tid < n_seq) sp = __ldcg(reinterpret_cast<const int2*>(ws.seqs) + n0 + tid);
   griddep_wait();                          // the latent sums and bad-page flags of the decode
   griddep_launch_dependents();
-  const bool early = __syncthreads_and(tid >= n_seq || sp.y == 1) != 0;
-  if (early && tid == 0)
+  if (tid == 0)
     for (int i = 0; i < 8; ++i) load_rows(b_st + i * b_bytes, &tm_o, 64 * i, h, n0, smem_u32(&bars->full[i]));
   const int bad = tid < n_seq ? ws.bad[n0 + tid] : 0;
   if (tid < n_seq) plan_s[tid] = make_int2(sp.x, bad ? 0 : sp.y);
-  const bool any_bad = __syncthreads_or(bad) != 0;
+  __syncthreads();
+  bool rows_landed = false;                // (this warp has waited for the row boxes)
+  auto wait_rows = [&]() {
+    if (rows_landed) return;
+    rows_landed = true;
+    bool landed = true;
+    for (int i = 0; i < 8; ++i) landed = mbar_wait(smem_u32(&bars->full[i]), 0, abort_flag) && landed;
+    if (!landed && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
+  };
+  // lane l's 16 values [16 l, 16 l + 16) of row j: box l / 4, 16-byte chunks 2 (l % 4) and
+  // 2 (l % 4) + 1, each at its swizzled place (chunk c of row j at c ^ (j % 8))
+  auto row_chunk = [&](int j, int c) -> uint4* {
+    return reinterpret_cast<uint4*>(smem + 8 * kBox + (lane >> 2) * b_bytes + j * 128 + ((c ^ (j & 7)) * 16));
+  };
   bool wrote = false;
-  for (int j = warp; j < n_seq && !early; j += kUpThreads / 32) {
-    const int b = n0 + j;
+  for (int j = warp; j < n_seq; j += kUpThreads / 32) {
     const int first = plan_s[j].x, nsplit = plan_s[j].y;
     if (nsplit == 1) continue;
     wrote = true;
-    uint4* dst = reinterpret_cast<uint4*>(ws.o_lat + ((size_t)b * n_h + h) * kDc) + 2 * lane;   // 16 values
+    const int c0 = 2 * (lane & 3);
     if (nsplit == 0) {
-      dst[0] = make_uint4(0, 0, 0, 0);
-      dst[1] = make_uint4(0, 0, 0, 0);
+      wait_rows();
+      *row_chunk(j, c0) = make_uint4(0, 0, 0, 0);
+      *row_chunk(j, c0 + 1) = make_uint4(0, 0, 0, 0);
       continue;
     }
     const float* lse = ws.part_lse + (size_t)first * n_h + h;
@@ -331,28 +346,16 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
     uint32_t o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = bf16x2_bits(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    wait_rows();                            // the TMA rows landed: this row may now be replaced
+    *row_chunk(j, c0) = make_uint4(o[0], o[1], o[2], o[3]);
+    *row_chunk(j, c0 + 1) = make_uint4(o[4], o[5], o[6], o[7]);
   }
-  if (early && any_bad) {
-    // rows of bad-page sequences, loaded before the flags were read, become zeros in the tile
-    bool landed = true;
-    for (int i = 0; i < 8; ++i) landed = mbar_wait(smem_u32(&bars->full[i]), 0, abort_flag) && landed;
-    if (!landed && atomicExch(&bars->abort, 1) == 0) atomicOr(check, kCheckTimeout);
-    for (int x = tid; x < n_seq * 8 * 8; x += kUpThreads) {   // (sequence, box, 16-byte piece)
-      const int j = x >> 6, i = (x >> 3) & 7, q = x & 7;
-      if (plan_s[j].y == 0) *reinterpret_cast<uint4*>(smem + 8 * kBox + i * b_bytes + j * 128 + q * 16) = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
-  }
-  if (wrote) fence_proxy_async_global();       // these rows are read below by TMA (async proxy)
+  if (wrote) fence_proxy_async_smem();     // these rows are read below by the tensor core
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   if (tid == 0) {
-    if (!early)
-      for (int i = 0; i < 8; ++i) load_rows(b_st + i * b_bytes, &tm_o, 64 * i, h, n0, smem_u32(&bars->full[i]));
     const uint32_t idesc = idesc_bf16_f32(128, n_here, false, false);
     const uint64_t a0 = sdesc_sw128(a_st, 16, 1024), b0 = sdesc_sw128(b_st, 16, 1024);
     bool ok = true;
