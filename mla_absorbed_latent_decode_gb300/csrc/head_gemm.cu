@@ -234,7 +234,9 @@ up_project_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constan
   volatile int* abort_flag = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, n0 = blockIdx.z * n_tile;
-  const int n_here = min(n_pad, n_tile);               // the TMA box height (rows past B arrive as zeros)
+  // the TMA box height = the MMA's N, at least 16 (rows past B arrive as zeros; with a tile of 8
+  // sequences the next tile's rows come along and their results are dropped)
+  const int n_here = max(16, min(n_pad, n_tile));
   const uint32_t b_bytes = (uint32_t)n_here * 128;
   if (tid == 0) {
     for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars->full[i]), 1);
@@ -488,11 +490,12 @@ cudaError_t launch_combine_uv(const Handle& h, int batch, const Workspace& ws, _
     attr = true;
   }
   const int n_pad = ((batch + 15) / 16) * 16;
-  // the largest tile of 64 / 32 / 16 sequences that still gives half the SMs a CTA (else 16)
+  // the largest tile of 64 / 32 / 16 / 8 sequences that still gives half the SMs a CTA (else 8):
+  // with few heads, small tiles spread the split merges (one warp per sequence) over more CTAs
   int n_tile = kUpN;
-  while (n_tile > 16 && (long long)h.cfg.n_h * ((batch + n_tile - 1) / n_tile) < h.num_sms / 2) n_tile /= 2;
+  while (n_tile > 8 && (long long)h.cfg.n_h * ((batch + n_tile - 1) / n_tile) < h.num_sms / 2) n_tile /= 2;
   alignas(64) CUtensorMap to;
-  cudaError_t e = rows_map(ws.o_lat, batch, h.cfg.n_h, kDc, min(n_pad, n_tile), &to);
+  cudaError_t e = rows_map(ws.o_lat, batch, h.cfg.n_h, kDc, max(16, min(n_pad, n_tile)), &to);
   if (e != cudaSuccess) return e;
   dim3 grid(h.cfg.n_h, 1, (batch + n_tile - 1) / n_tile);
   return launch_pdl(up_project_kernel, grid, dim3(kUpThreads), kUpSmem, st,
