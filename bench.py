@@ -196,6 +196,18 @@ def oracle_sample(wl, seconds):
                            f"({done_tokens} tokens), fp64 absorbed path, {elapsed:.1f} s")
 
 
+def arithmetic_note(wl):
+    """What the decode computes in, for the JSON line's config."""
+    if cache_name(wl) == "fp8_e4m3":
+        ops = ("e4m3 MMA operands (the cached codes as stored, the absorbed query quantised per head and "
+               "half, P in e4m3; the RoPE part in bf16)")
+    elif cache_name(wl) == "fp8_e4m3_block":
+        ops = "bf16 MMA operands (the per-block e4m3 cache decoded to bf16 in shared memory)"
+    else:
+        ops = "bf16 MMA operands"
+    return ops + ", fp32 accumulation and softmax, fp16 partial scores between the CTA pair"
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -227,8 +239,9 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(us_equiv / 1000.0, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "s_ctx": wl.max_ctx, "n_h": wl.n_h,
-                   "cache": cache_name(wl),
+        "config": {"workload": wl.name, "B": wl.B, "s_ctx": wl.max_ctx, "n_h": wl.n_h, "d_c": wl.d_c,
+                   "d_rope": wl.d_rope, "cache": cache_name(wl), "total_tokens": wl.total_tokens,
+                   "parallelism": "replicas x1 (rank 0 only)",
                    "note": "ms_per_step extrapolated from the sampled throughput to the whole batch"},
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s (latent KV)", "cores": blas_threads(), "kind": "oracle",
                          "sample": desc},
@@ -599,7 +612,7 @@ def run_ours(args):
                              "note": "the same step captured once in a CUDA graph and replayed, L2 flushed "
                                      "between replays; not the headline"},
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
+            "dtype": "e4m3" if cache_name(wl) == "fp8_e4m3" else "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "s_ctx": wl.max_ctx, "n_h": wl.n_h, "d_c": wl.d_c,
                        "d_rope": wl.d_rope, "cache": cache_name(wl),
                        "total_tokens": wl.total_tokens,
@@ -608,8 +621,7 @@ def run_ours(args):
                              f"cache read per step ({wl.total_tokens * cache_bytes_per_token(wl) >> 20} MiB) also exceeds L2",
                        "timing": "value from K steps without per-kernel events; per_kernel_us and roofline "
                                  "from a second K-step pass with per-kernel events (which serialise the kernels)",
-                       "arithmetic": "bf16 MMA operands (an FP8 cache is converted to bf16 in shared memory), "
-                                     "fp32 accumulation and softmax, fp16 partial scores between the CTA pair",
+                       "arithmetic": arithmetic_note(wl),
                        "parallelism": f"replicas x{world}"},
             "per_kernel_us": per_kernel,
             "roofline": {"bound": "hbm", "kernel": "mla_decode_splitkv", "achieved": round(achieved, 1),
