@@ -112,6 +112,31 @@ def test_large_batches_match_oracle(batch, splits):
     s.close()
 
 
+@pytest.mark.parametrize("n_h,batch", [(16, 13), (32, 20)])
+def test_small_head_up_projection_tiles(n_h, batch):
+    """With few heads the up-projection takes tiles of 8 sequences (its MMA still multiplies 16
+    rows and drops the next tile's); the last tile is partial.  Forced splits route every
+    sequence of more than one page through the merge, and a bad page zeroes one sequence of a
+    later tile."""
+    lens = np.random.default_rng(batch).integers(1, 700, size=batch).tolist()
+    wl = W.make_decode("uptiles", 500 + n_h + batch, n_h, lens)
+    s, out, flags = _run(wl, splits=3)
+    assert flags == 0
+    ref = oracle_decode_paged(wl, oracle_values(wl, oracle_stored(wl)))
+    rel, err, scale = compare(out, ref, BF16_TOL)
+    assert rel <= BF16_TOL, (rel, err, scale)
+    bt = s.block_table.clone()
+    victim = batch - 2
+    bt[victim, 0] = wl.num_pages + 3
+    s.mla.decode(s.q, s.ctx_len, wl.max_ctx, bt, s.cache, wl.num_pages, s.workspace, s.out)
+    out2 = bf16_out_to_f64(s.out)
+    assert s.status() == B.MLA_CHECK_PAGE_ID
+    assert np.all(out2[victim] == 0)
+    keep = [i for i in range(batch) if i != victim]
+    assert np.array_equal(out2[keep], out[keep])
+    s.close()
+
+
 def test_split_count_does_not_change_the_result():
     wl = W.make_decode("split", 51, 128, [3000, 1500, 64, 1])
     outs = []
