@@ -344,7 +344,7 @@ mla_status_t mla_decode(mla_handle_t h, const void* q, const int32_t* ctx_len, i
  *
  *   - A batch whose mla_decode_workspace_size exceeds MLA_FIXED_SCRATCH_BYTES
  *     fails with MLA_ERR_WORKSPACE before anything is enqueued (on a 152-SM GB300
- *     up to 25 sequences fit at 128 heads, up to 458 at 16 heads).
+ *     up to 25 sequences fit at 128 heads, up to 422 at 16 heads).
  *   - The handle's device must be current (else MLA_ERR_INVALID_ARG).
  *   - Every call writes the scratch before reading it; it never needs clearing.
  *   - All calls on one device share the array, whatever the handle or stream:
@@ -397,6 +397,13 @@ mla_status_t mla_get_status(mla_handle_t h, mla_stream_t stream, uint32_t* devic
                                converted to bf16 in shared memory and both contractions run in bf16.
                                The two differ by the e4m3 rounding of q and P (within the FP8
                                tolerance of the tests).  No effect on other caches. */
+#define MLA_OPT_SMALL_HEADS 5 /* bf16 cache with n_h <= 32: value 1 runs the decode with heads on the
+                               MMAs' N dimension, one CTA per work unit ("G5 MLA KV 访存建模设计规格"
+                               附录 B's streamed decode; V2-Lite has 16 heads): no partial-score exchange
+                               between two CTAs, and the 128-head layout's idle MMA rows are gone.
+                               Value 0 (the default): the 128-row layout for every shape.  The
+                               results differ by fp32 rounding only.  No effect on other shapes or
+                               caches.  A workspace sized by mla_decode_workspace_size serves both. */
 
 mla_status_t mla_set_option(mla_handle_t h, int32_t option, int64_t value);
 

@@ -35,6 +35,7 @@ MLA_OPT_SPLITS = 1
 MLA_OPT_PROFILE = 2
 MLA_OPT_TEST_STALL = 3
 MLA_OPT_FP8_MMA = 4
+MLA_OPT_SMALL_HEADS = 5
 
 MLA_FIXED_SCRATCH_BYTES = 32 << 20     # include/mla.h: scratch of mla_decode_fixed_scratch
 

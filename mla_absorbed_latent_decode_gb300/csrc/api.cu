@@ -101,7 +101,10 @@ long long decode_unit_bound(const Handle& h, int batch, int max_ctx) {
   // has pages, at most ceil(max_ctx / 64) each.  The decode grid is sized by this bound, so a
   // small step (one short sequence) launches one CTA pair, not one per SM pair.
   const long long by_pages = (long long)batch * ((max_ctx + kPage - 1) / kPage);
-  const long long by_plan = (long long)batch * (h.force_splits > 0 ? h.force_splits : 1) + h.num_pairs;
+  // (a handle whose decode may run one CTA per unit plans a wave of num_sms units: sized for it
+  // whatever MLA_OPT_SMALL_HEADS is set to when the workspace is sized)
+  const int wave = (h.cfg.n_h <= kShMaxHeads && h.cfg.cache_dtype == MLA_CACHE_BF16) ? h.num_sms : h.num_pairs;
+  const long long by_plan = (long long)batch * (h.force_splits > 0 ? h.force_splits : 1) + wave;
   return std::min<long long>(by_plan, std::max<long long>(1, by_pages));
 }
 
@@ -194,6 +197,7 @@ mla_status_t mla_create(const mla_config_t* cfg, const void* w_uk, const void* w
   h->num_sms = sms;
   h->num_pairs = sms / 2;
   h->fp8_mma = 1;                           // MLA_OPT_FP8_MMA default
+  h->small_heads = 0;                       // MLA_OPT_SMALL_HEADS default
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   auto cleanup = [&](mla_status_t err) { mla_destroy(reinterpret_cast<mla_handle_t>(h)); return err; };
@@ -507,8 +511,10 @@ mla_status_t mla_decode(mla_handle_t hh, const void* q, const int32_t* ctx_len, 
       cudaSuccess)
     return cuda_fail(e, "q_absorb launch");
   mark();
-  if ((e = mla::launch_decode(*h, ctx_len, batch, block_table, bt_stride, cache, num_pages, ws, st)) != cudaSuccess)
-    return cuda_fail(e, "decode launch");
+  e = mla::small_head_decode(*h)
+          ? mla::launch_decode_small_heads(*h, ctx_len, batch, block_table, bt_stride, cache, num_pages, ws, st)
+          : mla::launch_decode(*h, ctx_len, batch, block_table, bt_stride, cache, num_pages, ws, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   mark();
   if ((e = mla::launch_combine_uv(*h, batch, ws, static_cast<__nv_bfloat16*>(out), st)) != cudaSuccess)
     return cuda_fail(e, "combine_uv launch");
@@ -557,6 +563,11 @@ mla_status_t mla_set_option(mla_handle_t hh, int32_t option, int64_t value) {
     case MLA_OPT_FP8_MMA:
       if (value < 0 || value > 1) return fail(MLA_ERR_INVALID_ARG, "MLA_OPT_FP8_MMA = %lld is not 0 or 1", (long long)value);
       h->fp8_mma = (int)value;
+      return MLA_OK;
+    case MLA_OPT_SMALL_HEADS:
+      if (value < 0 || value > 1)
+        return fail(MLA_ERR_INVALID_ARG, "MLA_OPT_SMALL_HEADS = %lld is not 0 or 1", (long long)value);
+      h->small_heads = (int)value;
       return MLA_OK;
   }
   return fail(MLA_ERR_INVALID_ARG, "mla_set_option: unknown option %d", option);

@@ -478,7 +478,7 @@ cudaError_t launch_q_absorb(const Handle& h, const __nv_bfloat16* q, const int32
   dim3 grid(h.cfg.n_h + 1, 1, (batch + kQaM - 1) / kQaM);     // + 1: the planner CTA
   return launch_pdl(q_absorb_kernel, grid, dim3(kThreads), kQaSmem, st,
                     *reinterpret_cast<const CUtensorMap*>(h.tmap_wuk), tq, tout, batch, h.cfg.n_h, max_ctx, q, ctx_len,
-                    (const float2*)h.rope_cs, h.cfg.max_position, h.num_pairs, h.force_splits, h.test_stall, ws,
+                    (const float2*)h.rope_cs, h.cfg.max_position, decode_wave(h), h.force_splits, h.test_stall, ws,
                     h.check_word);
 }
 

@@ -67,6 +67,7 @@ struct Handle {
   int profile;              // MLA_OPT_PROFILE
   int test_stall;           // MLA_OPT_TEST_STALL
   int fp8_mma;              // MLA_OPT_FP8_MMA
+  int small_heads;          // MLA_OPT_SMALL_HEADS
   cudaEvent_t ev[8];
   int n_ev_recorded;
   int prof_prefill;         // the last profiled call was mla_prefill (else mla_decode)
@@ -124,6 +125,14 @@ cudaError_t launch_kv_append(const Handle& h, const __nv_bfloat16* rows, const i
 // Query absorption; one extra CTA of the same launch runs the split planner.
 cudaError_t launch_q_absorb(const Handle& h, const __nv_bfloat16* q, const int32_t* ctx_len,
                             int batch, int max_ctx, const Workspace& ws, cudaStream_t st);
+// The decode for few heads (decode_sh.cu): a bf16 cache and n_h <= kShMaxHeads, one CTA per
+// work unit (so the planner's one wave is num_sms units, not num_pairs).
+constexpr int kShMaxHeads = 32;
+bool small_head_decode(const Handle& h);
+inline int decode_wave(const Handle& h) { return small_head_decode(h) ? h.num_sms : h.num_pairs; }
+cudaError_t launch_decode_small_heads(const Handle& h, const int32_t* ctx_len, int batch, const int32_t* block_table,
+                                      int bt_stride, const void* cache, int num_pages, const Workspace& ws,
+                                      cudaStream_t st);
 cudaError_t launch_decode(const Handle& h, const int32_t* ctx_len, int batch,
                           const int32_t* block_table, int bt_stride, const void* cache,
                           int num_pages, const Workspace& ws, cudaStream_t st);

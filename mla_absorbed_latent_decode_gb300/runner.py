@@ -23,7 +23,7 @@ def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
 
 class DecodeSession:
     def __init__(self, wl: Workload, device: str = "cuda", max_position: int | None = None,
-                 splits: int = 0, stream=None, fp8_mma: bool | None = None):
+                 splits: int = 0, stream=None, fp8_mma: bool | None = None, small_heads: bool | None = None):
         self.wl = wl
         self.device = torch.device(device)
         self.stream = stream
@@ -38,6 +38,8 @@ class DecodeSession:
             self.mla.set_option(B.MLA_OPT_SPLITS, splits)
         if fp8_mma is not None:                 # None: the library's default (FP8 MMAs)
             self.mla.set_option(B.MLA_OPT_FP8_MMA, int(fp8_mma))
+        if small_heads is not None:             # None: the library's default
+            self.mla.set_option(B.MLA_OPT_SMALL_HEADS, int(small_heads))
         row_bytes = ROW_BYTES[wl.cache_dtype]
         self.cache = torch.full((wl.num_pages, wl.page_size, row_bytes), SENTINEL, dtype=torch.uint8,
                                 device=self.device)

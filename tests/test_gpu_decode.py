@@ -78,19 +78,27 @@ def plan_reference(ctx_len, max_ctx, num_pairs, forced=0):
     return units, seqs
 
 
+@pytest.mark.parametrize("small_heads", [False, True])
 @pytest.mark.parametrize("forced", [0, 3])
-def test_plan_is_bit_exact(forced):
+def test_plan_is_bit_exact(forced, small_heads):
+    """The work list against the rule restated.  A wave is one unit per SM pair, or per SM when
+    the decode runs one CTA per unit (MLA_OPT_SMALL_HEADS); a bf16 handle of at most 32 heads
+    sizes its workspace for the SM wave either way."""
     ctx = [1, 4096, 65, 700, 3000, 64, 129, 2048] * 4
     wl = W.make_decode("plan", 41, 16, ctx)
-    s, _, _ = _run(wl, splits=forced)
-    num_pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
-    max_units = wl.B * max(1, forced) + num_pairs
+    s = DecodeSession(wl, splits=forced, small_heads=small_heads)
+    s.append_rows()
+    s.decode()
+    assert s.status() == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    wave = sms if small_heads else sms // 2
+    max_units = wl.B * max(1, forced) + sms
     off = _workspace_layout(wl.B, wl.n_h, max_units)
     ws = s.workspace.cpu().numpy()
     n_units = int(ws[off["counters"]:off["counters"] + 4].view(np.int32)[0])
     units = ws[off["units"]:off["units"] + 16 * n_units].view(np.int32).reshape(-1, 4)
     seqs = ws[off["seqs"]:off["seqs"] + 8 * wl.B].view(np.int32).reshape(-1, 2)
-    ref_units, ref_seqs = plan_reference(wl.ctx_len.tolist(), wl.max_ctx, num_pairs, forced)
+    ref_units, ref_seqs = plan_reference(wl.ctx_len.tolist(), wl.max_ctx, wave, forced)
     assert n_units == len(ref_units)
     assert [tuple(u) for u in units.tolist()] == ref_units
     assert [tuple(x) for x in seqs.tolist()] == ref_seqs
